@@ -1,0 +1,506 @@
+/*
+ * eagle_oracle.c - CPU oracle of one EAGLE / EAGLE-2 dynamic draft-tree step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file restates the method as plain, slow loops so that a
+ * reader can check it against the pages by eye.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load it; the product (the CUDA library) never does, and the two
+ * share no code, header, table or helper.  The only thing both sides consume is the seeded
+ * input generator, which holds none of the method's arithmetic.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [notes04]  "EAGLE 推测解码为什么比 Medusa 快？（含 EAGLE-2 动态草稿树）"
+ *              (zzszmyf.github.io speculative-decoding notes, chapter 04)
+ *   [tomjerr]  "(EAGLE 1) EAGLE: Speculative Sampling Requires Rethinking Feature Uncertainty"
+ *              (tom-jerr.github.io paper reading)
+ *   [zdszero]  Medusa -> EAGLE -> EAGLE-2 notes (zdszero.github.io, spec_medusa_eagle), with its
+ *              sections "draft 结构", "EAGLE-2：树的形状应该跟着上下文变" and "在 SGLang 里"
+ *   [jsqmd]    "投机解码：从eagle1到dflash" (jsqmd.com), section "二、EAGLE-2"
+ *
+ * Arithmetic contract (the pages fix none; these are the readings the test suite relies on):
+ *   - every dot product accumulates in fp32, terms added in ascending index order, each product
+ *     rounded to fp32 before its add (the file is built with -ffp-contract=off, so no host fuses
+ *     them into an FMA);
+ *   - bf16 inputs are widened exactly to fp32 (a bf16 is the upper half of a binary32);
+ *   - for bf16 configurations the FC output is rounded once to bf16, round-to-nearest-even;
+ *   - path scores are kept as fp32 logs, S(child) = fl(S(parent) + logp(child)): a monotone
+ *     restatement of the product of confidences in [notes04] §10.3;
+ *   - every ranking breaks ties toward the lowest index (token id, or candidate id, which is
+ *     level-major so a shallower node wins a tie, as [notes04] §10.3 property 2 asks).
+ *
+ * Parity status of each function: pinned by tests/test_oracle_*.py (see the header of each
+ * function for its pin).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_ERR_ARG 1
+#define ORC_ERR_TREE 2  /* a kept node's parent was not kept: the connectivity property failed */
+#define ORC_ERR_NOMEM 3
+
+/* ------------------------------------------------------------------------------------------ */
+/* Number formats                                                                             */
+/* ------------------------------------------------------------------------------------------ */
+
+/* A bf16 value is the upper 16 bits of an IEEE-754 binary32; widening is exact. */
+float orc_bf16_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round a binary32 to bf16, to nearest, ties to even.  NaN stays a (quiet) NaN.
+ * Pin: equals torch's float32 -> bfloat16 conversion on every tested bit pattern. */
+uint16_t orc_f32_to_bf16(float x) {
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+static float load_elem(const void *p, int32_t is_bf16, int64_t i) {
+    return is_bf16 ? orc_bf16_to_f32(((const uint16_t *)p)[i]) : ((const float *)p)[i];
+}
+
+int32_t orc_num_threads(void) {
+#ifdef _OPENMP
+    return (int32_t)omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void orc_set_num_threads(int32_t n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* One draft row: FC then LM head                                                             */
+/* ------------------------------------------------------------------------------------------ */
+
+/* [notes04] §4.1 and [zdszero] "draft 结构": the draft input is the concatenation
+ * [f || e(t)] in R^{2h} of a feature and the embedding of the (shifted) next token; an FC
+ * (2h -> h, with bias) maps it back to h.  The decoder layer that follows the FC on the pages
+ * is taken as the identity here (spec scope: FC then LM head).
+ *   w_fc : [h][2h] row-major; columns 0..h-1 act on the feature, h..2h-1 on e(t)
+ *   b_fc : [h] or NULL
+ *   feat : [h] fp32 (already widened)
+ *   emb  : [V][h] embedding table; row `tok` is e(t)
+ *   fhat : [h] out, fp32 (holding a bf16 value when is_bf16)
+ * Pin: float64 matrix product of the same widened inputs, within the fp32 dot-product bound. */
+void orc_fc_row(int32_t h, int32_t is_bf16, const void *w_fc, const void *b_fc,
+                const float *feat, const void *emb, int32_t tok, float *fhat) {
+#pragma omp parallel for schedule(static)
+    for (int32_t o = 0; o < h; ++o) {
+        float acc = 0.0f;
+        for (int32_t i = 0; i < 2 * h; ++i) {
+            float x = (i < h) ? feat[i] : load_elem(emb, is_bf16, (int64_t)tok * h + (i - h));
+            float w = load_elem(w_fc, is_bf16, (int64_t)o * 2 * h + i);
+            acc = acc + w * x;
+        }
+        if (b_fc) acc = acc + load_elem(b_fc, is_bf16, o);
+        fhat[o] = is_bf16 ? orc_bf16_to_f32(orc_f32_to_bf16(acc)) : acc;
+    }
+}
+
+/* [notes04] §4.1-§4.2 and [zdszero] "draft 结构": the draft distribution comes from the
+ * target's own frozen LM head, z = W_lm f^ (no bias, no norm in front of it).
+ *   w_lm : [V][h] row-major;  z : [V] out.
+ * Pin: float64 matrix product, within the fp32 dot-product bound. */
+void orc_lm_head_row(int32_t h, int32_t V, int32_t is_bf16, const void *w_lm,
+                     const float *fhat, float *z) {
+#pragma omp parallel for schedule(static)
+    for (int32_t v = 0; v < V; ++v) {
+        float acc = 0.0f;
+        for (int32_t i = 0; i < h; ++i)
+            acc = acc + load_elem(w_lm, is_bf16, (int64_t)v * h + i) * fhat[i];
+        z[v] = acc;
+    }
+}
+
+/* True when (za, a) ranks strictly before (zb, b) in the order (value descending, index
+ * ascending). */
+static int ranks_before(float za, int32_t a, float zb, int32_t b) {
+    return za > zb || (za == zb && a < b);
+}
+
+/* [notes04] §10.2 (the confidence of a drafted token is its draft probability) and §10.3
+ * (each expanded node keeps its top-k children): per-row log-softmax and top-k.
+ *   lse  = M + log(sum_v exp(z_v - M)),  M = max_v z_v   (sum in ascending v, fp32)
+ *   ids  = the k best v by (z descending, v ascending)
+ *   logp = z[ids] - lse
+ * The j-th pick is the best element that ranks after pick j-1.
+ * Pin: float64 logsumexp, and a full sort of the row by (-z, v). */
+void orc_log_softmax_topk(int32_t V, int32_t k, const float *z, int32_t *ids, float *logp,
+                          float *lse_out) {
+    float M = z[0];
+    for (int32_t v = 1; v < V; ++v)
+        if (z[v] > M) M = z[v];
+    float S = 0.0f;
+    for (int32_t v = 0; v < V; ++v) S = S + expf(z[v] - M);
+    float lse = M + logf(S);
+
+    int32_t prev = -1;
+    for (int32_t j = 0; j < k; ++j) {
+        int32_t best = -1;
+        for (int32_t v = 0; v < V; ++v) {
+            if (prev >= 0 && !ranks_before(z[prev], prev, z[v], v)) continue; /* already taken */
+            if (best < 0 || ranks_before(z[v], v, z[best], best)) best = v;
+        }
+        ids[j] = best;
+        logp[j] = z[best] - lse;
+        prev = best;
+    }
+    if (lse_out) *lse_out = lse;
+}
+
+/* Top-n of `count` scored items by (score descending, id ascending), where item i has id
+ * ids[i].  Writes positions (0..count-1) into `out` in rank order.  Same pick-after-previous
+ * rule as above. */
+static void select_top(int32_t count, const float *score, const int32_t *ids, int32_t n,
+                       int32_t *out) {
+    int32_t prev = -1;
+    for (int32_t j = 0; j < n; ++j) {
+        int32_t best = -1;
+        for (int32_t i = 0; i < count; ++i) {
+            if (prev >= 0 && !ranks_before(score[prev], ids[prev], score[i], ids[i])) continue;
+            if (best < 0 || ranks_before(score[i], ids[i], score[best], ids[best])) best = i;
+        }
+        out[j] = best;
+        prev = best;
+    }
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* The draft-tree step                                                                        */
+/* ------------------------------------------------------------------------------------------ */
+
+typedef struct {
+    int32_t batch;    /* B: independent requests */
+    int32_t hidden;   /* h */
+    int32_t vocab;    /* V */
+    int32_t depth;    /* d: drafted levels = draft forwards ([zdszero] "在 SGLang 里": steps) */
+    int32_t topk;     /* k: children per expanded node, frontier width */
+    int32_t num_keep; /* m: drafted nodes kept by the rerank (the tree has m+1 with the root) */
+    int32_t is_bf16;  /* weights, embedding and features are bf16 (else fp32) */
+} orc_dims;
+
+/* Candidates one request contributes to the rerank pool: the k children of the root, then
+ * k*k for every further level ([zdszero] "在 SGLang 里": each level's top-k of k^2). */
+int32_t orc_num_candidates(int32_t depth, int32_t k) { return k + (depth - 1) * k * k; }
+
+/* Tree depth of candidate c (1 = child of the root).  Candidate ids are level-major:
+ * 0..k-1 at depth 1, then k^2 per depth. */
+static int32_t cand_depth(int32_t c, int32_t k) { return c < k ? 1 : 2 + (c - k) / (k * k); }
+
+/*
+ * One full draft-tree step for a batch of independent requests.
+ *
+ * Per request b ([notes04] §6.1 feature-level drafting, §10.3 expand + rerank; [zdszero]
+ * "EAGLE-2" and "在 SGLang 里"; [jsqmd] "二、EAGLE-2" steps ① ②):
+ *   level 0 : row x = [f_b || e(root_b)] -> f^ -> z -> top-k.  Its k children become
+ *             candidates 0..k-1 with S = logp; the frontier is all k, in that order.
+ *   level l : (l = 1..d-1) for frontier slot s (in frontier order) the row is
+ *             x = [f^ of the row that produced the slot's node || e(token of that node)];
+ *             child j becomes candidate k + (l-1)k^2 + s*k + j with
+ *             S = fl(S_slot + logp_j); the next frontier (needed while l < d-1) is the top-k
+ *             of these k^2 by (S desc, candidate asc).
+ *   rerank  : the top-m of all candidates by (S desc, candidate asc).
+ *   build   : tree index 0 is the root (position pos_base, parent -1, S = 0); the kept
+ *             candidates in ascending candidate order take indices 1..m; parent = tree index
+ *             of the parent candidate (0 for depth 1); position = depth + pos_base;
+ *             mask bit j of row i is set iff j is i or an ancestor of i
+ *             ([notes04] §12.5: ancestor-only mask, positions shared per level).
+ *
+ * Rows of level 0 are numbered b; rows of level l >= 1 are numbered b*k + s.
+ * All per-row outputs are optional (NULL skips them); arrays are [depth][B*k][...], rows of
+ * level 0 beyond B are left untouched.
+ *   row_fhat [d][R][h], row_z [d][R][V], row_lse [d][R], row_ids/row_logp [d][R][k]
+ *   front_cand [d][B][k] : candidate in each frontier slot entering level l (-1 at level 0)
+ *   cand_tok/cand_S/cand_parent/cand_row [B][n_cand] : the rerank pool; cand_row is the row
+ *             (within its producing level) whose f^ is the candidate's input feature
+ *   tree_tok/tree_parent/tree_pos/tree_S/tree_cand [B][m+1], tree_mask [B][m+1][W],
+ *             W = ceil((m+1)/32), bits packed LSB-first per 32-bit word
+ *   node_z [B][m+1][V] : draft logits of every tree node's own row (the row that would expand
+ *             it), used to synthesise target logits; optional.
+ * Returns ORC_OK, ORC_ERR_ARG, ORC_ERR_TREE or ORC_ERR_NOMEM.
+ */
+int32_t orc_draft_tree(const orc_dims *dm, const void *w_fc, const void *b_fc, const void *w_lm,
+                       const void *emb, const void *root_feat, const int32_t *root_tok,
+                       const int32_t *pos_base, float *row_fhat, float *row_z, float *row_lse,
+                       int32_t *row_ids, float *row_logp, int32_t *front_cand, int32_t *cand_tok,
+                       float *cand_S, int32_t *cand_parent, int32_t *cand_row, int32_t *tree_tok,
+                       int32_t *tree_parent, int32_t *tree_pos, uint32_t *tree_mask,
+                       float *tree_S, int32_t *tree_cand, float *node_z) {
+    const int32_t B = dm->batch, h = dm->hidden, V = dm->vocab, d = dm->depth, k = dm->topk;
+    const int32_t m = dm->num_keep, bf = dm->is_bf16;
+    if (B < 0 || h < 1 || V < 1 || d < 1 || k < 1 || k > V) return ORC_ERR_ARG;
+    const int32_t n_cand = orc_num_candidates(d, k);
+    if (m < 0 || m > n_cand) return ORC_ERR_ARG;
+    if (!w_fc || !w_lm || !emb || !root_feat || !root_tok) return ORC_ERR_ARG;
+    if (B == 0) return ORC_OK;
+
+    const int64_t R = (int64_t)B * k;
+    const int32_t n_nodes = m + 1;
+    const int32_t W = (n_nodes + 31) / 32;
+
+    /* scratch: f^ of every row of every level, one logit row, per-request pool and frontier */
+    float *fh = (float *)malloc(sizeof(float) * (size_t)d * (size_t)R * (size_t)h);
+    float *z = (float *)malloc(sizeof(float) * (size_t)V);
+    float *feat = (float *)malloc(sizeof(float) * (size_t)h);
+    float *x_fhat = (float *)malloc(sizeof(float) * (size_t)h);
+    int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)k);
+    float *logp = (float *)malloc(sizeof(float) * (size_t)k);
+    int32_t *p_tok = (int32_t *)malloc(sizeof(int32_t) * (size_t)n_cand);
+    float *p_S = (float *)malloc(sizeof(float) * (size_t)n_cand);
+    int32_t *p_par = (int32_t *)malloc(sizeof(int32_t) * (size_t)n_cand);
+    int32_t *p_row = (int32_t *)malloc(sizeof(int32_t) * (size_t)n_cand);
+    int32_t *p_id = (int32_t *)malloc(sizeof(int32_t) * (size_t)n_cand);
+    int32_t *f_cand = (int32_t *)malloc(sizeof(int32_t) * (size_t)k);
+    float *f_S = (float *)malloc(sizeof(float) * (size_t)k);
+    int32_t *pick = (int32_t *)malloc(sizeof(int32_t) * (size_t)n_cand);
+    int32_t *tree_of_cand = (int32_t *)malloc(sizeof(int32_t) * (size_t)n_cand);
+    int32_t *t_par = (int32_t *)malloc(sizeof(int32_t) * (size_t)n_nodes);
+    int32_t *t_cand = (int32_t *)malloc(sizeof(int32_t) * (size_t)n_nodes);
+    int32_t rc = ORC_OK;
+    if (!fh || !z || !feat || !x_fhat || !ids || !logp || !p_tok || !p_S || !p_par || !p_row ||
+        !p_id || !f_cand || !f_S || !pick || !tree_of_cand || !t_par || !t_cand) {
+        rc = ORC_ERR_NOMEM;
+        goto done;
+    }
+
+    for (int32_t b = 0; b < B; ++b) {
+        /* ---------------- level 0: the root's row ---------------- */
+        for (int32_t i = 0; i < h; ++i) feat[i] = load_elem(root_feat, bf, (int64_t)b * h + i);
+        {
+            const int64_t r = b;
+            float *fo = fh + ((int64_t)0 * R + r) * h;
+            orc_fc_row(h, bf, w_fc, b_fc, feat, emb, root_tok[b], fo);
+            orc_lm_head_row(h, V, bf, w_lm, fo, z);
+            float lse;
+            orc_log_softmax_topk(V, k, z, ids, logp, &lse);
+            if (row_fhat) memcpy(row_fhat + ((int64_t)0 * R + r) * h, fo, sizeof(float) * h);
+            if (row_z) memcpy(row_z + ((int64_t)0 * R + r) * V, z, sizeof(float) * V);
+            if (row_lse) row_lse[(int64_t)0 * R + r] = lse;
+            if (row_ids) memcpy(row_ids + ((int64_t)0 * R + r) * k, ids, sizeof(int32_t) * k);
+            if (row_logp) memcpy(row_logp + ((int64_t)0 * R + r) * k, logp, sizeof(float) * k);
+            if (front_cand)
+                for (int32_t s = 0; s < k; ++s) front_cand[((int64_t)0 * B + b) * k + s] = -1;
+            for (int32_t j = 0; j < k; ++j) {
+                p_tok[j] = ids[j];
+                p_S[j] = logp[j];
+                p_par[j] = -1;
+                p_row[j] = (int32_t)r;
+                f_cand[j] = j; /* the level-1 frontier is all k children, in child order */
+                f_S[j] = logp[j];
+            }
+        }
+
+        /* ---------------- levels 1..d-1: expand the frontier ---------------- */
+        for (int32_t l = 1; l < d; ++l) {
+            const int32_t base = k + (l - 1) * k * k;
+            for (int32_t s = 0; s < k; ++s) {
+                const int64_t r = (int64_t)b * k + s;
+                const int32_t c_in = f_cand[s];
+                const int32_t lvl_in = cand_depth(c_in, k) - 1; /* level whose row made c_in */
+                const float *src = fh + ((int64_t)lvl_in * R + p_row[c_in]) * h;
+                float *fo = fh + ((int64_t)l * R + r) * h;
+                orc_fc_row(h, bf, w_fc, b_fc, src, emb, p_tok[c_in], fo);
+                orc_lm_head_row(h, V, bf, w_lm, fo, z);
+                float lse;
+                orc_log_softmax_topk(V, k, z, ids, logp, &lse);
+                if (row_fhat) memcpy(row_fhat + ((int64_t)l * R + r) * h, fo, sizeof(float) * h);
+                if (row_z) memcpy(row_z + ((int64_t)l * R + r) * V, z, sizeof(float) * V);
+                if (row_lse) row_lse[(int64_t)l * R + r] = lse;
+                if (row_ids) memcpy(row_ids + ((int64_t)l * R + r) * k, ids, sizeof(int32_t) * k);
+                if (row_logp)
+                    memcpy(row_logp + ((int64_t)l * R + r) * k, logp, sizeof(float) * k);
+                if (front_cand) front_cand[((int64_t)l * B + b) * k + s] = c_in;
+                for (int32_t j = 0; j < k; ++j) {
+                    const int32_t c = base + s * k + j;
+                    p_tok[c] = ids[j];
+                    p_S[c] = f_S[s] + logp[j];
+                    p_par[c] = c_in;
+                    p_row[c] = (int32_t)r;
+                }
+            }
+            if (l < d - 1) {
+                /* next frontier: top-k of this level's k^2 children by (S desc, cand asc) */
+                for (int32_t i = 0; i < k * k; ++i) p_id[i] = base + i;
+                select_top(k * k, p_S + base, p_id, k, pick);
+                for (int32_t s = 0; s < k; ++s) {
+                    f_cand[s] = base + pick[s];
+                    f_S[s] = p_S[base + pick[s]];
+                }
+            }
+        }
+
+        /* ---------------- rerank: top-m of the whole pool ---------------- */
+        for (int32_t c = 0; c < n_cand; ++c) {
+            p_id[c] = c;
+            tree_of_cand[c] = -1;
+        }
+        select_top(n_cand, p_S, p_id, m, pick);
+        for (int32_t j = 0; j < m; ++j) tree_of_cand[pick[j]] = 1; /* mark kept */
+
+        /* ---------------- build: level-major flattening ---------------- */
+        t_par[0] = -1;
+        t_cand[0] = -1;
+        {
+            int32_t t = 1;
+            for (int32_t c = 0; c < n_cand; ++c)
+                if (tree_of_cand[c] == 1) {
+                    tree_of_cand[c] = t;
+                    t_cand[t] = c;
+                    ++t;
+                }
+        }
+        for (int32_t t = 1; t < n_nodes; ++t) {
+            const int32_t pc = p_par[t_cand[t]];
+            if (pc < 0) {
+                t_par[t] = 0;
+            } else if (tree_of_cand[pc] >= 1) {
+                t_par[t] = tree_of_cand[pc];
+            } else {
+                rc = ORC_ERR_TREE;
+                goto done;
+            }
+        }
+        for (int32_t t = 0; t < n_nodes; ++t) {
+            const int64_t o = (int64_t)b * n_nodes + t;
+            const int32_t c = t_cand[t];
+            const int32_t dep = (t == 0) ? 0 : cand_depth(c, k);
+            const int32_t pb = pos_base ? pos_base[b] : 0;
+            if (tree_tok) tree_tok[o] = (t == 0) ? root_tok[b] : p_tok[c];
+            if (tree_parent) tree_parent[o] = t_par[t];
+            if (tree_pos) tree_pos[o] = dep + pb;
+            if (tree_S) tree_S[o] = (t == 0) ? 0.0f : p_S[c];
+            if (tree_cand) tree_cand[o] = c;
+            if (tree_mask) {
+                uint32_t *row = tree_mask + o * W;
+                for (int32_t w = 0; w < W; ++w) row[w] = 0u;
+                for (int32_t a = t; a >= 0; a = t_par[a]) row[a / 32] |= 1u << (a % 32);
+            }
+        }
+
+        /* ---------------- draft logits of every tree node's own row ---------------- */
+        if (node_z) {
+            for (int32_t t = 0; t < n_nodes; ++t) {
+                const float *src;
+                int32_t tok;
+                if (t == 0) {
+                    for (int32_t i = 0; i < h; ++i)
+                        feat[i] = load_elem(root_feat, bf, (int64_t)b * h + i);
+                    src = feat;
+                    tok = root_tok[b];
+                } else {
+                    const int32_t c = t_cand[t];
+                    src = fh + ((int64_t)(cand_depth(c, k) - 1) * R + p_row[c]) * h;
+                    tok = p_tok[c];
+                }
+                orc_fc_row(h, bf, w_fc, b_fc, src, emb, tok, x_fhat);
+                orc_lm_head_row(h, V, bf, w_lm, x_fhat, node_z + ((int64_t)b * n_nodes + t) * V);
+            }
+        }
+
+        /* ---------------- pool out ---------------- */
+        for (int32_t c = 0; c < n_cand; ++c) {
+            const int64_t o = (int64_t)b * n_cand + c;
+            if (cand_tok) cand_tok[o] = p_tok[c];
+            if (cand_S) cand_S[o] = p_S[c];
+            if (cand_parent) cand_parent[o] = p_par[c];
+            if (cand_row) cand_row[o] = p_row[c];
+        }
+    }
+
+done:
+    free(fh); free(z); free(feat); free(x_fhat); free(ids); free(logp);
+    free(p_tok); free(p_S); free(p_par); free(p_row); free(p_id); free(f_cand); free(f_S);
+    free(pick); free(tree_of_cand); free(t_par); free(t_cand);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Greedy tree verification                                                                   */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * [notes04] §6.2 (the target scores every tree node in one forward, verification walks the
+ * tree from the root), [zdszero] "Medusa" (at temperature 0 acceptance reduces to greedy) and
+ * [jsqmd] "二、EAGLE-2" (accept the longest consistent root path, then continue from its last
+ * node).  For request b:
+ *   g_i  = argmax_v T[b][i][v], ties to the lowest v
+ *   walk : cur = 0 (root); while some child c of cur has token(c) == g_cur: accept c, cur = c
+ *          (siblings carry distinct tokens, so at most one child matches; the lowest index is
+ *          taken if an input breaks that)
+ *   out  : accept_len = number of drafted nodes accepted (0..depth);
+ *          accept_nodes[0..accept_len] = the path's tree indices, root first;
+ *          accept_tok[0..accept_len-1] = their tokens, accept_tok[accept_len] = g_cur (the
+ *          bonus token); unused slots -1.  Both outputs are [B][depth+1].
+ * T is [B][n_nodes][V] fp32.  g_out [B][n_nodes] is optional.
+ * Pins: brute force over every root path of small random trees; the expected committed
+ * tokens per round against the worked values of [notes04] §8 and exercise 2.
+ */
+int32_t orc_verify_greedy(int32_t B, int32_t n_nodes, int32_t V, int32_t depth,
+                          const int32_t *tree_tok, const int32_t *tree_parent, const float *T,
+                          int32_t *g_out, int32_t *accept_len, int32_t *accept_nodes,
+                          int32_t *accept_tok) {
+    if (B < 0 || n_nodes < 1 || V < 1 || depth < 0) return ORC_ERR_ARG;
+    int32_t *g = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n_nodes > 0 ? n_nodes : 1));
+    if (!g) return ORC_ERR_NOMEM;
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t *tok = tree_tok + (int64_t)b * n_nodes;
+        const int32_t *par = tree_parent + (int64_t)b * n_nodes;
+        for (int32_t i = 0; i < n_nodes; ++i) {
+            const float *row = T + ((int64_t)b * n_nodes + i) * V;
+            int32_t best = 0;
+            for (int32_t v = 1; v < V; ++v)
+                if (row[v] > row[best]) best = v;
+            g[i] = best;
+            if (g_out) g_out[(int64_t)b * n_nodes + i] = best;
+        }
+        int32_t *an = accept_nodes + (int64_t)b * (depth + 1);
+        int32_t *at = accept_tok + (int64_t)b * (depth + 1);
+        for (int32_t i = 0; i <= depth; ++i) {
+            an[i] = -1;
+            at[i] = -1;
+        }
+        int32_t cur = 0, n = 0;
+        an[0] = 0;
+        while (n < depth) {
+            int32_t next = -1;
+            for (int32_t c = 1; c < n_nodes; ++c)
+                if (par[c] == cur && tok[c] == g[cur]) {
+                    next = c;
+                    break;
+                }
+            if (next < 0) break;
+            at[n] = tok[next];
+            ++n;
+            an[n] = next;
+            cur = next;
+        }
+        at[n] = g[cur];
+        accept_len[b] = n;
+    }
+    free(g);
+    return ORC_OK;
+}
+
+/* Element-wise bf16 rounding of an fp32 array (test helper for the rounding pin). */
+void orc_round_bf16_array(int64_t n, const float *in, uint16_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_bf16(in[i]);
+}
