@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Throughput of one EAGLE-2 dynamic draft-tree step on GB300.
+
+A step is the whole hot path over one batch: d draft levels (gather, FC, LM head, log-softmax +
+top-k, expand), the rerank + tree build, and greedy verification (target argmax + walk).  The
+default workload is the Vicuna-7B shape (h=4096, V=32000, batch 1, depth 6, k=10, m=60).
+Inputs are seeded synthetic data; target logits are the draft's own logits of every tree node
+plus N(0, sigma) noise.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5] [--impl eagle|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+METRIC = "draft-tree steps/sec (tree nodes/sec) at 1 GB300; % HBM or tensor roofline"
+UNIT = "steps/s"
+PEAKS_FILE = ROOT / "MEASURED_PEAKS.json"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = ROOT / "profiles" / "linear_bf16_tc_vicuna7b.md"
+KERNEL_SOURCES = ["eagle_speculative_decoding_draft_gb300/csrc/gemm.cu",
+                  "eagle_speculative_decoding_draft_gb300/csrc/common.cuh"]
+N_INPUT_SETS = 4
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--workload", type=int, default=2)
+    p.add_argument("--impl", choices=["eagle", "reference"], default="eagle")
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="wall-clock budget of the oracle's timed sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=300)
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        h.update((ROOT / rel).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """dram read+write bytes per GEMM launch from the committed ncu summary, or None when the
+    kernel source changed since that capture."""
+    if not TRAFFIC_FILE.exists():
+        return None
+    text = TRAFFIC_FILE.read_text()
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    m_val = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_val or m_hash.group(1) != kernel_hash():
+        return None
+    return float(m_val.group(1))
+
+
+def hbm_peak():
+    try:
+        return float(json.loads(PEAKS_FILE.read_text())["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu_index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.12)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def visible_gpu_index(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids) and ids[local_rank].isdigit():
+            return int(ids[local_rank])
+    return local_rank
+
+
+# ----------------------------------------------------------------------------------------------
+# The CPU oracle, timed on this host's cores (CPU-baseline leg and the reference arm)
+# ----------------------------------------------------------------------------------------------
+
+def oracle_sample(w, inp):
+    """A bounded sample of the workload for the oracle: the first r requests (r = 1 unless the
+    whole batch is small), with their target logits (oracle node logits + noise, untimed)."""
+    import oracle
+
+    r = w.batch if w.batch * w.num_nodes * w.hidden <= 4096 * 64 else 1
+    idx = list(range(r))
+    feat = inp.root_feat[idx].contiguous()
+    tok = inp.root_tok[idx].contiguous()
+    ref = oracle.draft_tree(inp.w_fc, inp.b_fc, inp.w_lm, inp.emb, feat, tok, w.depth, w.topk,
+                            w.num_keep, w.is_bf16, rows=False, node_logits=True)
+    rng = np.random.default_rng(4242)
+    T = ref["node_z"] + rng.standard_normal(ref["node_z"].shape, dtype=np.float32) * np.float32(
+        w.target_sigma)
+    return r, feat, tok, T.astype(np.float32)
+
+
+def time_oracle(w, inp, sample, budget_s, max_steps=None, warmup=0):
+    """Runs the oracle's draft-tree step + greedy verify on the sample until the wall-clock budget
+    (or max_steps) is used; returns (steps of the sample, seconds)."""
+    import oracle
+
+    r, feat, tok, T = sample
+
+    def one():
+        out = oracle.draft_tree(inp.w_fc, inp.b_fc, inp.w_lm, inp.emb, feat, tok, w.depth, w.topk,
+                                w.num_keep, w.is_bf16, rows=False)
+        oracle.verify_greedy(out["tree_tok"], out["tree_parent"], T, w.depth)
+
+    for _ in range(warmup):
+        one()
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        one()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_steps is not None and n >= max_steps):
+            break
+    return n, el
+
+
+def cpu_baseline(w, inp, budget_s):
+    import oracle
+
+    sample = oracle_sample(w, inp)
+    r = sample[0]
+    n, el = time_oracle(w, inp, sample, budget_s)
+    value = n * r / w.batch / el
+    return {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} oracle draft-tree steps (draft levels, rerank/build, greedy verify) of "
+                      f"{r} of {w.batch} request(s), {el:.1f} s wall; value scaled to whole steps"}
+
+
+def workload_config(w):
+    mb = (2 * w.hidden * w.hidden + w.vocab * w.hidden) * (2 if w.is_bf16 else 4) / 1e6
+    l2 = (f"inputs larger than L2: each level streams {mb:.0f} MB of weights (L2 is 129 MB); "
+          "no flush") if mb > 129 else f"weights ({mb:.1f} MB) fit in L2: L2-resident timing"
+    return {"workload": w.name, "hidden": w.hidden, "vocab": w.vocab, "batch": w.batch,
+            "depth": w.depth, "topk": w.topk, "num_keep": w.num_keep,
+            "tree_nodes_per_request": w.num_nodes, "global_batch": w.batch,
+            "parallelism": "replicas (one independent engine per GPU)", "l2": l2}
+
+
+def run_reference(args, w):
+    """The reference arm: the oracle, as it stands, on this host's cores."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from eagle_speculative_decoding_draft_gb300 import synth
+
+    inp = synth.make_inputs(w)
+    sample = oracle_sample(w, inp)
+    r = sample[0]
+    budget = 150.0
+    n, el = time_oracle(w, inp, sample, budget, max_steps=max(1, args.steps),
+                        warmup=min(args.warmup, 1))
+    value = n * r / w.batch / el
+    cb = {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+          "sample": f"{n} oracle steps of {r} of {w.batch} request(s) in {el:.1f} s (at most "
+                    f"{budget:.0f} s), value scaled to whole steps"}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": n, "warmup": min(args.warmup, 1),
+            "ms_per_step": 1e3 / value, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.is_bf16 else "f32", "data": "synthetic (seeded)",
+            "config": workload_config(w), "tree_nodes_per_s": value * w.batch * w.num_nodes,
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------------
+# The GPU engine
+# ----------------------------------------------------------------------------------------------
+
+def run_eagle(args, w):
+    import torch
+
+    from eagle_speculative_decoding_draft_gb300 import synth
+    from eagle_speculative_decoding_draft_gb300.engine import EagleTree
+
+    world, rank, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum_over_ranks(x: float) -> float:
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t)
+        return float(t.item())
+
+    inp = synth.make_inputs(w)
+    g = lambda t: t.to(dev).contiguous()
+    eng = EagleTree(g(inp.w_fc), g(inp.b_fc) if w.bias else None, g(inp.w_lm), g(inp.emb),
+                    w.batch, w.depth, w.topk, w.num_keep)
+    B, h, V, n, d = w.batch, w.hidden, w.vocab, w.num_nodes, w.depth
+    fdt = torch.bfloat16 if w.is_bf16 else torch.float32
+
+    # a few distinct input batches, each with its synthetic target (draft logits + noise)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+    sets = []
+    for i in range(N_INPUT_SETS):
+        if i == 0:
+            feat, tok = inp.root_feat, inp.root_tok
+        else:
+            rng = np.random.default_rng(5000 + 17 * i + rank)
+            feat = torch.from_numpy(rng.standard_normal((B, h), dtype=np.float32)).to(fdt)
+            tok = torch.from_numpy(rng.integers(0, V, size=B).astype(np.int32))
+        feat, tok = g(feat), g(tok)
+        eng.draft(feat, tok)
+        nz = eng.node_logits(feat)
+        T = nz + w.target_sigma * torch.randn(nz.shape, generator=gen, device=dev)
+        sets.append((feat, tok, T))
+    tree_out, ver_out = eng.new_tree_outputs(), eng.new_verify_outputs()
+
+    def step(i):
+        feat, tok, T = sets[i % N_INPUT_SETS]
+        eng.step(feat, tok, T, tree_out=tree_out, verify_out=ver_out)
+
+    for i in range(max(args.warmup, 0)):
+        step(i)
+    eng.profile(64)
+    step(0)
+    gemm_per_step, _, _ = eng.profile_read()
+    torch.cuda.synchronize()
+    eng.status()
+
+    # ---------------- timed region: K steps, device time ----------------
+    K = args.steps
+    eng.profile(K * gemm_per_step)
+    l0 = eng.launch_count()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(visible_gpu_index(local)) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        start.record()
+        for i in range(K):
+            step(i)
+        end.record()
+        torch.cuda.synchronize()
+        barrier()
+    ms = start.elapsed_time(end)
+    launches = eng.launch_count() - l0
+    n_prof, gemm_ms, gemm_bytes = eng.profile_read()
+    eng.profile(0)
+    eng.status()
+    ms_max = max_over_ranks(ms)
+    value = world * K / (ms_max / 1e3)
+
+    accept = []
+    for i in range(N_INPUT_SETS):
+        step(i)
+        accept.append(ver_out["accept_len"].float().mean().item())
+    torch.cuda.synchronize()
+
+    # ---------------- end to end: host buffers through eagle_tree_step_host ----------------
+    pin = lambda t: t.cpu().pin_memory()
+    hsets = [(pin(f), pin(t), pin(T)) for f, t, T in sets]
+    staging = torch.empty_like(sets[0][2])
+    W = eng.mask_words
+    i32 = dict(dtype=torch.int32, pin_memory=True)
+    hout = {"tokens": torch.empty(B, n, **i32), "parents": torch.empty(B, n, **i32),
+            "positions": torch.empty(B, n, **i32), "mask": torch.empty(B, n, W, **i32),
+            "accept_len": torch.empty(B, **i32), "accept_tokens": torch.empty(B, d + 1, **i32)}
+    for i in range(3):
+        f, t, T = hsets[i % N_INPUT_SETS]
+        eng.step_host(f, t, T, staging, hout)
+    E = max(1, args.e2e_steps)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(E):
+        f, t, T = hsets[i % N_INPUT_SETS]
+        eng.step_host(f, t, T, staging, hout)
+    e2e_s = max_over_ranks(time.perf_counter() - t0)
+    barrier()
+    f, t, T = hsets[0]
+    h2d = f.numel() * f.element_size() + t.numel() * 4 + T.numel() * T.element_size()
+    d2h = 4 * (3 * B * n + B * n * W + B + B * (d + 1))
+
+    peak, peak_kind = hbm_peak()
+    achieved = gemm_bytes / (gemm_ms * 1e-3) / 1e9 if gemm_ms > 0 else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_max / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.is_bf16 else "f32",
+        "data": "synthetic (seeded); target logits = the draft's logits of every tree node + "
+                f"N(0, {w.target_sigma})",
+        "config": dict(workload_config(w),
+                       mode="eager launches through the C ABI from Python; CUDA events on the "
+                            "launching stream"),
+        "tree_nodes_per_s": value * B * n,
+        "mean_accept_len": float(np.mean(accept)),
+        "roofline": {"bound": "hbm", "kernel": "linear_bf16_tc_kernel (FC and LM head)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": None if achieved is None else achieved / peak,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": recorded_traffic(),
+                     "algorithmic_bytes_per_launch": gemm_bytes / max(n_prof, 1),
+                     "launches_timed": n_prof, "ms_per_launch": gemm_ms / max(n_prof, 1),
+                     "share_of_step": gemm_ms / ms if ms > 0 else None},
+        "clocks": clocks.summary(),
+        "e2e": {"value": world * E / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "how": "eagle_tree_step_host per step: pinned host inputs and target logits "
+                       "copied in, tree and verify results copied out, stream synchronised"},
+        "gpu_launches": int(sum_over_ranks(launches)),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    eng.close()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    from eagle_speculative_decoding_draft_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_eagle(args, w)
+
+
+if __name__ == "__main__":
+    main()

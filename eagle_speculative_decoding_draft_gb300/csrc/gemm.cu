@@ -1,0 +1,464 @@
+// gemm.cu - the draft FC (2h -> h, bias) and the shared LM head (h -> V) as streamed-weight GEMMs.
+//
+// EAGLE notes ch. 04 §4.1 / zdszero "draft 结构": f^ = FC([f || e(t)]) and z = LM_head(f^).  At
+// draft time the rows (frontier nodes) are few (1..256) and the weights are large (64 MiB to
+// 1 GB), so every launch streams its weight matrix through shared memory exactly once:
+//
+//   swap-AB     the weight tile is the MMA's A operand (M = 128 weight rows) and the activation
+//               rows are its N (16..256), so one weight byte feeds all rows of the batch;
+//   TMA         a producer warp streams 128x64 bf16 weight tiles (16 KB, 128-byte swizzle) and
+//               the matching 64-wide slice of the activation rows into a ring of stages;
+//   tcgen05     one thread issues tcgen05.mma (kind::f16, bf16 in, fp32 accumulate) into a
+//               double-buffered TMEM accumulator; tcgen05.commit frees each stage;
+//   epilogue    four warps read the accumulator with tcgen05.ld (one TMEM lane per weight row)
+//               and write Y[r][o] coalesced along o (+ bias, rounding to bf16 for the FC);
+//   stream-K    all k-blocks of all tiles are one sequence split evenly over one CTA per SM, so
+//               every SM streams the same number of weight bytes whatever the tile count; a tile
+//               cut between CTAs is summed by the last CTA to arrive (atomic ticket, no waiting),
+//               which adds the partials in ascending CTA order so results are deterministic.
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace eagle {
+namespace {
+
+constexpr int BM = kLinearTileM;
+constexpr int BK = kLinearTileK;
+constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB weight tile
+constexpr int kMaxStages = 16;
+constexpr int kThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
+constexpr size_t kMaxDynSmem = 232448;  // 227 KB per CTA on sm_100-class parts
+
+struct SmemCtl {
+    uint64_t full[kMaxStages];   // TMA -> MMA: stage loaded
+    uint64_t empty[kMaxStages];  // MMA -> TMA: stage consumed
+    uint64_t acc_full[2];        // MMA -> epilogue: accumulator ready
+    uint64_t acc_empty[2];       // epilogue -> MMA: accumulator drained (4 warps arrive)
+    uint64_t drain;              // used only when unwinding after a timeout
+    uint32_t tmem_base;
+    int32_t abort;
+    int32_t is_last;
+};
+
+struct LinearArgs {
+    int32_t M, K, rows, n_tile, num_kb, num_tiles, stages, tmem_cols;
+    const __nv_bfloat16 *bias;
+    void *out;
+    int64_t ldo;
+    int32_t out_bf16;
+    float *partials;
+    int32_t *counters;
+    int32_t *status;
+};
+
+// CTA whose k-block range [total*g/G, total*(g+1)/G) contains k-block p.
+__device__ __forceinline__ int32_t cta_of(int64_t p, int64_t total, int32_t G) {
+    return static_cast<int32_t>(((p + 1) * G + total - 1) / total) - 1;
+}
+
+__device__ __forceinline__ void store_y(const LinearArgs &a, int32_t r, int32_t o, float v) {
+    if (a.out_bf16)
+        reinterpret_cast<__nv_bfloat16 *>(a.out)[static_cast<int64_t>(r) * a.ldo + o] =
+            __float2bfloat16_rn(v);
+    else
+        reinterpret_cast<float *>(a.out)[static_cast<int64_t>(r) * a.ldo + o] = v;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                          const __grid_constant__ CUtensorMap tmap_x, const LinearArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const int32_t stages = a.stages;
+    const uint32_t b_bytes = static_cast<uint32_t>(a.n_tile) * 128u;
+    uint8_t *a_tiles = base;
+    uint8_t *b_tiles = base + static_cast<size_t>(stages) * kABytes;
+    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(b_tiles + static_cast<size_t>(stages) * b_bytes);
+    volatile int32_t *abort_flag = &ctl->abort;
+
+    const int32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t G = gridDim.x, g = blockIdx.x;
+    const int64_t nkb = a.num_kb;
+    const int64_t total = static_cast<int64_t>(a.num_tiles) * nkb;
+    const int64_t kb_begin = total * g / G, kb_end = total * (g + 1) / G;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctl->acc_full[i], 1);
+            mbar_init(&ctl->acc_empty[i], 4);
+        }
+        mbar_init(&ctl->drain, 1);
+        ctl->abort = 0;
+        ctl->is_last = 0;
+        fence_barrier_init();
+        prefetch_tensormap(&tmap_w);
+        prefetch_tensormap(&tmap_x);
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctl->tmem_base, static_cast<uint32_t>(a.tmem_cols));
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+
+    uint32_t issued = 0, issued_parity = 0;  // producer bookkeeping, for unwinding
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            const uint64_t pol_w = policy_evict_first();  // weights: streamed once
+            const uint64_t pol_x = policy_evict_last();   // activation rows: read by every CTA
+            uint32_t stage = 0, phase = 0;
+            for (int64_t kb = kb_begin; kb < kb_end; ++kb) {
+                const int32_t tile = static_cast<int32_t>(kb / nkb);
+                const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(tile) * nkb) * BK;
+                if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
+                    *abort_flag = 1;
+                    latch(a.status, kDevTimeout);
+                    break;
+                }
+                mbar_arrive_expect_tx(&ctl->full[stage], kABytes + b_bytes);
+                tma_load_2d(a_tiles + static_cast<size_t>(stage) * kABytes, &tmap_w,
+                            &ctl->full[stage], kx, tile * BM, pol_w);
+                tma_load_2d(b_tiles + static_cast<size_t>(stage) * b_bytes, &tmap_x,
+                            &ctl->full[stage], kx, 0, pol_x);
+                issued |= 1u << stage;
+                issued_parity = phase ? (issued_parity | (1u << stage))
+                                      : (issued_parity & ~(1u << stage));
+                if (++stage == static_cast<uint32_t>(stages)) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer (single thread) ----------------
+            const uint32_t idesc = idesc_bf16_f32(BM, static_cast<uint32_t>(a.n_tile));
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int64_t kb = kb_begin; kb < kb_end && ok;) {
+                const int64_t tile = kb / nkb;
+                const int64_t k1 = min(kb_end, (tile + 1) * nkb);
+                if (!mbar_wait(&ctl->acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * static_cast<uint32_t>(a.n_tile);
+                for (int64_t k = kb; k < k1; ++k) {
+                    if (!mbar_wait(&ctl->full[stage], phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(a_tiles + static_cast<size_t>(stage) * kABytes);
+                    const uint32_t b0 = smem_u32(b_tiles + static_cast<size_t>(stage) * b_bytes);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_bf16_ss(d_tmem, sw128_kmajor_desc(a0 + kk * 32),
+                                    sw128_kmajor_desc(b0 + kk * 32), idesc,
+                                    (k > kb || kk > 0) ? 1u : 0u);
+                    mma_commit(&ctl->empty[stage]);
+                    if (++stage == static_cast<uint32_t>(stages)) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&ctl->acc_full[acc]);
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+                kb = k1;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                latch(a.status, kDevTimeout);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: warps 2..5, TMEM lane quarter = warp % 4 ----------------
+        const int32_t q = warp & 3;
+        const int32_t m_local = q * 32 + lane;
+        uint32_t acc = 0, acc_phase = 0;
+        bool first = true;
+        for (int64_t kb = kb_begin; kb < kb_end;) {
+            const int32_t tile = static_cast<int32_t>(kb / nkb);
+            const int64_t t0 = static_cast<int64_t>(tile) * nkb;
+            const int64_t k1 = min(kb_end, t0 + nkb);
+            const bool full = (kb == t0) && (k1 == t0 + nkb);
+            const bool got = mbar_wait(&ctl->acc_full[acc], acc_phase, abort_flag);
+            if (!got) {
+                *abort_flag = 1;
+                latch(a.status, kDevTimeout);
+            }
+            const int32_t o = tile * BM + m_local;
+            const bool o_ok = o < a.M;
+            const float bias_o = (a.bias != nullptr && o_ok) ? __bfloat162float(a.bias[o]) : 0.0f;
+            __syncwarp();
+            if (got) {
+                tc_fence_after();
+                const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       acc * static_cast<uint32_t>(a.n_tile);
+                float *part = a.partials + static_cast<size_t>(g * 2 + (first ? 0 : 1)) *
+                                               a.n_tile * BM;
+                for (int32_t n0 = 0; n0 < a.rows; n0 += 16) {
+                    uint32_t r[16];
+                    __syncwarp();
+                    tmem_ld_16(t_row + static_cast<uint32_t>(n0), r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int32_t n = n0 + j;
+                        if (n < a.rows) {
+                            const float v = __uint_as_float(r[j]);
+                            if (full) {
+                                if (o_ok) store_y(a, n, o, v + bias_o);
+                            } else {
+                                part[static_cast<size_t>(n) * BM + m_local] = v;
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && got) mbar_arrive(&ctl->acc_empty[acc]);
+            if (!full) {
+                __threadfence();
+                named_barrier_sync(1, 128);
+                const int32_t gf = cta_of(t0, total, G), gl = cta_of(t0 + nkb - 1, total, G);
+                if (threadIdx.x == 64) {
+                    int32_t last = 0;
+                    if (!*abort_flag) {
+                        const int32_t prev = atomicAdd(&a.counters[tile], 1);
+                        last = (prev == gl - gf);
+                        if (last) a.counters[tile] = 0;  // ready for the next launch
+                    }
+                    ctl->is_last = last;
+                }
+                named_barrier_sync(1, 128);
+                if (ctl->is_last) {
+                    __threadfence();
+                    for (int32_t n = 0; n < a.rows; ++n) {
+                        float s = 0.0f;
+                        for (int32_t gg = gf; gg <= gl; ++gg) {
+                            const int64_t first_tile = (total * gg / G) / nkb;
+                            const int32_t slot = (first_tile == tile) ? 0 : 1;
+                            const float x = __ldcg(a.partials +
+                                                   (static_cast<size_t>(gg * 2 + slot) * a.n_tile +
+                                                    n) * BM + m_local);
+                            s = (gg == gf) ? x : s + x;
+                        }
+                        if (o_ok) store_y(a, n, o, s + bias_o);
+                    }
+                }
+                named_barrier_sync(1, 128);
+            }
+            if (*abort_flag) break;
+            first = false;
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+            kb = k1;
+        }
+    }
+
+    // ---------------- teardown ----------------
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (*abort_flag) {
+        // Unwind after a timeout: let every copy and MMA this CTA started land before the CTA
+        // exits and its shared and tensor memory are handed to another CTA.
+        if (warp == 0 && lane == 0) {
+            for (int s = 0; s < stages; ++s)
+                if ((issued >> s) & 1u) mbar_wait(&ctl->full[s], (issued_parity >> s) & 1u, nullptr);
+        }
+        if (warp == 1 && lane == 0) {
+            mma_commit(&ctl->drain);
+            mbar_wait(&ctl->drain, 0, nullptr);
+        }
+        __syncwarp();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, static_cast<uint32_t>(a.tmem_cols));
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// fp32: one warp per output feature, lanes stride the reduction, 8 rows per pass.
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+    linear_f32_kernel(const float *__restrict__ w, int64_t ldw, const float *__restrict__ x,
+                      int64_t ldx, const float *__restrict__ bias, float *__restrict__ y,
+                      int64_t ldy, int32_t M, int32_t K, int32_t rows) {
+    const int32_t o = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int32_t lane = threadIdx.x & 31;
+    if (o >= M) return;
+    const float *wr = w + static_cast<int64_t>(o) * ldw;
+    const float b = bias ? bias[o] : 0.0f;
+    for (int32_t r0 = 0; r0 < rows; r0 += 8) {
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+        for (int32_t i = lane; i < K; i += 32) {
+            const float wi = wr[i];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (r0 + j < rows) acc[j] = fmaf(wi, x[static_cast<int64_t>(r0 + j) * ldx + i], acc[j]);
+        }
+        float mine = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float v = acc[j];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == j) mine = v;
+        }
+        if (lane < 8 && r0 + lane < rows) y[static_cast<int64_t>(r0 + lane) * ldy + o] = mine + b;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool encode_bf16_2d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer,
+                    uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn fn = encoder();
+    if (!fn) return false;
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return false;
+    if ((row_stride_elems * 2) % 16 != 0) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_elems * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int32_t linear_n_tile(int32_t rows) { return ((rows + 15) / 16) * 16; }
+
+size_t linear_partials_bytes(int32_t grid, int32_t n_tile) {
+    return static_cast<size_t>(grid) * 2 * n_tile * BM * sizeof(float);
+}
+
+size_t linear_counters_bytes(int32_t M) {
+    return static_cast<size_t>((M + BM - 1) / BM) * sizeof(int32_t);
+}
+
+bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int32_t K, const void *x,
+                      int64_t ldx, int32_t rows, const void *bias, void *out, int64_t ldo,
+                      int32_t out_bf16, float *partials, int32_t *counters, int32_t *status,
+                      int32_t num_sms) {
+    if (M < 1 || K < 1 || rows < 1 || rows > kLinearMaxRows || num_sms < 1) return false;
+    if (ldw < K || ldx < K || ldo < M) return false;
+    p->M = M;
+    p->K = K;
+    p->rows = rows;
+    p->n_tile = linear_n_tile(rows);
+    p->num_kb = (K + BK - 1) / BK;
+    p->num_tiles = (M + BM - 1) / BM;
+    const int64_t total = static_cast<int64_t>(p->num_kb) * p->num_tiles;
+    p->grid = static_cast<int32_t>(total < num_sms ? total : num_sms);
+    const size_t stage_bytes = kABytes + static_cast<size_t>(p->n_tile) * 128;
+    size_t stages = (kMaxDynSmem - 1024 - sizeof(SmemCtl)) / stage_bytes;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) return false;
+    p->stages = static_cast<int32_t>(stages);
+    p->smem_bytes = 1024 + stages * stage_bytes + sizeof(SmemCtl);
+    int32_t cols = 32;
+    while (cols < 2 * p->n_tile) cols *= 2;
+    p->tmem_cols = cols;
+    p->bias = bias;
+    p->out = out;
+    p->ldo = ldo;
+    p->out_bf16 = out_bf16;
+    p->partials = partials;
+    p->counters = counters;
+    p->status = status;
+    if (!encode_bf16_2d(&p->tmap_w, w, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                        static_cast<uint64_t>(ldw), BK, BM))
+        return false;
+    if (!encode_bf16_2d(&p->tmap_x, x, static_cast<uint64_t>(K), static_cast<uint64_t>(rows),
+                        static_cast<uint64_t>(ldx), BK, static_cast<uint32_t>(p->n_tile)))
+        return false;
+    return true;
+}
+
+cudaError_t prepare_kernels() {
+    cudaError_t e = cudaFuncSetAttribute(linear_bf16_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kMaxDynSmem));
+    return e;
+}
+
+cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
+    LinearArgs a;
+    a.M = p.M;
+    a.K = p.K;
+    a.rows = p.rows;
+    a.n_tile = p.n_tile;
+    a.num_kb = p.num_kb;
+    a.num_tiles = p.num_tiles;
+    a.stages = p.stages;
+    a.tmem_cols = p.tmem_cols;
+    a.bias = reinterpret_cast<const __nv_bfloat16 *>(p.bias);
+    a.out = p.out;
+    a.ldo = p.ldo;
+    a.out_bf16 = p.out_bf16;
+    a.partials = p.partials;
+    a.counters = p.counters;
+    a.status = p.status;
+    linear_bf16_tc_kernel<<<p.grid, kThreads, p.smem_bytes, st>>>(p.tmap_w, p.tmap_x, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_linear_f32(const float *w, int64_t ldw, const float *x, int64_t ldx,
+                              const float *bias, float *y, int64_t ldy, int32_t M, int32_t K,
+                              int32_t rows, cudaStream_t st) {
+    if (M < 1 || rows < 1) return cudaSuccess;
+    const int warps = 8;
+    linear_f32_kernel<<<(M + warps - 1) / warps, warps * 32, 0, st>>>(w, ldw, x, ldx, bias, y, ldy, M,
+                                                                      K, rows);
+    return cudaGetLastError();
+}
+
+}  // namespace eagle

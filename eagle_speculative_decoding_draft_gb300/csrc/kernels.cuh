@@ -1,0 +1,122 @@
+// kernels.cuh - host-side interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace eagle {
+
+// ---------------------------------------------------------------------------------------------
+// Streamed-weight GEMM (FC and LM head), bf16 on the tensor cores:
+//   Y[r][o] = sum_i W[o][i] * X[r][i] (+ bias[o]),  r < rows, o < M
+// The weight matrix is cut into 128-row tiles and 64-wide k-blocks; the k-blocks of all tiles
+// form one stream that is split evenly over a persistent grid (one CTA per SM).  A tile whose
+// k-blocks land in more than one CTA is finished by the last CTA to arrive, which adds the
+// partial sums in ascending CTA order (deterministic).
+// ---------------------------------------------------------------------------------------------
+constexpr int kLinearTileM = 128;
+constexpr int kLinearTileK = 64;
+constexpr int kLinearMaxRows = 256;  // MMA N limit of one launch
+
+struct LinearPlan {
+    CUtensorMap tmap_w;  // W [M][K] bf16, box {64, 128}, 128-byte swizzle
+    CUtensorMap tmap_x;  // X [rows][K] bf16, box {64, n_tile}, 128-byte swizzle
+    int32_t M, K, rows, n_tile, num_kb, num_tiles, stages, tmem_cols, grid;
+    size_t smem_bytes;
+    const void *bias;  // [M] bf16 or null
+    void *out;         // [rows][ldo]
+    int64_t ldo;
+    int32_t out_bf16;
+    float *partials;   // [grid][2][n_tile][128]
+    int32_t *counters; // [num_tiles], zero before and after
+    int32_t *status;
+};
+
+// Bytes of split-K scratch (partials) and tile counters a launch with these sizes needs.
+size_t linear_partials_bytes(int32_t grid, int32_t n_tile);
+size_t linear_counters_bytes(int32_t M);
+int32_t linear_n_tile(int32_t rows);
+
+// Fills `plan` (tensor maps included).  Returns false on an unusable argument (alignment,
+// strides, sizes) or when the driver's tensor-map encoder is unavailable.
+bool plan_linear_bf16(LinearPlan *plan, const void *w, int64_t ldw, int32_t M, int32_t K,
+                      const void *x, int64_t ldx, int32_t rows, const void *bias, void *out,
+                      int64_t ldo, int32_t out_bf16, float *partials, int32_t *counters,
+                      int32_t *status, int32_t num_sms);
+cudaError_t launch_linear_bf16(const LinearPlan &plan, cudaStream_t st);
+// One-time per-device kernel attributes (large dynamic shared memory).
+cudaError_t prepare_kernels();
+
+// fp32 path (FMA on the CUDA cores), same contract, no scratch.
+cudaError_t launch_linear_f32(const float *w, int64_t ldw, const float *x, int64_t ldx,
+                              const float *bias, float *y, int64_t ldy, int32_t M, int32_t K,
+                              int32_t rows, cudaStream_t st);
+
+// ---------------------------------------------------------------------------------------------
+// Per-row log-softmax + top-k (k <= 16), or argmax (k = 1, lse == null).
+// ---------------------------------------------------------------------------------------------
+cudaError_t launch_row_topk(const void *logits, int32_t is_bf16, int32_t rows, int32_t V,
+                            int64_t ld, int32_t k, int32_t *ids, float *vals, float *lse,
+                            cudaStream_t st);
+
+// ---------------------------------------------------------------------------------------------
+// Tree kernels
+// ---------------------------------------------------------------------------------------------
+struct ExpandArgs {
+    int32_t level, B, k, n_cand, h, V, elem_bytes;
+    const int32_t *row_ids;
+    const float *row_logp;
+    const int32_t *front_cand_in;
+    const float *front_S_in;
+    int32_t *front_cand_out;  // null on the last level
+    float *front_S_out;
+    int32_t *pool_tok;
+    float *pool_S;
+    int32_t *pool_parent;
+    int32_t *pool_row;
+    const void *fhat;  // this level's f^ rows [.][h], or null (no feature copy)
+    const void *emb;   // [V][h]
+    void *x_next;      // [B*k][2h], or null
+    int32_t *status;
+};
+cudaError_t launch_expand(const ExpandArgs &a, cudaStream_t st);
+
+struct BuildArgs {
+    int32_t B, k, d, m, n_cand, r_pad;
+    const int32_t *pool_tok;
+    const float *pool_S;
+    const int32_t *pool_parent;
+    const int32_t *pool_row;  // may be null (node_src then not written)
+    const int32_t *root_tok;
+    const int32_t *pos_base;  // may be null
+    int32_t *tokens, *parents, *positions;
+    uint32_t *mask;
+    float *logscore;          // may be null
+    int32_t *node_tok, *node_src;  // may be null
+    int32_t *status;
+};
+constexpr int32_t kMaxCandidates = 4096;  // rerank pool per request
+cudaError_t launch_build_tree(const BuildArgs &a, cudaStream_t st);
+cudaError_t prepare_tree_kernels();
+
+cudaError_t launch_verify_walk(int32_t B, int32_t n, int32_t d, const int32_t *tok,
+                               const int32_t *par, const int32_t *g, int32_t *accept_len,
+                               int32_t *accept_nodes, int32_t *accept_tok, cudaStream_t st);
+
+// X[r] = [feature(src[r]) || E[tok[r]]]: src[r] >= 0 is a row of fhat_all, -1-b is row b of
+// root_feat; src == null means src[r] = -1-r.
+struct GatherArgs {
+    int32_t n_rows, h, V, elem_bytes;
+    const int32_t *src;
+    const int32_t *tok;
+    const void *root_feat;
+    const void *fhat_all;
+    const void *emb;
+    void *x;
+    int32_t *status;
+};
+cudaError_t launch_gather(const GatherArgs &a, cudaStream_t st);
+
+}  // namespace eagle

@@ -1,0 +1,311 @@
+// tree.cu - expand, rerank + tree build, greedy verify walk, and the row gather of the draft.
+//
+// EAGLE notes ch. 04 §10.3 (expand: keep the top-k nodes of the newest level; rerank: keep the
+// top-m of all nodes; a child never outscores its parent so the kept set is a tree, ties to the
+// shallower node), §12.5 (ancestor-only mask, positions shared per level), §6.2 (tree verify);
+// zdszero "在 SGLang 里" (top-k of k^2 per level, top num_draft_tokens-1 overall, then the tree
+// and mask); jsqmd "二、EAGLE-2" (flatten, positions, tree mask, longest consistent path).
+//
+// Scores are fp32 logs: S(child) = S(parent) + logp(child).  Every ranking is by
+// (S descending, candidate ascending); candidates are numbered level-major, so a parent always
+// ranks before its children and the kept set is closed under parents.
+#include <climits>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace eagle {
+namespace {
+
+__device__ __forceinline__ int32_t cand_depth(int32_t c, int32_t k) {
+    return c < k ? 1 : 2 + (c - k) / (k * k);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Expand.  Grid (B, Y): block (b, y) recomputes request b's candidates and their ranks (at most
+// 256 of them); block y == 0 writes the pool and the next frontier; all Y blocks share the copy
+// of the next level's rows [f^(producing row) || E[token]].
+// ---------------------------------------------------------------------------------------------
+constexpr int kExpandThreads = 256;
+
+__global__ void __launch_bounds__(kExpandThreads) expand_kernel(const ExpandArgs a) {
+    __shared__ float sS[256];
+    __shared__ int32_t sTok[256], sRow[256], sC[256];
+    __shared__ int32_t slot[16];
+    const int32_t b = blockIdx.x, t = threadIdx.x, k = a.k, kk = a.k * a.k;
+    const int32_t nl = (a.level == 0) ? k : kk;
+    if (t < nl) {
+        int32_t tok, row, par, c;
+        float S;
+        if (a.level == 0) {
+            row = b;
+            tok = a.row_ids[static_cast<int64_t>(b) * k + t];
+            S = a.row_logp[static_cast<int64_t>(b) * k + t];
+            par = -1;
+            c = t;
+        } else {
+            const int32_t s = t / k, j = t - (t / k) * k;
+            row = b * k + s;
+            tok = a.row_ids[static_cast<int64_t>(row) * k + j];
+            S = a.front_S_in[b * k + s] + a.row_logp[static_cast<int64_t>(row) * k + j];
+            par = a.front_cand_in[b * k + s];
+            c = k + (a.level - 1) * kk + t;
+        }
+        if (tok < 0 || tok >= a.V) {
+            latch(a.status, kDevBounds);
+            tok = 0;
+        }
+        sS[t] = S;
+        sTok[t] = tok;
+        sRow[t] = row;
+        sC[t] = c;
+        if (blockIdx.y == 0) {
+            const int64_t o = static_cast<int64_t>(b) * a.n_cand + c;
+            a.pool_tok[o] = tok;
+            a.pool_S[o] = S;
+            a.pool_parent[o] = par;
+            a.pool_row[o] = row;
+        }
+    }
+    if (a.front_cand_out == nullptr) return;  // last level: no next frontier
+    if (t < 16) slot[t] = 0;  // every slot is overwritten when the scores are finite
+    __syncthreads();
+    if (t < nl) {
+        int32_t rank = 0;
+        for (int32_t u = 0; u < nl; ++u) rank += ranks_before(sS[u], sC[u], sS[t], sC[t]) ? 1 : 0;
+        if (rank < k) slot[rank] = t;
+    }
+    __syncthreads();
+    if (blockIdx.y == 0 && t < k) {
+        a.front_cand_out[b * k + t] = sC[slot[t]];
+        a.front_S_out[b * k + t] = sS[slot[t]];
+    }
+    if (a.x_next == nullptr || a.fhat == nullptr) return;
+    const int32_t eb = a.elem_bytes;
+    const int32_t vpr = (2 * a.h * eb) / 16, vh = (a.h * eb) / 16;
+    const uint8_t *fh = reinterpret_cast<const uint8_t *>(a.fhat);
+    const uint8_t *em = reinterpret_cast<const uint8_t *>(a.emb);
+    uint8_t *xo = reinterpret_cast<uint8_t *>(a.x_next);
+    for (int32_t i = blockIdx.y * kExpandThreads + t; i < k * vpr; i += gridDim.y * kExpandThreads) {
+        const int32_t sp = i / vpr, off = i - (i / vpr) * vpr;
+        const int32_t src = slot[sp];
+        const uint4 *from = (off < vh)
+            ? reinterpret_cast<const uint4 *>(fh + static_cast<int64_t>(sRow[src]) * a.h * eb) + off
+            : reinterpret_cast<const uint4 *>(em + static_cast<int64_t>(sTok[src]) * a.h * eb) + (off - vh);
+        uint4 *to = reinterpret_cast<uint4 *>(xo + static_cast<int64_t>(b * k + sp) * 2 * a.h * eb) + off;
+        *to = __ldg(from);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Rerank + build: one CTA per request.
+// ---------------------------------------------------------------------------------------------
+constexpr int kBuildThreads = 512;
+
+__global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(const BuildArgs a) {
+    extern __shared__ int32_t sm[];
+    const int32_t nc = a.n_cand, n = a.m + 1;
+    float *sS = reinterpret_cast<float *>(sm);
+    int32_t *sPar = sm + nc;
+    int32_t *sIdx = sPar + nc;  // tree index of a kept candidate, 0 if not kept
+    int32_t *tPar = sIdx + nc;  // parent tree index of each node
+    __shared__ int32_t warp_cnt[kBuildThreads / 32], warp_off[kBuildThreads / 32], running;
+
+    const int32_t b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int64_t pb = static_cast<int64_t>(b) * nc;
+    for (int32_t c = t; c < nc; c += kBuildThreads) {
+        sS[c] = a.pool_S[pb + c];
+        sPar[c] = a.pool_parent[pb + c];
+    }
+    __syncthreads();
+    // kept iff fewer than m candidates rank before it
+    for (int32_t c = t; c < nc; c += kBuildThreads) {
+        const float S = sS[c];
+        int32_t rank = 0;
+        for (int32_t u = 0; u < nc; ++u) rank += ranks_before(sS[u], u, S, c) ? 1 : 0;
+        sIdx[c] = (rank < a.m) ? 1 : 0;
+    }
+    if (t == 0) running = 0;
+    __syncthreads();
+    // tree index = 1 + number of kept candidates with a smaller id (block scan, chunk by chunk)
+    for (int32_t base = 0; base < nc; base += kBuildThreads) {
+        const int32_t c = base + t;
+        const int32_t flag = (c < nc) ? sIdx[c] : 0;
+        const uint32_t ballot = __ballot_sync(0xffffffffu, flag);
+        if (lane == 0) warp_cnt[warp] = __popc(ballot);
+        __syncthreads();
+        if (t == 0) {
+            int32_t acc = 0;
+            for (int w = 0; w < kBuildThreads / 32; ++w) {
+                warp_off[w] = acc;
+                acc += warp_cnt[w];
+            }
+        }
+        __syncthreads();
+        if (flag) sIdx[c] = 1 + running + warp_off[warp] + __popc(ballot & ((1u << lane) - 1u));
+        __syncthreads();
+        if (t == 0) running += warp_off[kBuildThreads / 32 - 1] + warp_cnt[kBuildThreads / 32 - 1];
+        __syncthreads();
+    }
+    const int64_t ob = static_cast<int64_t>(b) * n;
+    const int32_t pos0 = a.pos_base ? a.pos_base[b] : 0;
+    for (int32_t i = t; i < n; i += kBuildThreads) tPar[i] = (i == 0) ? -1 : 0;
+    __syncthreads();
+    if (t == 0) {
+        a.tokens[ob] = a.root_tok[b];
+        a.parents[ob] = -1;
+        a.positions[ob] = pos0;
+        if (a.logscore) a.logscore[ob] = 0.0f;
+        if (a.node_tok) a.node_tok[ob] = a.root_tok[b];
+        if (a.node_src) a.node_src[ob] = -1 - b;
+    }
+    for (int32_t c = t; c < nc; c += kBuildThreads) {
+        const int32_t ti = sIdx[c];
+        if (ti <= 0 || ti >= n) continue;
+        const int32_t pc = sPar[c];
+        int32_t pt = 0;
+        if (pc >= nc) {
+            latch(a.status, kDevBounds);
+        } else if (pc >= 0) {
+            pt = sIdx[pc];
+            if (pt <= 0) {  // parent not kept: impossible for finite scores
+                latch(a.status, kDevTree);
+                pt = 0;
+            }
+        }
+        tPar[ti] = pt;
+        const int32_t dep = cand_depth(c, a.k);
+        const int32_t tok = a.pool_tok[pb + c];
+        a.tokens[ob + ti] = tok;
+        a.parents[ob + ti] = pt;
+        a.positions[ob + ti] = dep + pos0;
+        if (a.logscore) a.logscore[ob + ti] = sS[c];
+        if (a.node_tok) a.node_tok[ob + ti] = tok;
+        if (a.node_src && a.pool_row)
+            a.node_src[ob + ti] = (dep - 1) * a.r_pad + a.pool_row[pb + c];
+    }
+    __syncthreads();
+    // ancestor-only mask, LSB-first bits: walk up the parents (strictly decreasing indices)
+    const int32_t W = (n + 31) / 32;
+    for (int32_t ti = t; ti < n; ti += kBuildThreads) {
+        for (int32_t w = 0; w < W; ++w) {
+            uint32_t word = 0;
+            for (int32_t x = ti; x >= 0; x = tPar[x])
+                if ((x >> 5) == w) word |= 1u << (x & 31);
+            a.mask[(ob + ti) * W + w] = word;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Verify walk: one warp per request.
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(128)
+    verify_walk_kernel(int32_t B, int32_t n, int32_t d, const int32_t *__restrict__ tok,
+                       const int32_t *__restrict__ par, const int32_t *__restrict__ g,
+                       int32_t *accept_len, int32_t *accept_nodes, int32_t *accept_tok) {
+    const int32_t b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int32_t lane = threadIdx.x & 31;
+    if (b >= B) return;
+    const int32_t *tk = tok + static_cast<int64_t>(b) * n;
+    const int32_t *pr = par + static_cast<int64_t>(b) * n;
+    const int32_t *gb = g + static_cast<int64_t>(b) * n;
+    int32_t *an = accept_nodes + static_cast<int64_t>(b) * (d + 1);
+    int32_t *at = accept_tok + static_cast<int64_t>(b) * (d + 1);
+    for (int32_t i = lane; i <= d; i += 32) {
+        an[i] = -1;
+        at[i] = -1;
+    }
+    __syncwarp();
+    int32_t cur = 0, L = 0, gc = gb[0];
+    if (lane == 0) an[0] = 0;
+    while (L < d) {
+        int32_t next = INT_MAX;
+        for (int32_t i = 1 + lane; i < n; i += 32)
+            if (pr[i] == cur && tk[i] == gc) next = min(next, i);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) next = min(next, __shfl_xor_sync(0xffffffffu, next, off));
+        if (next == INT_MAX) break;
+        if (lane == 0) {
+            at[L] = tk[next];
+            an[L + 1] = next;
+        }
+        ++L;
+        cur = next;
+        gc = gb[cur];
+    }
+    if (lane == 0) {
+        at[L] = gc;
+        accept_len[b] = L;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Row gather: X[r] = [feature || E[token]].
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
+    const int32_t r = blockIdx.x;
+    const int32_t si = a.src ? a.src[r] : -1 - r;
+    int32_t tok = a.tok[r];
+    if (tok < 0 || tok >= a.V) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) latch(a.status, kDevBounds);
+        tok = 0;
+    }
+    const int32_t eb = a.elem_bytes;
+    const int32_t vpr = (2 * a.h * eb) / 16, vh = (a.h * eb) / 16;
+    const uint8_t *fsrc = (si >= 0)
+        ? reinterpret_cast<const uint8_t *>(a.fhat_all) + static_cast<int64_t>(si) * a.h * eb
+        : reinterpret_cast<const uint8_t *>(a.root_feat) + static_cast<int64_t>(-1 - si) * a.h * eb;
+    const uint8_t *esrc = reinterpret_cast<const uint8_t *>(a.emb) + static_cast<int64_t>(tok) * a.h * eb;
+    uint4 *to = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(a.x) + static_cast<int64_t>(r) * 2 * a.h * eb);
+    for (int32_t i = blockIdx.y * blockDim.x + threadIdx.x; i < vpr; i += gridDim.y * blockDim.x)
+        to[i] = (i < vh) ? __ldg(reinterpret_cast<const uint4 *>(fsrc) + i)
+                         : __ldg(reinterpret_cast<const uint4 *>(esrc) + (i - vh));
+}
+
+}  // namespace
+
+cudaError_t launch_expand(const ExpandArgs &a, cudaStream_t st) {
+    if (a.B < 1) return cudaSuccess;
+    int32_t y = 1;
+    if (a.x_next && a.fhat) {
+        const int64_t bytes = static_cast<int64_t>(a.k) * 2 * a.h * a.elem_bytes;
+        y = static_cast<int32_t>((bytes + 8191) / 8192);  // about 8 KB of copy per block
+        if (y < 1) y = 1;
+        if (y > 64) y = 64;
+    }
+    expand_kernel<<<dim3(a.B, y), kExpandThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_build_tree(const BuildArgs &a, cudaStream_t st) {
+    if (a.B < 1) return cudaSuccess;
+    const size_t smem = (3 * static_cast<size_t>(a.n_cand) + a.m + 1) * sizeof(int32_t);
+    build_tree_kernel<<<a.B, kBuildThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t prepare_tree_kernels() {
+    return cudaFuncSetAttribute(build_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>((3 * kMaxCandidates + kMaxCandidates + 1) * 4));
+}
+
+cudaError_t launch_verify_walk(int32_t B, int32_t n, int32_t d, const int32_t *tok, const int32_t *par,
+                               const int32_t *g, int32_t *accept_len, int32_t *accept_nodes,
+                               int32_t *accept_tok, cudaStream_t st) {
+    if (B < 1) return cudaSuccess;
+    verify_walk_kernel<<<(B + 3) / 4, 128, 0, st>>>(B, n, d, tok, par, g, accept_len, accept_nodes,
+                                                    accept_tok);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const GatherArgs &a, cudaStream_t st) {
+    if (a.n_rows < 1) return cudaSuccess;
+    const int64_t bytes = 2LL * a.h * a.elem_bytes;
+    int32_t y = static_cast<int32_t>((bytes + 4095) / 4096);
+    if (y < 1) y = 1;
+    gather_kernel<<<dim3(a.n_rows, y), 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace eagle

@@ -1,0 +1,176 @@
+"""End-to-end parity of one draft-tree step on the GPU against the oracle, on the same seeded inputs.
+
+For the tiny fp32 workload, the Vicuna-7B-shaped workload and a set of ragged / edge shapes the
+oracle runs the whole batch; for the three large workloads (SGLang default, LLaMA2-70B shape,
+Llama-3-8B vocabulary) the GPU runs the full batch in the benchmark's launch configuration and
+the oracle recomputes sampled requests (requests are independent).
+
+Per request, level by level while both sides expand the same nodes: every draft row's logits
+within tolerance, and a decision (children of a row, the frontier, the rerank cut) allowed to
+differ only when its margin is at most max(1e-3, twice the GPU-oracle deviation measured at that
+level).  When all decisions agree: tree arrays, mask, positions, node logits and the verify
+result bit-exact / within tolerance.  Always: the GPU tree is valid (parents first, child score
+<= parent score, mask = ancestor closure, positions = depth) and greedy verify of the oracle's
+own tree is bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from eagle_speculative_decoding_draft_gb300 import synth
+from parity import assert_close_logits, assert_valid_tree, close_logits, lockstep_compare, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from eagle_speculative_decoding_draft_gb300 import build, _lib
+    build.build()
+    _lib.load()
+    return torch.device("cuda:0")
+
+
+def sub(t, idx):
+    return t[idx].contiguous()
+
+
+def run_case(dev, w, inp, sample=None, report=None):
+    from eagle_speculative_decoding_draft_gb300.engine import EagleTree
+    B, d, k, m, V, n = w.batch, w.depth, w.topk, w.num_keep, w.vocab, w.num_nodes
+    idx = list(range(B)) if sample is None else list(sample)
+    # ---- oracle on the sampled requests ----
+    ref = oracle.draft_tree(inp.w_fc, inp.b_fc, inp.w_lm, inp.emb, sub(inp.root_feat, idx),
+                            sub(inp.root_tok, idx), d, k, m, w.is_bf16,
+                            pos_base=np.array([7 * b + 1 for b in idx], np.int32),
+                            row_logits=True, node_logits=True)
+    noise = synth.target_noise(inp)  # [B][n][V] for the whole batch, drawn next in the stream
+    T = noise.copy()
+    T[idx] += ref["node_z"]
+    ref_ver = oracle.verify_greedy(ref["tree_tok"], ref["tree_parent"], T[idx], d)
+
+    # ---- GPU, whole batch ----
+    g = lambda t: t.to(dev).contiguous()
+    eng = EagleTree(g(inp.w_fc), g(inp.b_fc) if w.bias else None, g(inp.w_lm), g(inp.emb), B, d,
+                    k, m)
+    R = B * k
+    logits_out = torch.empty(d, max(R, 1), V, dtype=torch.float32, device=dev)
+    pos_base = torch.tensor([7 * b + 1 for b in range(B)], dtype=torch.int32, device=dev)
+    root_feat, root_tok = g(inp.root_feat), g(inp.root_tok)
+    tree = eng.draft(root_feat, root_tok, pos_base, logits_out=logits_out)
+    views = eng.views()
+    gpu = {key: to_np(views[key]) for key in ("pool_tok", "pool_S", "pool_parent")}
+    gpu["logits"] = logits_out
+    node_z = eng.node_logits(root_feat)
+    Td = torch.from_numpy(T).to(dev)
+    ver = eng.verify_greedy(tree["tokens"], tree["parents"], Td)
+    # verify of the oracle's own trees (bit-exact always)
+    tok_mix, par_mix = tree["tokens"].clone(), tree["parents"].clone()
+    tok_mix[idx] = torch.from_numpy(ref["tree_tok"]).to(dev)
+    par_mix[idx] = torch.from_numpy(ref["tree_parent"]).to(dev)
+    ver_ref_tree = eng.verify_greedy(tok_mix, par_mix, Td)
+    # a second identical step must give bit-identical results
+    tree2 = eng.draft(root_feat, root_tok, pos_base)
+    eng.status()
+    torch.cuda.synchronize()
+
+    G = {key: to_np(v) for key, v in tree.items()}
+    G2 = {key: to_np(v) for key, v in tree2.items()}
+    for key in ("tokens", "parents", "positions", "mask", "logscore"):
+        assert np.array_equal(G[key], G2[key]), f"{key} not deterministic"
+    GV = {key: to_np(v) for key, v in ver.items()}
+    GVR = {key: to_np(v) for key, v in ver_ref_tree.items()}
+    exact, diverged, dz = 0, [], []
+    for j, b in enumerate(idx):
+        # validity of the GPU tree, always
+        assert_valid_tree(G["tokens"][b], G["parents"][b], G["positions"][b], G["mask"][b],
+                          G["logscore"][b], d, 7 * b + 1)
+        assert G["tokens"][b, 0] == int(inp.root_tok[b])
+        # greedy verify of the oracle's tree: bit-exact
+        assert GVR["accept_len"][b] == ref_ver["accept_len"][j]
+        assert np.array_equal(GVR["accept_nodes"][b], ref_ver["accept_nodes"][j])
+        assert np.array_equal(GVR["accept_tokens"][b], ref_ver["accept_tok"][j])
+        info = lockstep_compare(ref, j, gpu, b, k, d, m, w.is_bf16)
+        dz.append(info["dz"])
+        if not info["exact"]:
+            diverged.append((b, info["diverged_at"], round(info["margin"], 6),
+                             round(info["threshold"], 6)))
+            continue
+        exact += 1
+        for key, rk in (("tokens", "tree_tok"), ("parents", "tree_parent"),
+                        ("positions", "tree_pos")):
+            assert np.array_equal(G[key][b], ref[rk][j]), key
+        assert np.array_equal(G["mask"][b].astype(np.uint32), ref["tree_mask"][j])
+        assert close_logits(G["logscore"][b], ref["tree_S"][j], w.is_bf16).all()
+        assert_close_logits(to_np(node_z[b]), ref["node_z"][j], w.is_bf16, "node logits")
+        assert GV["accept_len"][b] == ref_ver["accept_len"][j]
+        assert np.array_equal(GV["accept_nodes"][b], ref_ver["accept_nodes"][j])
+        assert np.array_equal(GV["accept_tokens"][b], ref_ver["accept_tok"][j])
+    if report is not None:
+        report.update(exact=exact, diverged=diverged, accept=GV["accept_len"][idx].tolist(),
+                      dz=[[round(x, 5) for x in row] for row in dz])
+    eng.close()
+    return exact, diverged
+
+
+@pytest.mark.parametrize("num", [1, 2])
+def test_full_oracle_workloads(dev, num):
+    w = synth.WORKLOADS[num]
+    inp = synth.make_inputs(w)
+    rep = {}
+    exact, diverged = run_case(dev, w, inp, report=rep)
+    print(f"workload {num}: trees identical {exact}, diverged at a near-tie {diverged}, "
+          f"accept_len {rep['accept']}, max|dz| per level {rep['dz']}")
+
+
+EDGE = [
+    dict(h=64, V=1000, B=4, d=5, k=4, m=20, dtype="bf16"),
+    dict(h=200, V=999, B=3, d=3, k=3, m=10, dtype="bf16"),     # K = 2h not a multiple of 64
+    dict(h=128, V=513, B=20, d=4, k=4, m=15, dtype="bf16"),    # ragged V, 80 rows
+    dict(h=64, V=500, B=5, d=5, k=1, m=5, dtype="bf16"),       # chain
+    dict(h=64, V=700, B=2, d=1, k=5, m=3, dtype="bf16"),       # one level
+    dict(h=64, V=700, B=3, d=3, k=3, m=0, dtype="bf16"),       # root only
+    dict(h=64, V=700, B=3, d=3, k=3, m=21, dtype="bf16"),      # keeps the whole pool
+    dict(h=64, V=700, B=40, d=3, k=8, m=30, dtype="bf16"),     # 320 rows: two GEMM launches
+    dict(h=96, V=3000, B=2, d=6, k=10, m=60, dtype="bf16"),    # EAGLE-2 paper shape, small
+    dict(h=32, V=300, B=3, d=4, k=3, m=12, dtype="f32"),
+    dict(h=256, V=1024, B=5, d=3, k=16, m=40, dtype="f32"),
+    dict(h=64, V=257, B=1, d=2, k=16, m=272, dtype="bf16"),    # k = 16, m = n_cand
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: "h{h}V{V}B{B}d{d}k{k}m{m}{dtype}".format(**c))
+def test_edge_shapes(dev, case):
+    w = synth.custom(case["h"], case["V"], case["B"], case["d"], case["k"], case["m"],
+                     dtype=case["dtype"])
+    inp = synth.make_inputs(w, seed=case["h"] + case["V"] + case["B"])
+    exact, diverged = run_case(dev, w, inp)
+    assert exact >= 1 or w.batch <= 1, f"no request checked exactly: {diverged}"
+
+
+@pytest.mark.parametrize("num", [3, 4, 5])
+def test_large_workloads_sampled(dev, num):
+    w = synth.WORKLOADS[num]
+    inp = synth.make_inputs(w)
+    sample = sorted({0, w.batch // 2, w.batch - 1})
+    rep = {}
+    exact, diverged = run_case(dev, w, inp, sample=sample, report=rep)
+    print(f"workload {num}: sampled {sample}, trees identical {exact}, diverged at a near-tie "
+          f"{diverged}, accept_len {rep['accept']}, max|dz| per level {rep['dz']}")
+
+
+def test_empty_batch_is_a_no_op(dev):
+    from eagle_speculative_decoding_draft_gb300.engine import EagleTree
+    w = synth.custom(64, 500, 0, 3, 2, 4, dtype="bf16")
+    inp = synth.make_inputs(w, seed=1)
+    g = lambda t: t.to(dev).contiguous()
+    eng = EagleTree(g(inp.w_fc), g(inp.b_fc), g(inp.w_lm), g(inp.emb), 0, 3, 2, 4)
+    rf = torch.zeros(0, 64, dtype=torch.bfloat16, device=dev)
+    rt = torch.zeros(0, dtype=torch.int32, device=dev)
+    tree = eng.draft(rf, rt)
+    assert tree["tokens"].shape == (0, 5)
+    eng.status()
+    eng.close()
