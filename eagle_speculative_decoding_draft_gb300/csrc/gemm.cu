@@ -252,17 +252,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_barrier_sync(1, 128);
                 if (ctl->is_last) {
                     __threadfence();
-                    for (int32_t n = 0; n < a.rows; ++n) {
-                        float s = 0.0f;
-                        for (int32_t gg = gf; gg <= gl; ++gg) {
-                            const int64_t first_tile = (total * gg / G) / nkb;
-                            const int32_t slot = (first_tile == tile) ? 0 : 1;
-                            const float x = __ldcg(a.partials +
-                                                   (static_cast<size_t>(gg * 2 + slot) * a.n_tile +
-                                                    n) * BM + m_local);
-                            s = (gg == gf) ? x : s + x;
+                    // Sum the partials in ascending CTA order.  All loads of a batch of rows x
+                    // CTAs are issued before any is used, so the fix-up costs a few L2 round
+                    // trips instead of one per (row, CTA).
+                    constexpr int kRowsPerBatch = 8, kCtasPerBatch = 8;
+                    for (int32_t n0 = 0; n0 < a.rows; n0 += kRowsPerBatch) {
+                        float acc[kRowsPerBatch];
+#pragma unroll
+                        for (int j = 0; j < kRowsPerBatch; ++j) acc[j] = 0.0f;
+                        for (int32_t g0 = gf; g0 <= gl; g0 += kCtasPerBatch) {
+                            float x[kCtasPerBatch][kRowsPerBatch];
+#pragma unroll
+                            for (int c = 0; c < kCtasPerBatch; ++c) {
+                                const int32_t gg = g0 + c;
+                                const int32_t slot =
+                                    ((total * gg / G) / nkb == static_cast<int64_t>(tile)) ? 0 : 1;
+                                const float *src = a.partials +
+                                    (static_cast<size_t>(gg * 2 + slot) * a.n_tile + n0) * BM + m_local;
+#pragma unroll
+                                for (int j = 0; j < kRowsPerBatch; ++j)
+                                    x[c][j] = (gg <= gl && n0 + j < a.rows)
+                                                  ? __ldcg(src + static_cast<size_t>(j) * BM) : 0.0f;
+                            }
+#pragma unroll
+                            for (int c = 0; c < kCtasPerBatch; ++c)
+#pragma unroll
+                                for (int j = 0; j < kRowsPerBatch; ++j)
+                                    if (g0 + c <= gl) acc[j] = (g0 + c == gf) ? x[c][j] : acc[j] + x[c][j];
                         }
-                        if (o_ok) store_y(a, n, o, s + bias_o);
+#pragma unroll
+                        for (int j = 0; j < kRowsPerBatch; ++j)
+                            if (o_ok && n0 + j < a.rows) store_y(a, n0 + j, o, acc[j] + bias_o);
                     }
                 }
                 named_barrier_sync(1, 128);

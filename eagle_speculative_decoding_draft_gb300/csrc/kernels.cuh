@@ -55,10 +55,12 @@ cudaError_t launch_linear_f32(const float *w, int64_t ldw, const float *x, int64
                               int32_t rows, cudaStream_t st);
 
 // ---------------------------------------------------------------------------------------------
-// Per-row log-softmax + top-k (k <= 16), or argmax (k = 1, lse == null).
+// Per-row log-softmax + top-k (k <= 16), or argmax (k = 1, lse == null).  Two launches (chunk
+// partials, then a per-row merge); `ws` holds the partials (row_topk_scratch_bytes).
 // ---------------------------------------------------------------------------------------------
+size_t row_topk_scratch_bytes(int32_t rows, int32_t V, int32_t k);
 cudaError_t launch_row_topk(const void *logits, int32_t is_bf16, int32_t rows, int32_t V,
-                            int64_t ld, int32_t k, int32_t *ids, float *vals, float *lse,
+                            int64_t ld, int32_t k, int32_t *ids, float *vals, float *lse, void *ws,
                             cudaStream_t st);
 
 // ---------------------------------------------------------------------------------------------
