@@ -328,6 +328,30 @@ EAGLE_API eagle_status eagle_linear_bf16(const void *d_w, int64_t ldw, const voi
                                          int64_t ldy, int32_t out_bf16, void *d_ws,
                                          size_t ws_bytes, eagle_stream_t stream);
 
+/*
+ * The streamed-weight GEMM of eagle_linear_bf16 without caller-provided scratch.  The pages have
+ * no counterpart: this is an engineering variant for callers that cannot allocate device memory
+ * (code where cudaMalloc is not allowed or not wanted because it synchronises the device and can
+ * fail under memory pressure, plug-ins whose host framework owns all device memory, loops that
+ * must not allocate per call).  The caller passes only inputs and outputs, with the meaning and
+ * layout of eagle_linear_bf16.
+ *   - Scratch: a fixed array of eagle_linear_noalloc_scratch_bytes() bytes (about 5 MiB) in this
+ *     library's own device memory, held by every GPU that loads the library until exit.  The
+ *     first call on a device looks its address up (cudaGetSymbolAddress, with that device
+ *     current) and sets the kernel's attributes; make that first call before any stream capture.
+ *   - Limits: rows <= 32, out_features <= 131072, at most 160 CTAs; larger sizes return
+ *     EAGLE_ERR_INVALID_ARG.
+ *   - Every call shares the one array: each call clears the tile tickets it needs on its stream
+ *     before launching, but calls that overlap on the GPU (other streams, other threads) race.
+ *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ */
+EAGLE_API size_t eagle_linear_noalloc_scratch_bytes(void);
+EAGLE_API eagle_status eagle_linear_bf16_noalloc(const void *d_w, int64_t ldw, const void *d_x,
+                                                 int64_t ldx, const void *d_bias,
+                                                 int32_t out_features, int32_t in_features,
+                                                 int32_t rows, void *d_y, int64_t ldy,
+                                                 int32_t out_bf16, eagle_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
