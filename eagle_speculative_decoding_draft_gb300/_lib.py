@@ -61,9 +61,8 @@ _SIGS = {
     "eagle_tree_destroy": (None, [c_void_p]),
     "eagle_status_str": (ctypes.c_char_p, [c_int]),
     "eagle_tree_get_layout": (c_int, [c_void_p, POINTER(TreeLayout)]),
-    "eagle_row_topk_workspace_bytes": (c_size_t, [c_int32, c_int32, c_int32]),
     "eagle_row_topk": (c_int, [c_void_p, c_int, c_int32, c_int32, c_int64, c_int32, c_void_p,
-                               c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+                               c_void_p, c_void_p, c_void_p]),
     "eagle_expand": (c_int, [c_int32, c_int32, c_int32, c_int32] + [c_void_p] * 10 + [c_void_p]),
     "eagle_build_tree": (c_int, [c_int32, c_int32, c_int32, c_int32] + [c_void_p] * 11
                          + [c_void_p]),

@@ -27,7 +27,7 @@ int32_t round16(int32_t x) { return (x + 15) / 16 * 16; }
 struct Layout {
     size_t status, counters, partials, x, fhat, logits, row_ids, row_logp, row_lse;
     size_t pool_tok, pool_S, pool_par, pool_row, front_cand, front_S;
-    size_t root_tok, node_tok, node_src, g, node_x, node_fhat, topk_ws;
+    size_t root_tok, node_tok, node_src, g, node_x, node_fhat;
     size_t st_feat, st_tok, st_pos, st_tokens, st_parents, st_positions, st_mask, st_acc_len,
         st_acc_nodes, st_acc_tok;
     size_t total;
@@ -94,9 +94,6 @@ Layout make_layout(const eagle_tree_config *c, int32_t num_sms) {
     L.g = take(static_cast<size_t>(node_rows) * 4);
     L.node_x = take(static_cast<size_t>(L.node_chunk) * 2 * h * L.eb);
     L.node_fhat = take(static_cast<size_t>(L.node_chunk) * h * L.eb);
-    L.topk_ws = take(std::max(row_topk_scratch_bytes(L.r_pad, static_cast<int32_t>(V), static_cast<int32_t>(k)),
-                              row_topk_scratch_bytes(static_cast<int32_t>(std::max<int64_t>(node_rows, 1)),
-                                                     static_cast<int32_t>(V), 1)));
     L.st_feat = take(static_cast<size_t>(B) * h * L.eb);
     L.st_tok = take(static_cast<size_t>(B) * 4);
     L.st_pos = take(static_cast<size_t>(B) * 4);
@@ -404,8 +401,8 @@ eagle_status eagle_draft_level(eagle_tree *t, int32_t level, const void *d_root_
     }
     // log-softmax + top-k children of every row
     EAGLE_CUDA(launch_row_topk(lg, 0, R, V, V, k, t->at<int32_t>(L.row_ids), t->at<float>(L.row_logp),
-                               t->at<float>(L.row_lse), t->ws + L.topk_ws, st));
-    t->launches += 2;
+                               t->at<float>(L.row_lse), st));
+    ++t->launches;
     // expand: pool, next frontier, next level's rows
     const size_t fstride = static_cast<size_t>(B) * k;
     ExpandArgs e{};
@@ -500,8 +497,8 @@ eagle_status eagle_verify_greedy(eagle_tree *t, const int32_t *d_tokens, const i
     if (d_target_logits) {
         int32_t *gw = t->at<int32_t>(t->L.g);
         EAGLE_CUDA(launch_row_topk(d_target_logits, target_dtype == EAGLE_BF16, c.batch * n, c.vocab, c.vocab, 1,
-                                   gw, nullptr, nullptr, t->ws + t->L.topk_ws, st));
-        t->launches += 2;
+                                   gw, nullptr, nullptr, st));
+        ++t->launches;
         g = gw;
     }
     EAGLE_CUDA(launch_verify_walk(c.batch, n, c.depth, d_tokens, d_parents, g, d_accept_len, d_accept_nodes,
@@ -661,21 +658,13 @@ int64_t eagle_tree_launch_count(const eagle_tree *t) { return t ? t->launches : 
 // Stateless entry points
 // ------------------------------------------------------------------------------------------------
 
-size_t eagle_row_topk_workspace_bytes(int32_t rows, int32_t vocab, int32_t k) {
-    if (rows < 0 || vocab < 1 || k < 1 || k > kMaxTopk || k > vocab) return 0;
-    return row_topk_scratch_bytes(std::max(rows, 1), vocab, k);
-}
-
 eagle_status eagle_row_topk(const void *d_logits, eagle_dtype dtype, int32_t rows, int32_t vocab, int64_t ld,
-                            int32_t k, int32_t *d_ids, float *d_vals, float *d_lse, void *d_ws,
-                            size_t ws_bytes, eagle_stream_t stream) {
+                            int32_t k, int32_t *d_ids, float *d_vals, float *d_lse, eagle_stream_t stream) {
     if (rows < 0 || vocab < 1 || ld < vocab || k < 1 || k > kMaxTopk || k > vocab) return EAGLE_ERR_INVALID_ARG;
     if (dtype != EAGLE_F32 && dtype != EAGLE_BF16) return EAGLE_ERR_INVALID_ARG;
     if (rows == 0) return EAGLE_OK;
-    if (!d_logits || !d_ids || !d_ws) return EAGLE_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(d_ws) & 15u) != 0) return EAGLE_ERR_INVALID_ARG;
-    if (ws_bytes < row_topk_scratch_bytes(rows, vocab, k)) return EAGLE_ERR_INVALID_ARG;
-    EAGLE_CUDA(launch_row_topk(d_logits, dtype == EAGLE_BF16, rows, vocab, ld, k, d_ids, d_vals, d_lse, d_ws,
+    if (!d_logits || !d_ids) return EAGLE_ERR_INVALID_ARG;
+    EAGLE_CUDA(launch_row_topk(d_logits, dtype == EAGLE_BF16, rows, vocab, ld, k, d_ids, d_vals, d_lse,
                                reinterpret_cast<cudaStream_t>(stream)));
     return EAGLE_OK;
 }

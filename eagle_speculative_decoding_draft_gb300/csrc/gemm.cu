@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t total = static_cast<int64_t>(a.num_tiles) * nkb;
     const int64_t kb_begin = total * g / G, kb_end = total * (g + 1) / G;
 
+    pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&ctl->full[s], 1);
@@ -118,8 +119,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------- TMA producer ----------------
             const uint64_t pol_w = policy_evict_first();  // weights: streamed once
             const uint64_t pol_x = policy_evict_last();   // activation rows: read by every CTA
-            uint32_t stage = 0, phase = 0;
-            for (int64_t kb = kb_begin; kb < kb_end; ++kb) {
+            // The weights do not depend on the previous kernel: fill the whole ring with weight
+            // tiles first, then wait for the previous kernel and add the activation slices.
+            const int64_t n_pre = min(static_cast<int64_t>(stages), kb_end - kb_begin);
+            for (int64_t i = 0; i < n_pre; ++i) {
+                const int64_t kb = kb_begin + i;
+                const int32_t tile = static_cast<int32_t>(kb / nkb);
+                const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(tile) * nkb) * BK;
+                mbar_arrive_expect_tx(&ctl->full[i], kABytes + b_bytes);
+                tma_load_2d(a_tiles + static_cast<size_t>(i) * kABytes, &tmap_w, &ctl->full[i], kx,
+                            tile * BM, pol_w);
+                issued |= 1u << i;
+            }
+            pdl_wait();
+            for (int64_t i = 0; i < n_pre; ++i) {
+                const int64_t kb = kb_begin + i;
+                const int32_t tile = static_cast<int32_t>(kb / nkb);
+                const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(tile) * nkb) * BK;
+                tma_load_2d(b_tiles + static_cast<size_t>(i) * b_bytes, &tmap_x, &ctl->full[i], kx, 0,
+                            pol_x);
+            }
+            uint32_t stage = static_cast<uint32_t>(n_pre % stages);
+            uint32_t phase = (n_pre == stages) ? 1u : 0u;
+            for (int64_t kb = kb_begin + n_pre; kb < kb_end; ++kb) {
                 const int32_t tile = static_cast<int32_t>(kb / nkb);
                 const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(tile) * nkb) * BK;
                 if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
@@ -190,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ---------------- epilogue: warps 2..5, TMEM lane quarter = warp % 4 ----------------
+        pdl_wait();  // partials, tickets and outputs may still be in use by the previous kernel
         const int32_t q = warp & 3;
         const int32_t m_local = q * 32 + lane;
         uint32_t acc = 0, acc_phase = 0;
@@ -328,6 +351,8 @@ __global__ void __launch_bounds__(256)
     linear_f32_kernel(const float *__restrict__ w, int64_t ldw, const float *__restrict__ x,
                       int64_t ldx, const float *__restrict__ bias, float *__restrict__ y,
                       int64_t ldy, int32_t M, int32_t K, int32_t rows) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int32_t o = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int32_t lane = threadIdx.x & 31;
     if (o >= M) return;
@@ -467,8 +492,8 @@ cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
     a.partials = p.partials;
     a.counters = p.counters;
     a.status = p.status;
-    linear_bf16_tc_kernel<<<p.grid, kThreads, p.smem_bytes, st>>>(p.tmap_w, p.tmap_x, a);
-    return cudaGetLastError();
+    return launch_pdl(linear_bf16_tc_kernel, dim3(p.grid), dim3(kThreads), p.smem_bytes, st, p.tmap_w,
+                      p.tmap_x, a);
 }
 
 cudaError_t launch_linear_f32(const float *w, int64_t ldw, const float *x, int64_t ldx,
@@ -476,9 +501,8 @@ cudaError_t launch_linear_f32(const float *w, int64_t ldw, const float *x, int64
                               int32_t rows, cudaStream_t st) {
     if (M < 1 || rows < 1) return cudaSuccess;
     const int warps = 8;
-    linear_f32_kernel<<<(M + warps - 1) / warps, warps * 32, 0, st>>>(w, ldw, x, ldx, bias, y, ldy, M,
-                                                                      K, rows);
-    return cudaGetLastError();
+    return launch_pdl(linear_f32_kernel, dim3((M + warps - 1) / warps), dim3(warps * 32), 0, st, w, ldw, x,
+                      ldx, bias, y, ldy, M, K, rows);
 }
 
 }  // namespace eagle

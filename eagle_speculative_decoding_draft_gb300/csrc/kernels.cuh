@@ -3,10 +3,30 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace eagle {
+
+// Launches `kernel` allowing programmatic dependent launch: it may start while the previous
+// kernel in the stream is still running.  Every kernel of this library calls griddepcontrol.wait
+// before it touches memory a previous kernel may write or read, and launch_dependents early.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------------------------------------
 // Streamed-weight GEMM (FC and LM head), bf16 on the tensor cores:
@@ -55,12 +75,10 @@ cudaError_t launch_linear_f32(const float *w, int64_t ldw, const float *x, int64
                               int32_t rows, cudaStream_t st);
 
 // ---------------------------------------------------------------------------------------------
-// Per-row log-softmax + top-k (k <= 16), or argmax (k = 1, lse == null).  Two launches (chunk
-// partials, then a per-row merge); `ws` holds the partials (row_topk_scratch_bytes).
+// Per-row log-softmax + top-k (k <= 16), or argmax (k = 1, lse == null); one CTA per row.
 // ---------------------------------------------------------------------------------------------
-size_t row_topk_scratch_bytes(int32_t rows, int32_t V, int32_t k);
 cudaError_t launch_row_topk(const void *logits, int32_t is_bf16, int32_t rows, int32_t V,
-                            int64_t ld, int32_t k, int32_t *ids, float *vals, float *lse, void *ws,
+                            int64_t ld, int32_t k, int32_t *ids, float *vals, float *lse,
                             cudaStream_t st);
 
 // ---------------------------------------------------------------------------------------------
@@ -106,7 +124,6 @@ cudaError_t prepare_tree_kernels();
 cudaError_t launch_verify_walk(int32_t B, int32_t n, int32_t d, const int32_t *tok,
                                const int32_t *par, const int32_t *g, int32_t *accept_len,
                                int32_t *accept_nodes, int32_t *accept_tok, cudaStream_t st);
-
 // X[r] = [feature(src[r]) || E[tok[r]]]: src[r] >= 0 is a row of fhat_all, -1-b is row b of
 // root_feat; src == null means src[r] = -1-r.
 struct GatherArgs {

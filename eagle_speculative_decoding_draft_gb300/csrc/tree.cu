@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(kExpandThreads) expand_kernel(const ExpandArgs
     __shared__ float sS[256];
     __shared__ int32_t sTok[256], sRow[256], sC[256];
     __shared__ int32_t slot[16];
+    pdl_wait();
+    pdl_launch_dependents();
     const int32_t b = blockIdx.x, t = threadIdx.x, k = a.k, kk = a.k * a.k;
     const int32_t nl = (a.level == 0) ? k : kk;
     if (t < nl) {
@@ -110,6 +112,8 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(const BuildAr
     int32_t *sIdx = sPar + nc;  // tree index of a kept candidate, 0 if not kept
     int32_t *tPar = sIdx + nc;  // parent tree index of each node
     __shared__ int32_t warp_cnt[kBuildThreads / 32], warp_off[kBuildThreads / 32], running;
+    pdl_wait();
+    pdl_launch_dependents();
 
     const int32_t b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int64_t pb = static_cast<int64_t>(b) * nc;
@@ -204,6 +208,8 @@ __global__ void __launch_bounds__(128)
     verify_walk_kernel(int32_t B, int32_t n, int32_t d, const int32_t *__restrict__ tok,
                        const int32_t *__restrict__ par, const int32_t *__restrict__ g,
                        int32_t *accept_len, int32_t *accept_nodes, int32_t *accept_tok) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int32_t b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int32_t lane = threadIdx.x & 31;
     if (b >= B) return;
@@ -244,6 +250,8 @@ __global__ void __launch_bounds__(128)
 // Row gather: X[r] = [feature || E[token]].
 // ---------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int32_t r = blockIdx.x;
     const int32_t si = a.src ? a.src[r] : -1 - r;
     int32_t tok = a.tok[r];
@@ -274,15 +282,13 @@ cudaError_t launch_expand(const ExpandArgs &a, cudaStream_t st) {
         if (y < 1) y = 1;
         if (y > 64) y = 64;
     }
-    expand_kernel<<<dim3(a.B, y), kExpandThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(expand_kernel, dim3(a.B, y), dim3(kExpandThreads), 0, st, a);
 }
 
 cudaError_t launch_build_tree(const BuildArgs &a, cudaStream_t st) {
     if (a.B < 1) return cudaSuccess;
     const size_t smem = (3 * static_cast<size_t>(a.n_cand) + a.m + 1) * sizeof(int32_t);
-    build_tree_kernel<<<a.B, kBuildThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(build_tree_kernel, dim3(a.B), dim3(kBuildThreads), smem, st, a);
 }
 
 cudaError_t prepare_tree_kernels() {
@@ -294,9 +300,8 @@ cudaError_t launch_verify_walk(int32_t B, int32_t n, int32_t d, const int32_t *t
                                const int32_t *g, int32_t *accept_len, int32_t *accept_nodes,
                                int32_t *accept_tok, cudaStream_t st) {
     if (B < 1) return cudaSuccess;
-    verify_walk_kernel<<<(B + 3) / 4, 128, 0, st>>>(B, n, d, tok, par, g, accept_len, accept_nodes,
-                                                    accept_tok);
-    return cudaGetLastError();
+    return launch_pdl(verify_walk_kernel, dim3((B + 3) / 4), dim3(128), 0, st, B, n, d, tok, par, g, accept_len,
+                      accept_nodes, accept_tok);
 }
 
 cudaError_t launch_gather(const GatherArgs &a, cudaStream_t st) {
@@ -304,8 +309,7 @@ cudaError_t launch_gather(const GatherArgs &a, cudaStream_t st) {
     const int64_t bytes = 2LL * a.h * a.elem_bytes;
     int32_t y = static_cast<int32_t>((bytes + 4095) / 4096);
     if (y < 1) y = 1;
-    gather_kernel<<<dim3(a.n_rows, y), 256, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(gather_kernel, dim3(a.n_rows, y), dim3(256), 0, st, a);
 }
 
 }  // namespace eagle

@@ -256,11 +256,8 @@ def row_topk(logits, k: int, with_lse: bool = True, stream=None):
     ids = torch.empty(rows, k, dtype=torch.int32, device=dev)
     vals = torch.empty(rows, k, dtype=torch.float32, device=dev)
     lse = torch.empty(rows, dtype=torch.float32, device=dev) if with_lse else None
-    nbytes = lib.eagle_row_topk_workspace_bytes(rows, V, k)
-    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
     check(lib.eagle_row_topk(_ptr(logits), _dtype_code(logits.dtype), rows, V, ld, k, _ptr(ids),
-                             _ptr(vals), _ptr(lse), _ptr(ws), nbytes, _stream(dev, stream)),
-          "eagle_row_topk")
+                             _ptr(vals), _ptr(lse), _stream(dev, stream)), "eagle_row_topk")
     return ids, vals, lse
 
 

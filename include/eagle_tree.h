@@ -264,14 +264,10 @@ EAGLE_API int64_t eagle_tree_launch_count(const eagle_tree *t);
  *   d_vals [rows][k]  value - lse when d_lse is given (log-probabilities), else the raw values
  *   d_lse [rows]      logsumexp of the row (fp32), or NULL
  * k in [1, 16], k <= vocab.  With k = 1 and no d_lse this is the target argmax of verify.
- * d_ws: scratch of at least eagle_row_topk_workspace_bytes(rows, vocab, k) bytes, 16-byte
- * aligned (per-chunk partial results; no initial contents needed).
  */
-EAGLE_API size_t eagle_row_topk_workspace_bytes(int32_t rows, int32_t vocab, int32_t k);
 EAGLE_API eagle_status eagle_row_topk(const void *d_logits, eagle_dtype dtype, int32_t rows,
                                       int32_t vocab, int64_t ld, int32_t k, int32_t *d_ids,
-                                      float *d_vals, float *d_lse, void *d_ws, size_t ws_bytes,
-                                      eagle_stream_t stream);
+                                      float *d_vals, float *d_lse, eagle_stream_t stream);
 
 /*
  * Expand one level for B requests, without features (zdszero "在 SGLang 里": select the top-k of
