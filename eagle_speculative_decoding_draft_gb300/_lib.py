@@ -68,6 +68,7 @@ _SIGS = {
                          + [c_void_p]),
     "eagle_verify_walk": (c_int, [c_int32, c_int32, c_int32] + [c_void_p] * 6 + [c_void_p]),
     "eagle_tree_profile": (c_int, [c_void_p, c_int32]),
+    "eagle_tree_profile_enable": (c_int, [c_void_p, c_int32]),
     "eagle_tree_profile_read": (c_int, [c_void_p, POINTER(c_int32), POINTER(ctypes.c_double),
                                         POINTER(ctypes.c_double)]),
     "eagle_tree_launch_count": (c_int64, [c_void_p]),

@@ -193,6 +193,7 @@ struct eagle_tree {
     std::vector<cudaEvent_t> prof_start, prof_stop;
     std::vector<double> prof_bytes;
     int32_t prof_n = 0;
+    bool prof_on = true;
 
     ~eagle_tree() { free_profile(); }
     void free_profile() {
@@ -205,7 +206,7 @@ struct eagle_tree {
     }
     // Launches one GEMM, bracketed by profiling events when enabled.
     cudaError_t gemm(const LinearPlan &p, cudaStream_t st) {
-        const bool timed = prof_n < static_cast<int32_t>(prof_start.size());
+        const bool timed = prof_on && prof_n < static_cast<int32_t>(prof_start.size());
         if (timed && cudaEventRecord(prof_start[prof_n], st) != cudaSuccess) return cudaErrorUnknown;
         cudaError_t e = launch_linear_bf16(p, st);
         ++launches;
@@ -649,6 +650,12 @@ eagle_status eagle_tree_profile_read(eagle_tree *t, int32_t *launches, double *t
     *total_ms = ms;
     *total_bytes = bytes;
     t->prof_n = 0;
+    return EAGLE_OK;
+}
+
+eagle_status eagle_tree_profile_enable(eagle_tree *t, int32_t enable) {
+    if (!t) return EAGLE_ERR_INVALID_ARG;
+    t->prof_on = enable != 0;
     return EAGLE_OK;
 }
 

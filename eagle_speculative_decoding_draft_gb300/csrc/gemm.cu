@@ -351,8 +351,8 @@ __global__ void __launch_bounds__(256)
     linear_f32_kernel(const float *__restrict__ w, int64_t ldw, const float *__restrict__ x,
                       int64_t ldx, const float *__restrict__ bias, float *__restrict__ y,
                       int64_t ldy, int32_t M, int32_t K, int32_t rows) {
+    pdl_launch_dependents();  // dependents still wait for this grid to finish
     pdl_wait();
-    pdl_launch_dependents();
     const int32_t o = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int32_t lane = threadIdx.x & 31;
     if (o >= M) return;

@@ -68,8 +68,8 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ int32_t s_count;
     __shared__ float r_v[kWarps];
     __shared__ int32_t r_i[kWarps];
+    pdl_launch_dependents();  // dependents still wait for this grid to finish
     pdl_wait();
-    pdl_launch_dependents();
     const int32_t row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const T *z = logits + static_cast<int64_t>(row) * ld;
     const bool want_lse = lse_out != nullptr;

@@ -32,8 +32,8 @@ __global__ void __launch_bounds__(kExpandThreads) expand_kernel(const ExpandArgs
     __shared__ float sS[256];
     __shared__ int32_t sTok[256], sRow[256], sC[256];
     __shared__ int32_t slot[16];
+    pdl_launch_dependents();  // dependents still wait for this grid to finish
     pdl_wait();
-    pdl_launch_dependents();
     const int32_t b = blockIdx.x, t = threadIdx.x, k = a.k, kk = a.k * a.k;
     const int32_t nl = (a.level == 0) ? k : kk;
     if (t < nl) {
@@ -112,8 +112,8 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(const BuildAr
     int32_t *sIdx = sPar + nc;  // tree index of a kept candidate, 0 if not kept
     int32_t *tPar = sIdx + nc;  // parent tree index of each node
     __shared__ int32_t warp_cnt[kBuildThreads / 32], warp_off[kBuildThreads / 32], running;
+    pdl_launch_dependents();  // dependents still wait for this grid to finish
     pdl_wait();
-    pdl_launch_dependents();
 
     const int32_t b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int64_t pb = static_cast<int64_t>(b) * nc;
@@ -208,8 +208,8 @@ __global__ void __launch_bounds__(128)
     verify_walk_kernel(int32_t B, int32_t n, int32_t d, const int32_t *__restrict__ tok,
                        const int32_t *__restrict__ par, const int32_t *__restrict__ g,
                        int32_t *accept_len, int32_t *accept_nodes, int32_t *accept_tok) {
+    pdl_launch_dependents();  // dependents still wait for this grid to finish
     pdl_wait();
-    pdl_launch_dependents();
     const int32_t b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int32_t lane = threadIdx.x & 31;
     if (b >= B) return;
@@ -250,8 +250,8 @@ __global__ void __launch_bounds__(128)
 // Row gather: X[r] = [feature || E[token]].
 // ---------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
+    pdl_launch_dependents();  // dependents still wait for this grid to finish
     pdl_wait();
-    pdl_launch_dependents();
     const int32_t r = blockIdx.x;
     const int32_t si = a.src ? a.src[r] : -1 - r;
     int32_t tok = a.tok[r];

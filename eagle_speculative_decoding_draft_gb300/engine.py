@@ -194,6 +194,10 @@ class EagleTree:
         """Time the next max_launches GEMM launches with CUDA events (0 stops)."""
         check(self.lib.eagle_tree_profile(self._h, int(max_launches)), "eagle_tree_profile")
 
+    def profile_enable(self, on: bool):
+        """Pause or resume the GEMM launch timing (the events stay allocated)."""
+        check(self.lib.eagle_tree_profile_enable(self._h, int(bool(on))), "eagle_tree_profile_enable")
+
     def profile_read(self):
         """(launches, total_ms, total_algorithmic_bytes) of the GEMM launches timed so far."""
         n = ctypes.c_int32()

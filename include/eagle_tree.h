@@ -249,6 +249,10 @@ EAGLE_API eagle_status eagle_tree_get_layout(const eagle_tree *t, eagle_tree_lay
  * eagle_tree_launch_count returns how many kernels this handle has launched since init.
  */
 EAGLE_API eagle_status eagle_tree_profile(eagle_tree *t, int32_t max_launches);
+/* Pauses (enable = 0) or resumes the timing of GEMM launches without freeing the events.  Each
+ * timed launch is bracketed by events on its stream, which keeps it from overlapping the
+ * previous kernel, so a caller that wants the overlapped throughput times only some steps. */
+EAGLE_API eagle_status eagle_tree_profile_enable(eagle_tree *t, int32_t enable);
 EAGLE_API eagle_status eagle_tree_profile_read(eagle_tree *t, int32_t *launches, double *total_ms,
                                                double *total_bytes);
 EAGLE_API int64_t eagle_tree_launch_count(const eagle_tree *t);
