@@ -22,6 +22,13 @@ enum : int32_t {
 // Wall-clock limit of every wait, in nanoseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// Atomic add at GPU scope with release (earlier writes) and acquire (later reads) semantics.
+__device__ __forceinline__ int32_t atomic_add_acq_rel_gpu(int32_t *p, int32_t v) {
+    int32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void latch(int32_t *status, int32_t bits) {
     if (status) atomicOr(status, bits);
 }
@@ -83,6 +90,42 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
         if (abort && *abort) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Thread-block clusters: rank, size, barrier and loads from a peer CTA's shared memory
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    return n;
+}
+// Every thread of every CTA of the cluster; orders shared-memory writes before it against reads
+// after it, across the cluster.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+// Address of `p` (a shared variable of this CTA) in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    return a;
+}
+__device__ __forceinline__ float ld_peer_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ int32_t ld_peer_s32(uint32_t a) {
+    int32_t v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -54,9 +54,17 @@ struct LinearArgs {
     int32_t *status;
 };
 
+// a / b for a >= 0, b > 0: one 32-bit division when a fits in 32 bits (64-bit division is a
+// long software sequence).
+__device__ __forceinline__ int64_t div_nonneg(int64_t a, int64_t b) {
+    if ((static_cast<uint64_t>(a) >> 32) == 0 && (static_cast<uint64_t>(b) >> 32) == 0)
+        return static_cast<uint32_t>(a) / static_cast<uint32_t>(b);
+    return a / b;
+}
+
 // CTA whose k-block range [total*g/G, total*(g+1)/G) contains k-block p.
 __device__ __forceinline__ int32_t cta_of(int64_t p, int64_t total, int32_t G) {
-    return static_cast<int32_t>(((p + 1) * G + total - 1) / total) - 1;
+    return static_cast<int32_t>(div_nonneg((p + 1) * G + total - 1, total)) - 1;
 }
 
 __device__ __forceinline__ void store_y(const LinearArgs &a, int32_t r, int32_t o, float v) {
@@ -84,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t G = gridDim.x, g = blockIdx.x;
     const int64_t nkb = a.num_kb;
     const int64_t total = static_cast<int64_t>(a.num_tiles) * nkb;
-    const int64_t kb_begin = total * g / G, kb_end = total * (g + 1) / G;
+    const int64_t kb_begin = div_nonneg(total * g, G), kb_end = div_nonneg(total * (g + 1), G);
 
     pdl_launch_dependents();
     if (threadIdx.x == 0) {
@@ -124,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t n_pre = min(static_cast<int64_t>(stages), kb_end - kb_begin);
             for (int64_t i = 0; i < n_pre; ++i) {
                 const int64_t kb = kb_begin + i;
-                const int32_t tile = static_cast<int32_t>(kb / nkb);
+                const int32_t tile = static_cast<int32_t>(div_nonneg(kb, nkb));
                 const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(tile) * nkb) * BK;
                 mbar_arrive_expect_tx(&ctl->full[i], kABytes + b_bytes);
                 tma_load_2d(a_tiles + static_cast<size_t>(i) * kABytes, &tmap_w, &ctl->full[i], kx,
@@ -134,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pdl_wait();
             for (int64_t i = 0; i < n_pre; ++i) {
                 const int64_t kb = kb_begin + i;
-                const int32_t tile = static_cast<int32_t>(kb / nkb);
+                const int32_t tile = static_cast<int32_t>(div_nonneg(kb, nkb));
                 const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(tile) * nkb) * BK;
                 tma_load_2d(b_tiles + static_cast<size_t>(i) * b_bytes, &tmap_x, &ctl->full[i], kx, 0,
                             pol_x);
@@ -142,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = static_cast<uint32_t>(n_pre % stages);
             uint32_t phase = (n_pre == stages) ? 1u : 0u;
             for (int64_t kb = kb_begin + n_pre; kb < kb_end; ++kb) {
-                const int32_t tile = static_cast<int32_t>(kb / nkb);
+                const int32_t tile = static_cast<int32_t>(div_nonneg(kb, nkb));
                 const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(tile) * nkb) * BK;
                 if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
                     *abort_flag = 1;
@@ -171,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int64_t kb = kb_begin; kb < kb_end && ok;) {
-                const int64_t tile = kb / nkb;
+                const int64_t tile = div_nonneg(kb, nkb);
                 const int64_t k1 = min(kb_end, (tile + 1) * nkb);
                 if (!mbar_wait(&ctl->acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
                     ok = false;
@@ -218,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc = 0, acc_phase = 0;
         bool first = true;
         for (int64_t kb = kb_begin; kb < kb_end;) {
-            const int32_t tile = static_cast<int32_t>(kb / nkb);
+            const int32_t tile = static_cast<int32_t>(div_nonneg(kb, nkb));
             const int64_t t0 = static_cast<int64_t>(tile) * nkb;
             const int64_t k1 = min(kb_end, t0 + nkb);
             const bool full = (kb == t0) && (k1 == t0 + nkb);
@@ -260,13 +268,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0 && got) mbar_arrive(&ctl->acc_empty[acc]);
             if (!full) {
-                __threadfence();
-                named_barrier_sync(1, 128);
+                named_barrier_sync(1, 128);  // this CTA's partials of the tile are written
                 const int32_t gf = cta_of(t0, total, G), gl = cta_of(t0 + nkb - 1, total, G);
                 if (threadIdx.x == 64) {
                     int32_t last = 0;
                     if (!*abort_flag) {
-                        const int32_t prev = atomicAdd(&a.counters[tile], 1);
+                        // release: the partials written before the barrier; acquire: the other
+                        // CTAs' partials, for the reads after the next barrier
+                        const int32_t prev = atomic_add_acq_rel_gpu(&a.counters[tile], 1);
                         last = (prev == gl - gf);
                         if (last) a.counters[tile] = 0;  // ready for the next launch
                     }
@@ -274,38 +283,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 named_barrier_sync(1, 128);
                 if (ctl->is_last) {
-                    __threadfence();
-                    // Sum the partials in ascending CTA order.  All loads of a batch of rows x
-                    // CTAs are issued before any is used, so the fix-up costs a few L2 round
-                    // trips instead of one per (row, CTA).
-                    constexpr int kRowsPerBatch = 8, kCtasPerBatch = 8;
-                    for (int32_t n0 = 0; n0 < a.rows; n0 += kRowsPerBatch) {
-                        float acc[kRowsPerBatch];
+                    // CTAs gf < g <= gl start inside this tile, so it is their first segment
+                    // (slot 0); CTA gf wrote slot 1 unless its range starts with this tile.
+                    const bool gf_second = div_nonneg(total * gf, G) < t0;
+                    // Sum the partials in ascending CTA order.  Thread e of the 128 sums outputs
+                    // 4(e % 32) .. +3 of rows e / 32, +4, +8, ...; all loads of a batch of rows x
+                    // CTAs are issued before any is used, so the fix-up costs one L2 round trip
+                    // per batch instead of one per (row, CTA).
+                    const int32_t et = static_cast<int32_t>(threadIdx.x) - 64;
+                    const int32_t m4 = (et & 31) * 4, rsub = et >> 5;
+                    float b4[4];
 #pragma unroll
-                        for (int j = 0; j < kRowsPerBatch; ++j) acc[j] = 0.0f;
+                    for (int q = 0; q < 4; ++q) {
+                        const int32_t oq = tile * BM + m4 + q;
+                        b4[q] = (a.bias != nullptr && oq < a.M) ? __bfloat162float(a.bias[oq]) : 0.0f;
+                    }
+                    constexpr int kRowsPerBatch = 2, kCtasPerBatch = 8;  // per thread
+                    for (int32_t n0 = rsub; n0 < a.rows; n0 += 4 * kRowsPerBatch) {
+                        float4 sum[kRowsPerBatch];
                         for (int32_t g0 = gf; g0 <= gl; g0 += kCtasPerBatch) {
-                            float x[kCtasPerBatch][kRowsPerBatch];
+                            float4 x[kCtasPerBatch][kRowsPerBatch];
 #pragma unroll
                             for (int c = 0; c < kCtasPerBatch; ++c) {
                                 const int32_t gg = g0 + c;
-                                const int32_t slot =
-                                    ((total * gg / G) / nkb == static_cast<int64_t>(tile)) ? 0 : 1;
-                                const float *src = a.partials +
-                                    (static_cast<size_t>(gg * 2 + slot) * a.n_tile + n0) * BM + m_local;
+                                const int32_t slot = (gg == gf && gf_second) ? 1 : 0;
+                                const float *src =
+                                    a.partials + static_cast<size_t>(gg * 2 + slot) * a.n_tile * BM + m4;
 #pragma unroll
-                                for (int j = 0; j < kRowsPerBatch; ++j)
-                                    x[c][j] = (gg <= gl && n0 + j < a.rows)
-                                                  ? __ldcg(src + static_cast<size_t>(j) * BM) : 0.0f;
+                                for (int j = 0; j < kRowsPerBatch; ++j) {
+                                    const int32_t n = n0 + 4 * j;
+                                    x[c][j] = (gg <= gl && n < a.rows)
+                                                  ? __ldcg(reinterpret_cast<const float4 *>(
+                                                        src + static_cast<size_t>(n) * BM))
+                                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                                }
                             }
 #pragma unroll
                             for (int c = 0; c < kCtasPerBatch; ++c)
 #pragma unroll
-                                for (int j = 0; j < kRowsPerBatch; ++j)
-                                    if (g0 + c <= gl) acc[j] = (g0 + c == gf) ? x[c][j] : acc[j] + x[c][j];
+                                for (int j = 0; j < kRowsPerBatch; ++j) {
+                                    if (g0 + c > gl) continue;
+                                    if (g0 + c == gf) {
+                                        sum[j] = x[c][j];
+                                    } else {
+                                        sum[j].x += x[c][j].x;
+                                        sum[j].y += x[c][j].y;
+                                        sum[j].z += x[c][j].z;
+                                        sum[j].w += x[c][j].w;
+                                    }
+                                }
                         }
 #pragma unroll
-                        for (int j = 0; j < kRowsPerBatch; ++j)
-                            if (o_ok && n0 + j < a.rows) store_y(a, n0 + j, o, acc[j] + bias_o);
+                        for (int j = 0; j < kRowsPerBatch; ++j) {
+                            const int32_t n = n0 + 4 * j;
+                            if (n >= a.rows) continue;
+                            const float v[4] = {sum[j].x, sum[j].y, sum[j].z, sum[j].w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                if (tile * BM + m4 + q < a.M) store_y(a, n, tile * BM + m4 + q, v[q] + b4[q]);
+                        }
                     }
                 }
                 named_barrier_sync(1, 128);

@@ -4,15 +4,21 @@
 // and every expanded node keeps its k most probable children.  Order: value descending, column
 // ascending.  With k = 1 and no lse this is the target argmax of greedy verification.
 //
-// One CTA per row, two passes over the row (the second one hits L2):
-//   pass 1  every thread takes the max of its elements; the row max M is the block max, and the
-//           threshold tau is the largest, over warps, of the warp's k-th largest thread max: that
-//           warp alone has k elements >= tau, so every element of the top k is >= tau.
-//   pass 2  sum of exp2((x - M) log2 e) for the logsumexp, and every element >= tau (usually a
-//           few more than k) is appended to a shared candidate list.
-//   select  one warp sorts the candidates with bitonic networks and keeps the first k.
-// A row with more than kCand elements >= tau (massive ties) falls back to k exact block-wide
-// arg-max passes.
+// One thread-block cluster of C CTAs (C <= 8) per row; CTA r owns the r-th slice of the row and
+// reads it from memory once, into registers:
+//   pass 1  every thread takes the max of its elements.  The slice max and the slice threshold
+//           (the largest, over warps, of the warp's k-th largest thread max: that warp alone has
+//           k elements >= it) go to the CTA's shared memory; after a cluster barrier every CTA
+//           takes the row max M and the row threshold tau as the max over the cluster.  Every
+//           element of the row's top k is >= tau.
+//   pass 2  from the registers: sum of exp2((x - M) log2 e) for the logsumexp, and every
+//           element >= tau is appended to a shared candidate list; one warp sorts it with
+//           bitonic networks and keeps the slice's best k.
+//   merge   after a second cluster barrier, rank 0 reads the C sorted lists and sums from its
+//           peers' shared memory, merges them and writes the row's top k and logsumexp; a third
+//           barrier keeps every CTA's shared memory alive until rank 0 has read it.
+// A slice with more than kCand elements >= tau (massive ties) falls back to k exact block-wide
+// arg-max passes over that slice.
 #include <cfloat>
 #include <climits>
 
@@ -26,57 +32,88 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCand = 256;
+constexpr int kMaxCluster = 8;
+constexpr int kCacheVec = 4;  // 16-byte vectors per thread held in registers between the passes
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 
-// Calls f(x, index) for every element of the row; 16-byte loads when the row is aligned.
+// This CTA's part of the row: 16-byte vectors [vbeg, vend) and scalar elements [sbeg, send).
+struct Slice {
+    int32_t vbeg, vend, sbeg, send;
+};
+
+// Calls f(x, column) for every element of the slice: the first kCacheVec vectors of each thread
+// come from `cache`, the rest (very long rows) and the scalar part from memory.
 template <typename T, typename F>
-__device__ __forceinline__ void for_each(const T *z, int32_t V, int32_t tid, F &&f) {
+__device__ __forceinline__ void visit(const T *z, const uint4 (&cache)[kCacheVec], const Slice &s,
+                                      int32_t tid, F &&f) {
     constexpr int EPV = 16 / sizeof(T);
-    const bool vec = (reinterpret_cast<uintptr_t>(z) % 16) == 0;
-    const int32_t nvec = vec ? V / EPV : 0;
-    int32_t c = tid;
-    for (; c + 3 * kThreads < nvec; c += 4 * kThreads) {
-        uint4 raw[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) raw[u] = __ldg(reinterpret_cast<const uint4 *>(z) + c + u * kThreads);
+    for (int u = 0; u < kCacheVec; ++u) {
+        const int32_t c = s.vbeg + tid + u * kThreads;
+        if (c < s.vend) {
+            const T *e = reinterpret_cast<const T *>(&cache[u]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const T *e = reinterpret_cast<const T *>(&raw[u]);
-#pragma unroll
-            for (int j = 0; j < EPV; ++j) f(to_f32(e[j]), (c + u * kThreads) * EPV + j);
+            for (int j = 0; j < EPV; ++j) f(to_f32(e[j]), c * EPV + j);
         }
     }
-    for (; c < nvec; c += kThreads) {
+    for (int32_t c = s.vbeg + kCacheVec * kThreads + tid; c < s.vend; c += kThreads) {
         const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(z) + c);
         const T *e = reinterpret_cast<const T *>(&raw);
 #pragma unroll
         for (int j = 0; j < EPV; ++j) f(to_f32(e[j]), c * EPV + j);
     }
-    for (int32_t id = nvec * EPV + tid; id < V; id += kThreads) f(to_f32(z[id]), id);
+    for (int32_t i = s.sbeg + tid; i < s.send; i += kThreads) f(to_f32(z[i]), i);
 }
 
+// Two CTAs per SM (64 registers a thread), so the CTAs of the next launch fit beside a GEMM CTA.
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
     row_topk_kernel(const T *__restrict__ logits, int32_t V, int64_t ld, int32_t k,
                     int32_t *__restrict__ ids, float *__restrict__ vals, float *__restrict__ lse_out) {
+    constexpr int EPV = 16 / sizeof(T);
     __shared__ float s_max[kWarps], s_kth[kWarps], s_sum[kWarps];
     __shared__ float c_v[kCand];
     __shared__ int32_t c_i[kCand];
     __shared__ int32_t s_count;
     __shared__ float r_v[kWarps];
     __shared__ int32_t r_i[kWarps];
+    __shared__ float s_row[2];  // row max and threshold over the cluster
+    // read by the cluster's other CTAs
+    __shared__ float x_stat[2];  // this slice's max and threshold
+    __shared__ float x_sum;      // this slice's sum of exp relative to the row max
+    __shared__ float x_v[16];    // this slice's best k, sorted
+    __shared__ int32_t x_i[16];
     pdl_launch_dependents();  // dependents still wait for this grid to finish
     pdl_wait();
-    const int32_t row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t C = cluster_size(), rank = cluster_rank();
+    const int32_t row = blockIdx.x / C, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const T *z = logits + static_cast<int64_t>(row) * ld;
     const bool want_lse = lse_out != nullptr;
 
-    // ---- pass 1: thread max, row max, threshold ----
+    // ---- this CTA's slice, loaded once ----
+    const bool vec = (reinterpret_cast<uintptr_t>(z) % 16) == 0;
+    const int32_t nvec = vec ? V / EPV : 0;
+    const int32_t per = (nvec + static_cast<int32_t>(C) - 1) / static_cast<int32_t>(C);
+    const int32_t rem = V - nvec * EPV;
+    const int32_t sper = (rem + static_cast<int32_t>(C) - 1) / static_cast<int32_t>(C);
+    Slice sl;
+    sl.vbeg = min(nvec, static_cast<int32_t>(rank) * per);
+    sl.vend = min(nvec, sl.vbeg + per);
+    sl.sbeg = nvec * EPV + min(rem, static_cast<int32_t>(rank) * sper);
+    sl.send = nvec * EPV + min(rem, static_cast<int32_t>(rank) * sper + sper);
+    uint4 cache[kCacheVec];
+#pragma unroll
+    for (int u = 0; u < kCacheVec; ++u) {
+        const int32_t c = sl.vbeg + tid + u * kThreads;
+        cache[u] = (c < sl.vend) ? __ldg(reinterpret_cast<const uint4 *>(z) + c) : make_uint4(0, 0, 0, 0);
+    }
+
+    // ---- pass 1: thread max; slice max and threshold; row max and threshold ----
     float tmax = -INFINITY;
-    for_each(z, V, tid, [&](float x, int32_t) { tmax = fmaxf(tmax, x); });
+    visit(z, cache, sl, tid, [&](float x, int32_t) { tmax = fmaxf(tmax, x); });
     const float sorted = warp_sort_values(tmax, lane);
     const float wmax = __shfl_sync(kFullMask, sorted, 0);
     const float wkth = __shfl_sync(kFullMask, sorted, k - 1);
@@ -86,17 +123,39 @@ __global__ void __launch_bounds__(kThreads)
     }
     if (tid == 0) s_count = 0;
     __syncthreads();
-    float M = -INFINITY, tau = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        M = fmaxf(M, s_max[w]);
-        tau = fmaxf(tau, s_kth[w]);
+    if (tid == 0) {
+        float m = -INFINITY, t = -INFINITY;
+        for (int w = 0; w < kWarps; ++w) {
+            m = fmaxf(m, s_max[w]);
+            t = fmaxf(t, s_kth[w]);
+        }
+        x_stat[0] = m;
+        x_stat[1] = t;
     }
+    cluster_sync();
+    if (warp == 0) {
+        float m = -INFINITY, t = -INFINITY;
+        if (lane < static_cast<int>(C)) {
+            m = ld_peer_f32(peer_addr(&x_stat[0], lane));
+            t = ld_peer_f32(peer_addr(&x_stat[1], lane));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            m = fmaxf(m, __shfl_xor_sync(kFullMask, m, off));
+            t = fmaxf(t, __shfl_xor_sync(kFullMask, t, off));
+        }
+        if (lane == 0) {
+            s_row[0] = m;
+            s_row[1] = t;
+        }
+    }
+    __syncthreads();
+    const float M = s_row[0], tau = s_row[1];
 
     // ---- pass 2: sum of exp, candidates >= tau ----
     float sum = 0.0f;
     const float Ms = (M == -INFINITY) ? 0.0f : M * kLog2e;
-    for_each(z, V, tid, [&](float x, int32_t id) {
+    visit(z, cache, sl, tid, [&](float x, int32_t id) {
         if (want_lse) sum += exp2f(fmaf(x, kLog2e, -Ms));
         if (x >= tau) {
             const int32_t pos = atomicAdd(&s_count, 1);
@@ -106,22 +165,18 @@ __global__ void __launch_bounds__(kThreads)
             }
         }
     });
-    if (want_lse) {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFullMask, sum, off);
-        if (lane == 0) s_sum[warp] = sum;
-    }
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFullMask, sum, off);
+    if (lane == 0) s_sum[warp] = sum;
     __syncthreads();
     const int32_t count = s_count;
-    float lse = 0.0f;
-    if (want_lse) {
+    if (tid == 0) {
         float tot = 0.0f;
-#pragma unroll
         for (int w = 0; w < kWarps; ++w) tot += s_sum[w];
-        lse = M + logf(tot);
+        x_sum = tot;
     }
 
-    // ---- select the top k ----
+    // ---- this slice's best k ----
     if (count <= kCand) {
         if (warp == 0) {
             float v = -INFINITY;
@@ -137,55 +192,87 @@ __global__ void __launch_bounds__(kThreads)
                     warp_merge_sorted(v, i, bv, bi, lane);
                 }
             }
+            if (lane < 16) {
+                x_v[lane] = v;
+                x_i[lane] = i;
+            }
+        }
+    } else {
+        // massive ties at the threshold: k exact passes, each the best element after the last pick
+        float pv = INFINITY;
+        int32_t pi = -1;
+        for (int32_t j = 0; j < k; ++j) {
+            float bv = -INFINITY;
+            int32_t bi = INT_MAX;
+            visit(z, cache, sl, tid, [&](float x, int32_t id) {
+                const bool after = before_nb(pv, pi, x, id);  // ranks after the previous pick
+                if (after && before_nb(x, id, bv, bi)) {
+                    bv = x;
+                    bi = id;
+                }
+            });
+            warp_best(bv, bi);
+            if (lane == 0) {
+                r_v[warp] = bv;
+                r_i[warp] = bi;
+            }
+            __syncthreads();
+            bv = r_v[0];
+            bi = r_i[0];
+            for (int w = 1; w < kWarps; ++w)
+                if (before_nb(r_v[w], r_i[w], bv, bi)) {
+                    bv = r_v[w];
+                    bi = r_i[w];
+                }
+            __syncthreads();
+            if (tid == 0) {
+                x_v[j] = bv;
+                x_i[j] = bi;
+            }
+            pv = bv;
+            pi = bi;
+        }
+    }
+    cluster_sync();
+
+    // ---- rank 0 merges the slices ----
+    if (rank == 0 && warp == 0) {
+        float v = (lane < k) ? x_v[lane] : -INFINITY;
+        int32_t i = (lane < k) ? x_i[lane] : INT_MAX;
+        float tot = (lane < static_cast<int>(C)) ? ld_peer_f32(peer_addr(&x_sum, lane)) : 0.0f;
+        for (uint32_t p = 1; p < C; ++p) {
+            float pv = -INFINITY;
+            int32_t pi = INT_MAX;
             if (lane < k) {
-                ids[static_cast<int64_t>(row) * k + lane] = i;
-                if (vals) vals[static_cast<int64_t>(row) * k + lane] = want_lse ? v - lse : v;
+                pv = ld_peer_f32(peer_addr(&x_v[lane], p));
+                pi = ld_peer_s32(peer_addr(&x_i[lane], p));
             }
-            if (want_lse && lane == 0) lse_out[row] = lse;
+            warp_merge_sorted(v, i, pv, pi, lane);
         }
-        return;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(kFullMask, tot, off);
+        const float lse = want_lse ? M + logf(tot) : 0.0f;
+        if (lane < k) {
+            ids[static_cast<int64_t>(row) * k + lane] = i;
+            if (vals) vals[static_cast<int64_t>(row) * k + lane] = want_lse ? v - lse : v;
+        }
+        if (want_lse && lane == 0) lse_out[row] = lse;
     }
-    // massive ties at the threshold: k exact passes, each the best element after the previous pick
-    float pv = INFINITY;
-    int32_t pi = -1;
-    for (int32_t j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int32_t bi = INT_MAX;
-        for_each(z, V, tid, [&](float x, int32_t id) {
-            const bool after = before_nb(pv, pi, x, id);  // ranks after the previous pick
-            if (after && before_nb(x, id, bv, bi)) {
-                bv = x;
-                bi = id;
-            }
-        });
-        warp_best(bv, bi);
-        if (lane == 0) {
-            r_v[warp] = bv;
-            r_i[warp] = bi;
-        }
-        __syncthreads();
-        bv = r_v[0];
-        bi = r_i[0];
-        for (int w = 1; w < kWarps; ++w)
-            if (before_nb(r_v[w], r_i[w], bv, bi)) {
-                bv = r_v[w];
-                bi = r_i[w];
-            }
-        __syncthreads();
-        if (tid == 0) {
-            ids[static_cast<int64_t>(row) * k + j] = bi;
-            if (vals) vals[static_cast<int64_t>(row) * k + j] = want_lse ? bv - lse : bv;
-        }
-        pv = bv;
-        pi = bi;
-    }
-    if (want_lse && tid == 0) lse_out[row] = lse;
+    cluster_sync();  // peers' shared memory stays alive until rank 0 has read it
 }
 
 template <typename T>
 cudaError_t launch_typed(const T *logits, int32_t rows, int32_t V, int64_t ld, int32_t k, int32_t *ids,
                          float *vals, float *lse, cudaStream_t st) {
-    return launch_pdl(row_topk_kernel<T>, dim3(rows), dim3(kThreads), 0, st, logits, V, ld, k, ids, vals, lse);
+    constexpr int EPV = 16 / sizeof(T);
+    // about two vectors per thread per CTA, at most kMaxCluster CTAs
+    const int64_t vecs = (static_cast<int64_t>(V) + EPV - 1) / EPV;
+    int64_t c = (vecs + 2 * kThreads - 1) / (2 * kThreads);
+    if (c < 1) c = 1;
+    if (c > kMaxCluster) c = kMaxCluster;
+    const unsigned C = static_cast<unsigned>(c);
+    return launch_pdl_cluster(row_topk_kernel<T>, dim3(static_cast<unsigned>(rows) * C), dim3(kThreads), C, 0,
+                              st, logits, V, ld, k, ids, vals, lse);
 }
 
 }  // namespace

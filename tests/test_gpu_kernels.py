@@ -103,6 +103,30 @@ def test_row_topk_matches_oracle(dev, rows, V, k, dt, strided):
         assert am[r, 0] == rid[0] and raw[r, 0] == z[r, rid[0]]
 
 
+@pytest.mark.parametrize("V,k,dt", [(32000, 10, "f32"), (1000, 16, "f32"), (128256, 16, "f32"),
+                                    (32000, 1, "bf16"), (4099, 7, "bf16")])
+def test_row_topk_massive_ties(dev, V, k, dt):
+    """Thousands of entries tie at the top: the candidate lists overflow and every slice falls
+    back to exact passes; ties go to the lower column."""
+    from eagle_speculative_decoding_draft_gb300.engine import row_topk
+    rng = np.random.default_rng(V + k)
+    z = rng.integers(0, 3, size=(4, V)).astype(np.float32)
+    z[1] = 0.0  # one constant row
+    z[2, ::5] = 3.0
+    zt = torch.from_numpy(z)
+    if dt == "bf16":
+        zt = zt.to(torch.bfloat16)
+    ids, logp, lse = row_topk(zt.to(dev), k, with_lse=True)
+    torch.cuda.synchronize()
+    ids, logp, lse = map(to_np, (ids, logp, lse))
+    for r in range(z.shape[0]):
+        rid, rlogp, rlse = oracle.log_softmax_topk(z[r], k)
+        assert ids[r].tolist() == rid.tolist()
+        bound = gamma(V) * 2 + 8 * U32 * (1 + abs(rlse)) + 1e-6
+        assert abs(lse[r] - rlse) <= bound
+        assert np.all(np.abs(logp[r] - rlogp) <= bound + 8 * U32 * np.abs(rlogp))
+
+
 def small_tree(dtype="bf16", B=3, d=4, k=3, m=12, h=32, V=300, seed=5):
     w = synth.custom(h, V, B, d, k, m, dtype=dtype)
     inp = synth.make_inputs(w, seed=seed)
