@@ -32,6 +32,7 @@ METRIC = "draft-tree steps/sec (tree nodes/sec) at 1 GB300; % HBM or tensor roof
 UNIT = "steps/s"
 PEAKS_FILE = ROOT / "MEASURED_PEAKS.json"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 TRAFFIC_FILE = ROOT / "profiles" / "linear_bf16_tc_vicuna7b.md"
 KERNEL_SOURCES = ["eagle_speculative_decoding_draft_gb300/csrc/gemm.cu",
                   "eagle_speculative_decoding_draft_gb300/csrc/common.cuh"]
@@ -85,6 +86,32 @@ def hbm_peak():
         return float(json.loads(PEAKS_FILE.read_text())["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Sustained dense bf16 TFLOP/s: the GEMM launches run inside a long loop of steps."""
+    try:
+        return float(json.loads(PEAKS_FILE.read_text())["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
+
+
+def per_level(plist, hbm, tflops):
+    """Mean duration, GB/s and TFLOP/s of the timed GEMM launches, by (level, kind)."""
+    agg = {}
+    for e in plist:
+        a = agg.setdefault((e["level"], e["kind"]), [0, 0.0, 0.0, 0.0])
+        a[0] += 1
+        a[1] += e["ms"]
+        a[2] += e["bytes"]
+        a[3] += e["flops"]
+    out = []
+    for (lvl, kind), (c, ms, by, fl) in sorted(agg.items()):
+        gbs = by / (ms * 1e-3) / 1e9
+        tfs = fl / (ms * 1e-3) / 1e12
+        out.append({"level": lvl, "kind": kind, "launches": c, "us": 1e3 * ms / c,
+                    "GB/s": gbs, "hbm_frac": gbs / hbm, "TFLOP/s": tfs, "tensor_frac": tfs / tflops})
+    return out
 
 
 class ClockSampler:
@@ -342,7 +369,10 @@ def run_eagle(args, w):
     eng.profile_enable(True)
     ms = start.elapsed_time(end)
     launches = eng.launch_count() - l0
-    n_prof, gemm_ms, gemm_bytes = eng.profile_read()
+    plist = eng.profile_list(len(sampled) * gemm_per_step)
+    n_prof = len(plist)
+    gemm_ms = sum(e["ms"] for e in plist)
+    gemm_bytes = sum(e["bytes"] for e in plist)
     eng.profile(0)
     eng.status()
     ms_max = max_over_ranks(ms)
@@ -379,6 +409,7 @@ def run_eagle(args, w):
     d2h = 4 * (3 * B * n + B * n * W + B + B * (d + 1))
 
     peak, peak_kind = hbm_peak()
+    tpeak, tpeak_kind = tensor_peak()
     achieved = gemm_bytes / (gemm_ms * 1e-3) / 1e9 if gemm_ms > 0 else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
@@ -400,7 +431,10 @@ def run_eagle(args, w):
                      "launches_timed": n_prof, "ms_per_launch": gemm_ms / max(n_prof, 1),
                      "timed_steps": f"GEMM launches of 1 step in {PROFILE_EVERY} (events stop "
                                     "those launches overlapping their predecessor)",
-                     "gemm_ms_per_step_standalone": gemm_ms / max(len(sampled), 1)},
+                     "gemm_ms_per_step_standalone": gemm_ms / max(len(sampled), 1),
+                     "per_level": per_level(plist, peak, tpeak),
+                     "tensor_peak": tpeak,
+                     "tensor_peak_source": f"{tpeak_kind} bf16_tflops_sustained"},
         "clocks": clocks.summary(),
         "e2e": {"value": world * E / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,

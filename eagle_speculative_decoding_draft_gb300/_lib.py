@@ -71,6 +71,9 @@ _SIGS = {
     "eagle_tree_profile_enable": (c_int, [c_void_p, c_int32]),
     "eagle_tree_profile_read": (c_int, [c_void_p, POINTER(c_int32), POINTER(ctypes.c_double),
                                         POINTER(ctypes.c_double)]),
+    "eagle_tree_profile_list": (c_int, [c_void_p, c_int32, POINTER(c_int32), POINTER(ctypes.c_float),
+                                        POINTER(ctypes.c_double), POINTER(ctypes.c_double),
+                                        POINTER(c_int32)]),
     "eagle_tree_launch_count": (c_int64, [c_void_p]),
     "eagle_linear_workspace_bytes": (c_size_t, [c_int32, c_int32]),
     "eagle_linear_noalloc_scratch_bytes": (c_size_t, []),

@@ -191,7 +191,8 @@ struct eagle_tree {
     std::vector<LinearSeq> fc, lm;  // per level (bf16 only)
     int64_t launches = 0;           // kernels launched by this handle
     std::vector<cudaEvent_t> prof_start, prof_stop;
-    std::vector<double> prof_bytes;
+    std::vector<double> prof_bytes, prof_flops;
+    std::vector<int32_t> prof_tag;
     int32_t prof_n = 0;
     bool prof_on = true;
 
@@ -202,29 +203,35 @@ struct eagle_tree {
         prof_start.clear();
         prof_stop.clear();
         prof_bytes.clear();
+        prof_flops.clear();
+        prof_tag.clear();
         prof_n = 0;
     }
     // Launches one GEMM, bracketed by profiling events when enabled.
-    cudaError_t gemm(const LinearPlan &p, cudaStream_t st) {
+    // tag: 2 * level + (0 for the FC, 1 for the LM head); -1 outside the draft levels.
+    cudaError_t gemm(const LinearPlan &p, cudaStream_t st, int32_t tag) {
         const bool timed = prof_on && prof_n < static_cast<int32_t>(prof_start.size());
         if (timed && cudaEventRecord(prof_start[prof_n], st) != cudaSuccess) return cudaErrorUnknown;
         cudaError_t e = launch_linear_bf16(p, st);
-        ++launches;
+        launches += p.defer ? 2 : 1;
         if (e != cudaSuccess) return e;
         if (timed) {
             if (cudaEventRecord(prof_stop[prof_n], st) != cudaSuccess) return cudaErrorUnknown;
             const double M = p.M, K = p.K, R = p.rows;
             prof_bytes[prof_n] = 2.0 * M * K + 2.0 * R * K + (p.out_bf16 ? 2.0 * R * M : 0.0);
+            prof_flops[prof_n] = 2.0 * M * K * R;
+            prof_tag[prof_n] = tag;
             ++prof_n;
         }
         return cudaSuccess;
     }
-    cudaError_t run(const LinearSeq &s, cudaStream_t st, void *out_override, int64_t ldo, int32_t ob) {
+    cudaError_t run(const LinearSeq &s, cudaStream_t st, void *out_override, int64_t ldo, int32_t ob,
+                    int32_t tag) {
         for (size_t i = 0; i < s.plans.size(); ++i) {
             LinearPlan p = s.plans[i];
             if (out_override)
                 p.out = reinterpret_cast<uint8_t *>(out_override) + static_cast<int64_t>(s.row0[i]) * ldo * ob;
-            cudaError_t e = gemm(p, st);
+            cudaError_t e = gemm(p, st, tag);
             if (e != cudaSuccess) return e;
         }
         return cudaSuccess;
@@ -383,7 +390,7 @@ eagle_status eagle_draft_level(eagle_tree *t, int32_t level, const void *d_root_
     }
     // FC: f^ = W_fc [f || e(t)] + b
     if (bf16) {
-        EAGLE_CUDA(t->run(t->fc[level], st, nullptr, h, 2));
+        EAGLE_CUDA(t->run(t->fc[level], st, nullptr, h, 2, 2 * level));
     } else {
         EAGLE_CUDA(launch_linear_f32(reinterpret_cast<const float *>(c.fc_weight), 2 * h,
                                      reinterpret_cast<const float *>(x), 2 * h,
@@ -394,7 +401,7 @@ eagle_status eagle_draft_level(eagle_tree *t, int32_t level, const void *d_root_
     // LM head: z = W_lm f^
     float *lg = d_logits_out ? d_logits_out : t->at<float>(L.logits);
     if (bf16) {
-        EAGLE_CUDA(t->run(t->lm[level], st, d_logits_out, V, 4));
+        EAGLE_CUDA(t->run(t->lm[level], st, d_logits_out, V, 4, 2 * level + 1));
     } else {
         EAGLE_CUDA(launch_linear_f32(reinterpret_cast<const float *>(c.lm_head), h,
                                      reinterpret_cast<const float *>(fh), h, nullptr, lg, V, V, h, R, st));
@@ -538,8 +545,8 @@ eagle_status eagle_tree_node_logits(eagle_tree *t, const void *d_root_feature, f
                 !plan_seq(&lm, c.lm_head, h, V, h, nf, h, rows, nullptr, out, V, 0, 4, t->partials, t->counters,
                           t->status, t->num_sms))
                 return EAGLE_ERR_UNSUPPORTED;
-            EAGLE_CUDA(t->run(fc, st, nullptr, h, 2));
-            EAGLE_CUDA(t->run(lm, st, nullptr, V, 4));
+            EAGLE_CUDA(t->run(fc, st, nullptr, h, 2, -1));
+            EAGLE_CUDA(t->run(lm, st, nullptr, V, 4, -1));
         } else {
             EAGLE_CUDA(launch_linear_f32(reinterpret_cast<const float *>(c.fc_weight), 2 * h,
                                          reinterpret_cast<const float *>(nx), 2 * h,
@@ -630,6 +637,8 @@ eagle_status eagle_tree_profile(eagle_tree *t, int32_t max_launches) {
         t->prof_start.push_back(a);
         t->prof_stop.push_back(b);
         t->prof_bytes.push_back(0.0);
+        t->prof_flops.push_back(0.0);
+        t->prof_tag.push_back(-1);
     }
     return EAGLE_OK;
 }
@@ -649,6 +658,24 @@ eagle_status eagle_tree_profile_read(eagle_tree *t, int32_t *launches, double *t
     *launches = t->prof_n;
     *total_ms = ms;
     *total_bytes = bytes;
+    t->prof_n = 0;
+    return EAGLE_OK;
+}
+
+eagle_status eagle_tree_profile_list(eagle_tree *t, int32_t cap, int32_t *n, float *ms, double *bytes,
+                                     double *flops, int32_t *tag) {
+    if (!t || !n || cap < 0 || (cap > 0 && (!ms || !bytes || !flops || !tag))) return EAGLE_ERR_INVALID_ARG;
+    DeviceGuard guard(t->device);
+    if (!guard.ok) return EAGLE_ERR_CUDA;
+    if (t->prof_n > 0) EAGLE_CUDA(cudaEventSynchronize(t->prof_stop[t->prof_n - 1]));
+    const int32_t m = std::min(cap, t->prof_n);
+    for (int32_t i = 0; i < m; ++i) {
+        EAGLE_CUDA(cudaEventElapsedTime(&ms[i], t->prof_start[i], t->prof_stop[i]));
+        bytes[i] = t->prof_bytes[i];
+        flops[i] = t->prof_flops[i];
+        tag[i] = t->prof_tag[i];
+    }
+    *n = m;
     t->prof_n = 0;
     return EAGLE_OK;
 }

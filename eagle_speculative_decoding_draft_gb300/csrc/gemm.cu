@@ -49,6 +49,7 @@ struct LinearArgs {
     void *out;
     int64_t ldo;
     int32_t out_bf16;
+    int32_t defer;  // split tiles: write partials only; linear_reduce_kernel sums them
     float *partials;
     int32_t *counters;
     int32_t *status;
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0 && got) mbar_arrive(&ctl->acc_empty[acc]);
-            if (!full) {
+            if (!full && !a.defer) {
                 named_barrier_sync(1, 128);  // this CTA's partials of the tile are written
                 const int32_t gf = cta_of(t0, total, G), gl = cta_of(t0 + nkb - 1, total, G);
                 if (threadIdx.x == 64) {
@@ -377,6 +378,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         __syncwarp();
         tmem_dealloc(tmem_base, static_cast<uint32_t>(a.tmem_cols));
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Deferred split-K sum for many rows: block (tile, y) adds, for rows y*kReduceRows .. +15 of a
+// tile that more than one CTA worked on, the partials of its CTAs in ascending CTA order (the
+// same order and the same sums as the in-kernel fix-up) and writes Y (+ bias).  Thread e sums
+// outputs 4(e % 32) .. +3 of rows e / 32 and e / 32 + 8; all its loads are issued together.
+// ---------------------------------------------------------------------------------------------
+constexpr int kReduceRows = 16;
+
+__global__ void __launch_bounds__(256) linear_reduce_kernel(const LinearArgs a, int32_t G) {
+    pdl_launch_dependents();  // dependents still wait for this grid to finish
+    pdl_wait();
+    const int32_t tile = blockIdx.x;
+    const int64_t nkb = a.num_kb;
+    const int64_t total = static_cast<int64_t>(a.num_tiles) * nkb;
+    const int64_t t0 = static_cast<int64_t>(tile) * nkb;
+    const int32_t gf = cta_of(t0, total, G), gl = cta_of(t0 + nkb - 1, total, G);
+    if (gf == gl) return;  // one CTA computed the whole tile and wrote it
+    const bool gf_second = div_nonneg(total * gf, G) < t0;
+    const int32_t m4 = (threadIdx.x & 31) * 4, rsub = threadIdx.x >> 5;
+    constexpr int kCtasPerBatch = 8;
+    float4 sum[2];
+    for (int32_t g0 = gf; g0 <= gl; g0 += kCtasPerBatch) {
+        float4 x[kCtasPerBatch][2];
+#pragma unroll
+        for (int c = 0; c < kCtasPerBatch; ++c) {
+            const int32_t gg = g0 + c;
+            const int32_t slot = (gg == gf && gf_second) ? 1 : 0;
+            const float *src = a.partials + static_cast<size_t>(gg * 2 + slot) * a.n_tile * BM + m4;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int32_t n = blockIdx.y * kReduceRows + rsub + 8 * j;
+                x[c][j] = (gg <= gl && n < a.rows)
+                              ? __ldcg(reinterpret_cast<const float4 *>(src + static_cast<size_t>(n) * BM))
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < kCtasPerBatch; ++c)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                if (g0 + c > gl) continue;
+                if (g0 + c == gf) {
+                    sum[j] = x[c][j];
+                } else {
+                    sum[j].x += x[c][j].x;
+                    sum[j].y += x[c][j].y;
+                    sum[j].z += x[c][j].z;
+                    sum[j].w += x[c][j].w;
+                }
+            }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int32_t n = blockIdx.y * kReduceRows + rsub + 8 * j;
+        if (n >= a.rows) continue;
+        const float v[4] = {sum[j].x, sum[j].y, sum[j].z, sum[j].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int32_t o = tile * BM + m4 + q;
+            if (o >= a.M) continue;
+            const float b = a.bias != nullptr ? __bfloat162float(a.bias[o]) : 0.0f;
+            store_y(a, n, o, v[q] + b);
+        }
     }
 }
 
@@ -492,6 +559,9 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     p->out = out;
     p->ldo = ldo;
     p->out_bf16 = out_bf16;
+    // Many rows: one CTA per tile cannot sum the partials fast enough (it reads CTAs x rows x 128
+    // floats); a separate launch spreads the sum over tiles x row blocks.
+    p->defer = rows > kLinearMaxFixupRows ? 1 : 0;
     p->partials = partials;
     p->counters = counters;
     p->status = status;
@@ -525,11 +595,15 @@ cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
     a.out = p.out;
     a.ldo = p.ldo;
     a.out_bf16 = p.out_bf16;
+    a.defer = p.defer;
     a.partials = p.partials;
     a.counters = p.counters;
     a.status = p.status;
-    return launch_pdl(linear_bf16_tc_kernel, dim3(p.grid), dim3(kThreads), p.smem_bytes, st, p.tmap_w,
-                      p.tmap_x, a);
+    cudaError_t e = launch_pdl(linear_bf16_tc_kernel, dim3(p.grid), dim3(kThreads), p.smem_bytes, st, p.tmap_w,
+                               p.tmap_x, a);
+    if (e != cudaSuccess || !p.defer) return e;
+    return launch_pdl(linear_reduce_kernel, dim3(p.num_tiles, (p.rows + kReduceRows - 1) / kReduceRows),
+                      dim3(256), 0, st, a, p.grid);
 }
 
 cudaError_t launch_linear_f32(const float *w, int64_t ldw, const float *x, int64_t ldx,

@@ -60,6 +60,7 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
 constexpr int kLinearTileM = 128;
 constexpr int kLinearTileK = 64;
 constexpr int kLinearMaxRows = 256;  // MMA N limit of one launch
+constexpr int kLinearMaxFixupRows = 16;  // above this, split tiles are summed by a second launch
 
 struct LinearPlan {
     CUtensorMap tmap_w;  // W [M][K] bf16, box {64, 128}, 128-byte swizzle
@@ -70,6 +71,7 @@ struct LinearPlan {
     void *out;         // [rows][ldo]
     int64_t ldo;
     int32_t out_bf16;
+    int32_t defer;     // rows > kLinearMaxFixupRows: a second launch sums the split tiles
     float *partials;   // [grid][2][n_tile][128]
     int32_t *counters; // [num_tiles], zero before and after
     int32_t *status;

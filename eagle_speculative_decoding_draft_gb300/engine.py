@@ -207,6 +207,24 @@ class EagleTree:
                                                ctypes.byref(by)), "eagle_tree_profile_read")
         return n.value, ms.value, by.value
 
+    def profile_list(self, cap: int):
+        """The GEMM launches timed so far, one dict per launch: ms, bytes, flops, level and
+        kind ('fc' or 'lm_head'; level -1 for node_logits)."""
+        n = ctypes.c_int32()
+        ms = (ctypes.c_float * max(cap, 1))()
+        by = (ctypes.c_double * max(cap, 1))()
+        fl = (ctypes.c_double * max(cap, 1))()
+        tg = (ctypes.c_int32 * max(cap, 1))()
+        check(self.lib.eagle_tree_profile_list(self._h, int(cap), ctypes.byref(n), ms, by, fl, tg),
+              "eagle_tree_profile_list")
+        out = []
+        for i in range(n.value):
+            t = tg[i]
+            out.append({"ms": float(ms[i]), "bytes": float(by[i]), "flops": float(fl[i]),
+                        "level": t // 2 if t >= 0 else -1,
+                        "kind": "lm_head" if (t >= 0 and t % 2) else "fc"})
+        return out
+
     def launch_count(self) -> int:
         return int(self.lib.eagle_tree_launch_count(self._h))
 

@@ -255,6 +255,13 @@ EAGLE_API eagle_status eagle_tree_profile(eagle_tree *t, int32_t max_launches);
 EAGLE_API eagle_status eagle_tree_profile_enable(eagle_tree *t, int32_t enable);
 EAGLE_API eagle_status eagle_tree_profile_read(eagle_tree *t, int32_t *launches, double *total_ms,
                                                double *total_bytes);
+/* The same timed launches one by one (at most cap of them, in launch order): duration ms[i],
+ * algorithmic bytes[i] (as above), flops[i] = 2 * out_features * in_features * rows, and
+ * tag[i] = 2 * level + 0 for the FC or + 1 for the LM head (-1: eagle_tree_node_logits).  *n is
+ * the number written; like eagle_tree_profile_read it restarts the count.  All arrays are host
+ * memory owned by the caller. */
+EAGLE_API eagle_status eagle_tree_profile_list(eagle_tree *t, int32_t cap, int32_t *n, float *ms,
+                                               double *bytes, double *flops, int32_t *tag);
 EAGLE_API int64_t eagle_tree_launch_count(const eagle_tree *t);
 
 /* ------------------------------------------------------------------------------------------ */
