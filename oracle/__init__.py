@@ -73,6 +73,9 @@ def lib():
             L.orc_draft_tree.argtypes = [ctypes.POINTER(Dims)] + [P] * 24
             L.orc_verify_greedy.restype = i32
             L.orc_verify_greedy.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
+            L.orc_verify_sample.restype = i32
+            L.orc_verify_sample.argtypes = [i32, i32, i32, i32, P, P, P, P, ctypes.c_double, i32,
+                                            ctypes.c_double, P, P, P, P, P]
             _lib = L
     return _lib
 
@@ -216,6 +219,31 @@ def draft_tree(w_fc, b_fc, w_lm, emb, root_feat, root_tok, depth: int, topk: int
     if rc != ORC_OK:
         raise RuntimeError(f"orc_draft_tree failed with code {rc}")
     return out
+
+
+def verify_sample(tree_tok, tree_parent, target, draft, depth: int, temperature: float,
+                  u_acc, u_bonus, mode: int = 0, threshold: float = 0.0) -> dict:
+    """Sampling tree verification (mode 0: recursive rejection sampling; mode 1: threshold).
+    target, draft: [B][n][V] float32 logits; u_acc [B][n], u_bonus [B] uniforms in [0, 1).
+    Returns accept_len [B] and accept_nodes / accept_tok [B][depth+1] (bonus last)."""
+    tt = np.ascontiguousarray(tree_tok, dtype=np.int32)
+    tp = np.ascontiguousarray(tree_parent, dtype=np.int32)
+    T = np.ascontiguousarray(target, dtype=np.float32)
+    Z = np.ascontiguousarray(draft, dtype=np.float32)
+    ua = np.ascontiguousarray(u_acc, dtype=np.float32)
+    ub = np.ascontiguousarray(u_bonus, dtype=np.float32)
+    B, n = tt.shape
+    V = T.shape[-1]
+    assert T.shape == (B, n, V) and Z.shape == (B, n, V) and ua.shape == (B, n) and ub.shape == (B,)
+    al = np.zeros(B, np.int32)
+    an = np.zeros((B, depth + 1), np.int32)
+    at = np.zeros((B, depth + 1), np.int32)
+    rc = lib().orc_verify_sample(B, n, V, depth, _ptr(tt), _ptr(tp), _ptr(T), _ptr(Z),
+                                 float(temperature), int(mode), float(threshold), _ptr(ua),
+                                 _ptr(ub), _ptr(al), _ptr(an), _ptr(at))
+    if rc != ORC_OK:
+        raise RuntimeError(f"orc_verify_sample failed with code {rc}")
+    return {"accept_len": al, "accept_nodes": an, "accept_tok": at}
 
 
 def verify_greedy(tree_tok, tree_parent, target, depth: int) -> dict:

@@ -500,6 +500,148 @@ int32_t orc_verify_greedy(int32_t B, int32_t n_nodes, int32_t V, int32_t depth,
     return ORC_OK;
 }
 
+/* ------------------------------------------------------------------------------------------ */
+/* Sampling tree verification (recursive rejection sampling; threshold variant)               */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * [notes04] §6.2 "验证阶段（树注意力 + 递归拒绝采样）": the target scores every tree node in one
+ * forward; then, node by node from the root, a drafted token t is accepted when a uniform r
+ * satisfies r <= min(1, p(t) / q(t)), and on rejection the distribution to draw from becomes
+ * norm(max(0, p - q)); with several drafted children the same step is repeated child after
+ * child on the updated p (the multi-candidate form of SpecInfer, which [notes04] names as the
+ * framework of EAGLE's tree verification).  [notes04] §7.1: with q == p every test passes.
+ * [tomjerr] "Summary" (the SGLang note): the threshold variant accepts a drafted token when its
+ * target probability passes a threshold and draws the bonus token by one rejection step over
+ * the layer only when every child fails.
+ *
+ * Readings where the pages leave a step open (each is listed in the design notes):
+ *   - p_i = softmax(T[b][i] / temperature) and q_i = softmax(Z[b][i] / temperature): T and Z are
+ *     the target's and the draft's logits at node i, i.e. the distributions of the token that
+ *     follows node i (q_i is what node i's children were drafted from); temperature > 0;
+ *   - children of a node are visited in ascending tree index (the draft's own ranking, since the
+ *     tree lists a parent's kept children by candidate id);
+ *   - the test of child c uses its own uniform u_acc[b][c]: accept iff P(t_c) > 0 and
+ *     u_acc * q(t_c) <= P(t_c) (the division-free form of u <= min(1, P/q); a token the target
+ *     gives probability 0 is never accepted);
+ *   - after a rejection P <- max(0, P - q) / sum; if that sum is 0 (P == q up to rounding),
+ *     P is left as it was;
+ *   - threshold mode (mode 1): the first child c with p_cur(t_c) >= threshold is accepted; if
+ *     none is, P = p_cur updated by one rejection step per child in order, and the bonus is drawn
+ *     from it;
+ *   - the bonus token is drawn from the final P by inverse CDF with u_bonus[b]: the smallest v
+ *     whose running sum (ascending v) exceeds u_bonus * sum(P); if rounding leaves none, the
+ *     largest v with P(v) > 0.
+ * Everything is computed in double precision.
+ * Outputs as in orc_verify_greedy: accept_len [B], accept_nodes / accept_tok [B][depth+1]
+ * (bonus last, unused slots -1).
+ * Pins: worked examples derived by hand (tests/golden/verify_sample_cases.json); with q == p the
+ * first child is always accepted ([notes04] §7.1); losslessness: with children drawn from q the
+ * first emitted token is distributed as p (chi-square over many draws); greedy limit of the
+ * threshold mode.
+ */
+static void orc_softmax_scaled(const float *logits, int32_t V, double inv_temp, double *out) {
+    double m = -HUGE_VAL;
+    for (int32_t v = 0; v < V; ++v)
+        if ((double)logits[v] * inv_temp > m) m = (double)logits[v] * inv_temp;
+    double s = 0.0;
+    for (int32_t v = 0; v < V; ++v) {
+        out[v] = exp((double)logits[v] * inv_temp - m);
+        s += out[v];
+    }
+    for (int32_t v = 0; v < V; ++v) out[v] /= s;
+}
+
+/* P <- norm(max(0, P - q)); P is left unchanged when the residual is empty. */
+static void orc_residual(double *P, const double *q, int32_t V) {
+    double s = 0.0;
+    for (int32_t v = 0; v < V; ++v) {
+        const double r = P[v] - q[v];
+        s += r > 0.0 ? r : 0.0;
+    }
+    if (!(s > 0.0)) return;
+    for (int32_t v = 0; v < V; ++v) {
+        const double r = P[v] - q[v];
+        P[v] = (r > 0.0 ? r : 0.0) / s;
+    }
+}
+
+static int32_t orc_inverse_cdf(const double *P, int32_t V, double u) {
+    double tot = 0.0;
+    for (int32_t v = 0; v < V; ++v) tot += P[v];
+    const double target = u * tot;
+    double run = 0.0;
+    int32_t last = -1;
+    for (int32_t v = 0; v < V; ++v) {
+        if (P[v] > 0.0) last = v;
+        run += P[v];
+        if (run > target && P[v] > 0.0) return v;
+    }
+    return last < 0 ? 0 : last;
+}
+
+int32_t orc_verify_sample(int32_t B, int32_t n_nodes, int32_t V, int32_t depth,
+                          const int32_t *tree_tok, const int32_t *tree_parent, const float *T,
+                          const float *Z, double temperature, int32_t mode, double threshold,
+                          const float *u_acc, const float *u_bonus, int32_t *accept_len,
+                          int32_t *accept_nodes, int32_t *accept_tok) {
+    if (B < 0 || n_nodes < 1 || V < 1 || depth < 0 || !(temperature > 0.0) || mode < 0 || mode > 1)
+        return ORC_ERR_ARG;
+    double *P = (double *)malloc(sizeof(double) * (size_t)V);
+    double *q = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!P || !q) {
+        free(P); free(q);
+        return ORC_ERR_NOMEM;
+    }
+    const double inv_t = 1.0 / temperature;
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t *tok = tree_tok + (int64_t)b * n_nodes;
+        const int32_t *par = tree_parent + (int64_t)b * n_nodes;
+        int32_t *an = accept_nodes + (int64_t)b * (depth + 1);
+        int32_t *at = accept_tok + (int64_t)b * (depth + 1);
+        for (int32_t i = 0; i <= depth; ++i) {
+            an[i] = -1;
+            at[i] = -1;
+        }
+        int32_t cur = 0, n = 0;
+        an[0] = 0;
+        for (;;) {
+            const float *trow = T + ((int64_t)b * n_nodes + cur) * V;
+            const float *zrow = Z + ((int64_t)b * n_nodes + cur) * V;
+            orc_softmax_scaled(trow, V, inv_t, P); /* p_cur */
+            orc_softmax_scaled(zrow, V, inv_t, q); /* q_cur */
+            int32_t next = -1;
+            if (n < depth) {
+                if (mode == 0) {
+                    for (int32_t c = 1; c < n_nodes && next < 0; ++c) {
+                        if (par[c] != cur) continue;
+                        const int32_t t = tok[c];
+                        const double u = (double)u_acc[(int64_t)b * n_nodes + c];
+                        if (P[t] > 0.0 && u * q[t] <= P[t]) next = c;
+                        else orc_residual(P, q, V);
+                    }
+                } else {
+                    for (int32_t c = 1; c < n_nodes && next < 0; ++c)
+                        if (par[c] == cur && P[tok[c]] >= threshold) next = c;
+                    if (next < 0)
+                        for (int32_t c = 1; c < n_nodes; ++c)
+                            if (par[c] == cur) orc_residual(P, q, V);
+                }
+            }
+            if (next < 0) break;
+            at[n] = tok[next];
+            ++n;
+            an[n] = next;
+            cur = next;
+        }
+        at[n] = orc_inverse_cdf(P, V, (double)u_bonus[b]);
+        accept_len[b] = n;
+    }
+    free(P);
+    free(q);
+    return ORC_OK;
+}
+
 /* Element-wise bf16 rounding of an fp32 array (test helper for the rounding pin). */
 void orc_round_bf16_array(int64_t n, const float *in, uint16_t *out) {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_bf16(in[i]);
