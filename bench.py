@@ -408,6 +408,36 @@ def run_eagle(args, w):
     h2d = f.numel() * f.element_size() + t.numel() * 4 + T.numel() * T.element_size()
     d2h = 4 * (3 * B * n + B * n * W + B + B * (d + 1))
 
+    # ---------------- sampling verification (recursive rejection sampling) ----------------
+    # On the tree of input set 0: q = the draft's logits of every node, p = the target logits,
+    # temperature 1, fresh uniforms per call.  Timed alone with CUDA events.
+    from eagle_speculative_decoding_draft_gb300.engine import verify_sample
+    feat0, tok0, T0 = sets[0]
+    eng.step(feat0, tok0, T0, tree_out=tree_out, verify_out=ver_out)
+    Zn = eng.node_logits(feat0).contiguous()
+    T0c = T0.float().contiguous()
+    scratch = torch.empty(B, w.vocab, dtype=torch.float32, device=dev)
+    ugen = torch.Generator(device=dev)
+    ugen.manual_seed(77 + rank)
+    S_CALLS = 50
+    us = [(torch.rand(B, n, generator=ugen, device=dev), torch.rand(B, generator=ugen, device=dev))
+          for _ in range(S_CALLS)]
+    sacc = []
+    for i in range(3):
+        verify_sample(tree_out["tokens"], tree_out["parents"], T0c, Zn, d, 1.0, us[i][0], us[i][1],
+                      scratch=scratch)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for i in range(S_CALLS):
+        o = verify_sample(tree_out["tokens"], tree_out["parents"], T0c, Zn, d, 1.0, us[i][0], us[i][1],
+                          scratch=scratch)
+        sacc.append(o["accept_len"])
+    s1.record()
+    torch.cuda.synchronize()
+    sample_us = s0.elapsed_time(s1) * 1e3 / S_CALLS
+    sample_accept = float(torch.stack(sacc).float().mean().item())
+
     peak, peak_kind = hbm_peak()
     tpeak, tpeak_kind = tensor_peak()
     achieved = gemm_bytes / (gemm_ms * 1e-3) / 1e9 if gemm_ms > 0 else None
@@ -441,6 +471,11 @@ def run_eagle(args, w):
                 "how": "eagle_tree_step_host per step: pinned host inputs and target logits "
                        "copied in, tree and verify results copied out, stream synchronised"},
         "gpu_launches": int(sum_over_ranks(launches)),
+        "sampling_verify": {"us_per_call": sample_us, "mean_accept_len": sample_accept,
+                            "temperature": 1.0, "mode": "recursive rejection sampling",
+                            "how": "eagle_verify_sample on the step's tree; q = draft logits of "
+                                   "every node, p = the synthetic target; CUDA events, "
+                                   f"{S_CALLS} calls"},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)

@@ -67,6 +67,9 @@ _SIGS = {
     "eagle_build_tree": (c_int, [c_int32, c_int32, c_int32, c_int32] + [c_void_p] * 11
                          + [c_void_p]),
     "eagle_verify_walk": (c_int, [c_int32, c_int32, c_int32] + [c_void_p] * 6 + [c_void_p]),
+    "eagle_verify_sample": (c_int, [c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                    c_void_p, ctypes.c_float, c_int32, ctypes.c_float, c_void_p,
+                                    c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "eagle_tree_profile": (c_int, [c_void_p, c_int32]),
     "eagle_tree_profile_enable": (c_int, [c_void_p, c_int32]),
     "eagle_tree_profile_read": (c_int, [c_void_p, POINTER(c_int32), POINTER(ctypes.c_double),

@@ -783,6 +783,26 @@ eagle_status eagle_verify_walk(int32_t batch, int32_t num_nodes, int32_t depth, 
     return EAGLE_OK;
 }
 
+eagle_status eagle_verify_sample(int32_t batch, int32_t num_nodes, int32_t vocab, int32_t depth,
+                                 const int32_t *d_tokens, const int32_t *d_parents, const float *d_target_logits,
+                                 const float *d_draft_logits, float temperature, int32_t mode, float threshold,
+                                 const float *d_u_accept, const float *d_u_bonus, float *d_scratch,
+                                 int32_t *d_accept_len, int32_t *d_accept_nodes, int32_t *d_accept_tokens,
+                                 eagle_stream_t stream) {
+    if (batch < 0 || num_nodes < 1 || num_nodes > kMaxCandidates + 1 || vocab < 1 || depth < 0 || depth > 64)
+        return EAGLE_ERR_INVALID_ARG;
+    if (!(temperature > 0.0f) || !(temperature < INFINITY) || (mode != 0 && mode != 1)) return EAGLE_ERR_INVALID_ARG;
+    if (batch == 0) return EAGLE_OK;
+    if (!d_tokens || !d_parents || !d_target_logits || !d_draft_logits || !d_u_accept || !d_u_bonus ||
+        !d_scratch || !d_accept_len || !d_accept_nodes || !d_accept_tokens)
+        return EAGLE_ERR_INVALID_ARG;
+    EAGLE_CUDA(launch_verify_sample(batch, num_nodes, vocab, depth, d_tokens, d_parents, d_target_logits,
+                                    d_draft_logits, temperature, mode, threshold, d_u_accept, d_u_bonus, d_scratch,
+                                    d_accept_len, d_accept_nodes, d_accept_tokens,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+    return EAGLE_OK;
+}
+
 size_t eagle_linear_workspace_bytes(int32_t out_features, int32_t rows) {
     if (out_features < 1 || rows < 1 || rows > kLinearMaxRows) return 0;
     const int32_t sms = current_num_sms(nullptr);

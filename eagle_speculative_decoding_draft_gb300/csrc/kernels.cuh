@@ -144,6 +144,13 @@ constexpr int32_t kMaxCandidates = 4096;  // rerank pool per request
 cudaError_t launch_build_tree(const BuildArgs &a, cudaStream_t st);
 cudaError_t prepare_tree_kernels();
 
+// Sampling verification (recursive rejection sampling, mode 0; threshold variant, mode 1); one
+// CTA per request; scratch is [B][V] fp32.
+cudaError_t launch_verify_sample(int32_t B, int32_t n, int32_t V, int32_t depth, const int32_t *tok,
+                                 const int32_t *par, const float *T, const float *Z, float temperature,
+                                 int32_t mode, float threshold, const float *u_acc, const float *u_bonus,
+                                 float *scratch, int32_t *accept_len, int32_t *accept_nodes,
+                                 int32_t *accept_tok, cudaStream_t st);
 cudaError_t launch_verify_walk(int32_t B, int32_t n, int32_t d, const int32_t *tok,
                                const int32_t *par, const int32_t *g, int32_t *accept_len,
                                int32_t *accept_nodes, int32_t *accept_tok, cudaStream_t st);

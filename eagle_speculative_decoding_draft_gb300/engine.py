@@ -329,6 +329,31 @@ def verify_walk(tokens, parents, target_ids, depth, stream=None):
     return out
 
 
+def verify_sample(tokens, parents, target_logits, draft_logits, depth, temperature, u_accept,
+                  u_bonus, mode=0, threshold=0.0, scratch=None, stream=None):
+    """Sampling tree verification on the GPU (mode 0: recursive rejection sampling, mode 1:
+    threshold).  tokens / parents [B][n] int32, logits [B][n][V] fp32, u_accept [B][n] and
+    u_bonus [B] fp32 uniforms.  Returns accept_len / accept_nodes / accept_tokens."""
+    lib = _lib.load()
+    B, n = tokens.shape
+    V = target_logits.shape[-1]
+    dev = tokens.device
+    for t in (target_logits, draft_logits, u_accept, u_bonus):
+        assert t.dtype == torch.float32 and t.is_contiguous()
+    if scratch is None:
+        scratch = torch.empty(B, V, dtype=torch.float32, device=dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = {"accept_len": torch.empty(B, **i32), "accept_nodes": torch.empty(B, depth + 1, **i32),
+           "accept_tokens": torch.empty(B, depth + 1, **i32)}
+    check(lib.eagle_verify_sample(B, n, V, depth, _ptr(tokens), _ptr(parents), _ptr(target_logits),
+                                  _ptr(draft_logits), float(temperature), int(mode), float(threshold),
+                                  _ptr(u_accept), _ptr(u_bonus), _ptr(scratch),
+                                  _ptr(out["accept_len"]), _ptr(out["accept_nodes"]),
+                                  _ptr(out["accept_tokens"]), _stream(dev, stream)),
+          "eagle_verify_sample")
+    return out
+
+
 def linear_bf16(w, x, bias=None, out_bf16=False, stream=None):
     """Y = X W^T (+ bias) for bf16 W [M][K], X [rows][K] (rows <= 256) on the tensor cores."""
     lib = _lib.load()

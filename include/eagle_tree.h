@@ -321,6 +321,40 @@ EAGLE_API eagle_status eagle_verify_walk(int32_t batch, int32_t num_nodes, int32
                                          eagle_stream_t stream);
 
 /*
+ * Sampling tree verification ("EAGLE notes ch. 04" §6.2 and §7.1; the SGLang note in the summary
+ * of tom-jerr's "(EAGLE 1) EAGLE" reading for mode 1).  Stateless; works on any tree given as
+ * arrays.  For request b, p_i = softmax(T[b][i] / temperature) and q_i = softmax(Z[b][i] /
+ * temperature), where T and Z are the target's and the draft's logits at node i (the
+ * distribution of the token after node i; q_i is what node i's children were drafted from).
+ * From the root, the children of the current node are tested in ascending tree index:
+ *   mode 0 (recursive rejection sampling): child c with token t is accepted iff P(t) > 0 and
+ *          u_acc[b][c] * q(t) <= P(t), P being the current distribution (p of the node, then
+ *          norm(max(0, P - q)) after each rejected child; an empty residual leaves P as is);
+ *   mode 1 (threshold): the first child with p(t) >= threshold is accepted; if none is, P is p
+ *          after one rejection step per child.
+ * An accepted child becomes the current node (P = its p); the walk stops at depth `depth`, at a
+ * leaf, or when no child is accepted, and the bonus token is drawn from P by inverse CDF: the
+ * smallest token whose running sum (ascending ids) exceeds u_bonus[b] * sum(P) (else the largest
+ * token with P > 0).  All arithmetic is fp32 (the decisions of a double-precision evaluation can
+ * differ when a uniform falls within rounding of its threshold).
+ *   d_tokens, d_parents [B][n], parents before children, n <= 4097
+ *   d_target_logits, d_draft_logits  [B][n][V] fp32 (finite)
+ *   d_u_accept [B][n], d_u_bonus [B]  uniforms in [0, 1) drawn by the caller
+ *   d_scratch  [B][V] fp32, caller-owned, overwritten
+ * Outputs as eagle_verify_greedy.  temperature > 0 (use eagle_verify_greedy for 0).  Errors:
+ * INVALID_ARG (sizes, null pointers, temperature, mode), CUDA.  Token ids outside [0, V) are
+ * never accepted.
+ */
+EAGLE_API eagle_status eagle_verify_sample(int32_t batch, int32_t num_nodes, int32_t vocab,
+                                           int32_t depth, const int32_t *d_tokens,
+                                           const int32_t *d_parents, const float *d_target_logits,
+                                           const float *d_draft_logits, float temperature,
+                                           int32_t mode, float threshold, const float *d_u_accept,
+                                           const float *d_u_bonus, float *d_scratch,
+                                           int32_t *d_accept_len, int32_t *d_accept_nodes,
+                                           int32_t *d_accept_tokens, eagle_stream_t stream);
+
+/*
  * Streamed-weight GEMM used by the FC and the LM head: Y[r][o] = sum_i W[o][i] X[r][i]
  * (+ bias[o]) for r < rows, o < out_features, with W [out][in] and X [rows][in] bf16 (row
  * strides in elements ldw, ldx; multiples of 8), fp32 accumulation on the tensor cores.  Output

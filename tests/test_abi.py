@@ -98,3 +98,19 @@ def test_stateless_entries_reject_bad_sizes_on_the_host(lib):
                                  P(256), 1 << 20, None) == 1  # rows > 256
     assert lib.eagle_linear_bf16(P(256), 60, P(256), 64, None, 128, 60, 16, P(256), 128, 0,
                                  P(256), 1 << 20, None) == 1  # ldw not a multiple of 8
+
+
+def test_verify_sample_rejects_bad_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+    ptrs_in = [P(256)] * 4
+    ptrs_out = [P(256)] * 6
+    ok = lib.eagle_verify_sample
+    assert ok(1, 0, 10, 1, *ptrs_in, 1.0, 0, 0.0, *ptrs_out, None) == 1      # no nodes
+    assert ok(1, 5000, 10, 1, *ptrs_in, 1.0, 0, 0.0, *ptrs_out, None) == 1   # too many nodes
+    assert ok(1, 5, 10, 1, *ptrs_in, 0.0, 0, 0.0, *ptrs_out, None) == 1      # temperature 0
+    assert ok(1, 5, 10, 1, *ptrs_in, -1.0, 0, 0.0, *ptrs_out, None) == 1
+    assert ok(1, 5, 10, 1, *ptrs_in, float("nan"), 0, 0.0, *ptrs_out, None) == 1
+    assert ok(1, 5, 10, 1, *ptrs_in, 1.0, 2, 0.0, *ptrs_out, None) == 1      # mode
+    assert ok(1, 5, 10, 1, *ptrs_in, 1.0, 0, 0.0, *([None] + ptrs_out[1:]), None) == 1
+    assert ok(0, 5, 10, 1, *([None] * 4), 1.0, 0, 0.0, *([None] * 6), None) == 0  # empty batch
+
