@@ -381,10 +381,10 @@ eagle_status eagle_draft_level(eagle_tree *t, int32_t level, const void *d_root_
     const bool bf16 = c.dtype == EAGLE_BF16;
 
     if (level == 0) {
-        EAGLE_CUDA(cudaMemcpyAsync(t->at<int32_t>(L.root_tok), d_root_token, sizeof(int32_t) * B,
-                                   cudaMemcpyDeviceToDevice, st));
+        // the gather also keeps a copy of the root tokens for the tree build (a kernel rather than
+        // a copy, so that the launch chain stays programmatic)
         GatherArgs g{B, h, V, L.eb, nullptr, d_root_token, d_root_feature, t->ws + L.fhat, c.embedding, x,
-                     t->status};
+                     t->status, t->at<int32_t>(L.root_tok)};
         EAGLE_CUDA(launch_gather(g, st));
         ++t->launches;
     }
@@ -534,7 +534,7 @@ eagle_status eagle_tree_node_logits(eagle_tree *t, const void *d_root_feature, f
     for (int32_t r0 = 0; r0 < total; r0 += L.node_chunk) {
         const int32_t rows = std::min(L.node_chunk, total - r0);
         GatherArgs g{rows, h, V, L.eb, t->at<int32_t>(L.node_src) + r0, t->at<int32_t>(L.node_tok) + r0,
-                     d_root_feature, t->ws + L.fhat, c.embedding, nx, t->status};
+                     d_root_feature, t->ws + L.fhat, c.embedding, nx, t->status, nullptr};
         EAGLE_CUDA(launch_gather(g, st));
         ++t->launches;
         float *out = d_node_logits + static_cast<int64_t>(r0) * V;

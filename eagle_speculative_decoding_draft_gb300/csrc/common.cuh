@@ -122,6 +122,18 @@ __device__ __forceinline__ float ld_peer_f32(uint32_t a) {
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
     return v;
 }
+// Atomic add on a 32-bit word in a cluster CTA's shared memory; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_peer_u32(uint32_t a, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(a), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void st_peer_f32(uint32_t a, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_peer_s32(uint32_t a, int32_t v) {
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
 __device__ __forceinline__ int32_t ld_peer_s32(uint32_t a) {
     int32_t v;
     asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");

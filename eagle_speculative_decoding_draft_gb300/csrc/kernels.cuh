@@ -165,6 +165,7 @@ struct GatherArgs {
     const void *emb;
     void *x;
     int32_t *status;
+    int32_t *tok_copy;  // [n_rows] receives tok as given, or null
 };
 cudaError_t launch_gather(const GatherArgs &a, cudaStream_t st);
 

@@ -14,9 +14,10 @@
 //   pass 2  from the registers: sum of exp2((x - M) log2 e) for the logsumexp, and every
 //           element >= tau is appended to a shared candidate list; one warp sorts it with
 //           bitonic networks and keeps the slice's best k.
-//   merge   after a second cluster barrier, rank 0 reads the C sorted lists and sums from its
-//           peers' shared memory, merges them and writes the row's top k and logsumexp; a third
-//           barrier keeps every CTA's shared memory alive until rank 0 has read it.
+//   merge   every CTA stores its sorted list and its sum into rank 0's shared memory; after a
+//           second cluster barrier rank 0 merges the C lists (a tree of pairwise bitonic merges
+//           whose levels run in lockstep) and writes the row's top k and logsumexp.
+// C shrinks when there are many rows, so that the grid fits in about one wave.
 // A slice with more than kCand elements >= tau (massive ties) falls back to k exact block-wide
 // arg-max passes over that slice.
 #include <cfloat>
@@ -68,6 +69,29 @@ __device__ __forceinline__ void visit(const T *z, const uint4 (&cache)[kCacheVec
     for (int32_t i = s.sbeg + tid; i < s.send; i += kThreads) f(to_f32(z[i]), i);
 }
 
+// One level of a tree merge of sorted lists held across the warp (lane j = entry j): lists
+// p and p + STEP (p a multiple of 2 STEP, both < C) merge into list p, keeping the best 32.  The
+// merges of a level are independent and run in lockstep.
+template <int STEP>
+__device__ __forceinline__ void merge_level(float (&lv)[kMaxCluster], int32_t (&li)[kMaxCluster], int lane,
+                                            uint32_t C) {
+#pragma unroll
+    for (int p = 0; p + STEP < kMaxCluster; p += 2 * STEP) {
+        if (p + STEP < static_cast<int>(C)) {
+            const float rv = __shfl_sync(kFullMask, lv[p + STEP], 31 - lane);
+            const int32_t ri = __shfl_sync(kFullMask, li[p + STEP], 31 - lane);
+            const bool take = before_nb(rv, ri, lv[p], li[p]);
+            lv[p] = take ? rv : lv[p];
+            li[p] = take ? ri : li[p];
+        }
+    }
+#pragma unroll
+    for (int j = 16; j > 0; j >>= 1)
+#pragma unroll
+        for (int p = 0; p + STEP < kMaxCluster; p += 2 * STEP)
+            if (p + STEP < static_cast<int>(C)) bitonic_step(lv[p], li[p], j, (lane & j) == 0);
+}
+
 // Two CTAs per SM (64 registers a thread), so the CTAs of the next launch fit beside a GEMM CTA.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -86,6 +110,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ float x_sum;      // this slice's sum of exp relative to the row max
     __shared__ float x_v[16];    // this slice's best k, sorted
     __shared__ int32_t x_i[16];
+    // rank 0's inbox: every slice's sorted best k and its sum of exp
+    __shared__ float m_v[kMaxCluster][16];
+    __shared__ int32_t m_i[kMaxCluster][16];
+    __shared__ float m_sum[kMaxCluster];
     pdl_launch_dependents();  // dependents still wait for this grid to finish
     pdl_wait();
     const uint32_t C = cluster_size(), rank = cluster_rank();
@@ -233,44 +261,69 @@ __global__ void __launch_bounds__(kThreads, 2)
             pi = bi;
         }
     }
+    __syncthreads();
+    // ---- every slice's list and sum go to rank 0's inbox ----
+    if (warp == 0) {
+        if (lane < 16) {
+            st_peer_f32(peer_addr(&m_v[rank][lane], 0), x_v[lane]);
+            st_peer_s32(peer_addr(&m_i[rank][lane], 0), x_i[lane]);
+        }
+        if (lane == 0) st_peer_f32(peer_addr(&m_sum[rank], 0), x_sum);
+    }
+    // After this barrier no CTA touches a peer's shared memory again: rank 0 merges from its own.
     cluster_sync();
 
-    // ---- rank 0 merges the slices ----
+    // ---- rank 0 merges the slices' lists: a tree of pairwise merges, levels in lockstep ----
     if (rank == 0 && warp == 0) {
-        float v = (lane < k) ? x_v[lane] : -INFINITY;
-        int32_t i = (lane < k) ? x_i[lane] : INT_MAX;
-        float tot = (lane < static_cast<int>(C)) ? ld_peer_f32(peer_addr(&x_sum, lane)) : 0.0f;
-        for (uint32_t p = 1; p < C; ++p) {
-            float pv = -INFINITY;
-            int32_t pi = INT_MAX;
-            if (lane < k) {
-                pv = ld_peer_f32(peer_addr(&x_v[lane], p));
-                pi = ld_peer_s32(peer_addr(&x_i[lane], p));
-            }
-            warp_merge_sorted(v, i, pv, pi, lane);
+        float lv[kMaxCluster];
+        int32_t li[kMaxCluster];
+#pragma unroll
+        for (int p = 0; p < kMaxCluster; ++p) {
+            const bool ok = p < static_cast<int>(C) && lane < k;
+            lv[p] = ok ? m_v[p][lane] : -INFINITY;
+            li[p] = ok ? m_i[p][lane] : INT_MAX;
         }
+        float tot = (lane < static_cast<int>(C)) ? m_sum[lane] : 0.0f;
+        merge_level<1>(lv, li, lane, C);
+        merge_level<2>(lv, li, lane, C);
+        merge_level<4>(lv, li, lane, C);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(kFullMask, tot, off);
         const float lse = want_lse ? M + logf(tot) : 0.0f;
         if (lane < k) {
-            ids[static_cast<int64_t>(row) * k + lane] = i;
-            if (vals) vals[static_cast<int64_t>(row) * k + lane] = want_lse ? v - lse : v;
+            ids[static_cast<int64_t>(row) * k + lane] = li[0];
+            if (vals) vals[static_cast<int64_t>(row) * k + lane] = want_lse ? lv[0] - lse : lv[0];
         }
         if (want_lse && lane == 0) lse_out[row] = lse;
     }
-    cluster_sync();  // peers' shared memory stays alive until rank 0 has read it
+}
+
+// Streaming multiprocessors of the current device (looked up once per device).
+int sms_of_current_device() {
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
 }
 
 template <typename T>
 cudaError_t launch_typed(const T *logits, int32_t rows, int32_t V, int64_t ld, int32_t k, int32_t *ids,
                          float *vals, float *lse, cudaStream_t st) {
     constexpr int EPV = 16 / sizeof(T);
-    // about two vectors per thread per CTA, at most kMaxCluster CTAs
+    // about two vectors per thread per CTA, at most kMaxCluster CTAs, and no more CTAs than two
+    // per SM in all (a power of two)
     const int64_t vecs = (static_cast<int64_t>(V) + EPV - 1) / EPV;
     int64_t c = (vecs + 2 * kThreads - 1) / (2 * kThreads);
-    if (c < 1) c = 1;
+    const int64_t fit = (2 * static_cast<int64_t>(sms_of_current_device())) / rows;
+    if (c > fit) c = fit;
     if (c > kMaxCluster) c = kMaxCluster;
-    const unsigned C = static_cast<unsigned>(c);
+    unsigned C = 1;
+    while (static_cast<int64_t>(C) * 2 <= c) C *= 2;
     return launch_pdl_cluster(row_topk_kernel<T>, dim3(static_cast<unsigned>(rows) * C), dim3(kThreads), C, 0,
                               st, logits, V, ld, k, ids, vals, lse);
 }

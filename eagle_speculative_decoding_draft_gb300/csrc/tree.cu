@@ -104,6 +104,26 @@ __global__ void __launch_bounds__(kExpandThreads) expand_kernel(const ExpandArgs
 // ---------------------------------------------------------------------------------------------
 constexpr int kBuildThreads = 512;
 
+// Order-preserving unsigned key of a float: a < b (as floats, no NaN) iff key(a) < key(b).
+__device__ __forceinline__ uint32_t order_key(float x) {
+    const uint32_t u = (x == 0.0f) ? 0u : __float_as_uint(x);  // -0 and +0 compare equal
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Block-wide sum of one int per thread; `red` holds kBuildThreads / 32 ints.
+__device__ __forceinline__ int32_t block_total(int32_t v, int32_t *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    __syncthreads();  // `red` may still be read by the previous call
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    int32_t s = 0;
+#pragma unroll
+    for (int w = 0; w < kBuildThreads / 32; ++w) s += red[w];
+    return s;
+}
+
 __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(const BuildArgs a) {
     extern __shared__ int32_t sm[];
     const int32_t nc = a.n_cand, n = a.m + 1;
@@ -122,12 +142,56 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(const BuildAr
         sPar[c] = a.pool_parent[pb + c];
     }
     __syncthreads();
-    // kept iff fewer than m candidates rank before it
-    for (int32_t c = t; c < nc; c += kBuildThreads) {
-        const float S = sS[c];
-        int32_t rank = 0;
-        for (int32_t u = 0; u < nc; ++u) rank += ranks_before(sS[u], u, S, c) ? 1 : 0;
-        sIdx[c] = (rank < a.m) ? 1 : 0;
+    // Kept iff fewer than m candidates rank before it by (S descending, id ascending).  Radix
+    // select of the m-th largest score on order-preserving keys (32 block-wide counts), then the
+    // candidates tied with it are kept in id order up to m.
+    uint32_t thr = 0;  // key of the m-th largest score
+    int32_t above = 0;  // candidates strictly above it
+    if (a.m > 0 && nc <= kBuildThreads) {
+        // one candidate per thread: each step is one counting barrier
+        const uint32_t key = (t < nc) ? order_key(sS[t]) : 0u;
+        const bool real = t < nc;
+        for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t cand = thr | (1u << bit);
+            if (__syncthreads_count(real && key >= cand) >= a.m) thr = cand;
+        }
+        above = __syncthreads_count(real && key > thr);
+    } else if (a.m > 0) {
+        for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t cand = thr | (1u << bit);
+            int32_t cnt = 0;
+            for (int32_t c = t; c < nc; c += kBuildThreads) cnt += (order_key(sS[c]) >= cand) ? 1 : 0;
+            if (block_total(cnt, warp_cnt) >= a.m) thr = cand;
+        }
+        int32_t cnt = 0;
+        for (int32_t c = t; c < nc; c += kBuildThreads) cnt += (order_key(sS[c]) > thr) ? 1 : 0;
+        above = block_total(cnt, warp_cnt);
+    }
+    if (t == 0) running = 0;
+    __syncthreads();
+    // ties with the m-th score, in id order: the first m - above of them are kept
+    for (int32_t base = 0; base < nc; base += kBuildThreads) {
+        const int32_t c = base + t;
+        const uint32_t key = (c < nc) ? order_key(sS[c]) : 0u;
+        const bool tie = a.m > 0 && c < nc && key == thr;
+        const uint32_t ballot = __ballot_sync(0xffffffffu, tie);
+        if (lane == 0) warp_cnt[warp] = __popc(ballot);
+        __syncthreads();
+        if (t == 0) {
+            int32_t acc = 0;
+            for (int w = 0; w < kBuildThreads / 32; ++w) {
+                warp_off[w] = acc;
+                acc += warp_cnt[w];
+            }
+        }
+        __syncthreads();
+        if (c < nc) {
+            const int32_t eq_rank = running + warp_off[warp] + __popc(ballot & ((1u << lane) - 1u));
+            sIdx[c] = (a.m > 0 && (key > thr || (tie && eq_rank < a.m - above))) ? 1 : 0;
+        }
+        __syncthreads();
+        if (t == 0) running += warp_off[kBuildThreads / 32 - 1] + warp_cnt[kBuildThreads / 32 - 1];
+        __syncthreads();
     }
     if (t == 0) running = 0;
     __syncthreads();
@@ -255,6 +319,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
     const int32_t r = blockIdx.x;
     const int32_t si = a.src ? a.src[r] : -1 - r;
     int32_t tok = a.tok[r];
+    if (a.tok_copy && blockIdx.y == 0 && threadIdx.x == 0) a.tok_copy[r] = tok;
     if (tok < 0 || tok >= a.V) {
         if (threadIdx.x == 0 && blockIdx.y == 0) latch(a.status, kDevBounds);
         tok = 0;
