@@ -29,7 +29,7 @@ struct Layout {
     size_t pool_tok, pool_S, pool_par, pool_row, front_cand, front_S;
     size_t root_tok, node_tok, node_src, g, node_x, node_fhat;
     size_t st_feat, st_tok, st_pos, st_tokens, st_parents, st_positions, st_mask, st_acc_len,
-        st_acc_nodes, st_acc_tok;
+        st_acc_nodes, st_acc_tok, st_out_end, st_in_end;
     size_t total;
     size_t partials_bytes, counters_bytes;
     int32_t r_pad, n_cand, n_nodes, mask_words, node_chunk, eb;
@@ -74,6 +74,21 @@ Layout make_layout(const eagle_tree_config *c, int32_t num_sms) {
         return at;
     };
     L.status = take(sizeof(int32_t));
+    // host-step staging right after the status word: [status | outputs | inputs] is one range, so
+    // the host step moves its inputs (and a cleared status word) in one copy and its outputs (with
+    // the status word) in another
+    L.st_tokens = take(static_cast<size_t>(node_rows) * 4);
+    L.st_parents = take(static_cast<size_t>(node_rows) * 4);
+    L.st_positions = take(static_cast<size_t>(node_rows) * 4);
+    L.st_mask = take(static_cast<size_t>(node_rows) * L.mask_words * 4);
+    L.st_acc_len = take(static_cast<size_t>(B) * 4);
+    L.st_acc_nodes = take(static_cast<size_t>(B) * (d + 1) * 4);
+    L.st_acc_tok = take(static_cast<size_t>(B) * (d + 1) * 4);
+    L.st_out_end = o;
+    L.st_feat = take(static_cast<size_t>(B) * h * L.eb);
+    L.st_tok = take(static_cast<size_t>(B) * 4);
+    L.st_pos = take(static_cast<size_t>(B) * 4);
+    L.st_in_end = o;
     L.counters = take(L.counters_bytes);
     L.partials = take(L.partials_bytes);
     L.x = take(static_cast<size_t>(L.r_pad) * 2 * h * L.eb);
@@ -94,16 +109,6 @@ Layout make_layout(const eagle_tree_config *c, int32_t num_sms) {
     L.g = take(static_cast<size_t>(node_rows) * 4);
     L.node_x = take(static_cast<size_t>(L.node_chunk) * 2 * h * L.eb);
     L.node_fhat = take(static_cast<size_t>(L.node_chunk) * h * L.eb);
-    L.st_feat = take(static_cast<size_t>(B) * h * L.eb);
-    L.st_tok = take(static_cast<size_t>(B) * 4);
-    L.st_pos = take(static_cast<size_t>(B) * 4);
-    L.st_tokens = take(static_cast<size_t>(node_rows) * 4);
-    L.st_parents = take(static_cast<size_t>(node_rows) * 4);
-    L.st_positions = take(static_cast<size_t>(node_rows) * 4);
-    L.st_mask = take(static_cast<size_t>(node_rows) * L.mask_words * 4);
-    L.st_acc_len = take(static_cast<size_t>(B) * 4);
-    L.st_acc_nodes = take(static_cast<size_t>(B) * (d + 1) * 4);
-    L.st_acc_tok = take(static_cast<size_t>(B) * (d + 1) * 4);
     L.total = o;
     return L;
 }
@@ -195,8 +200,19 @@ struct eagle_tree {
     std::vector<int32_t> prof_tag;
     int32_t prof_n = 0;
     bool prof_on = true;
+    // host step: pinned image of the workspace range [status, inputs end), a side stream for the
+    // target logits and two events (created by the first eagle_tree_step_host)
+    uint8_t *h_stage = nullptr;
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_in = nullptr, ev_t = nullptr;
 
-    ~eagle_tree() { free_profile(); }
+    ~eagle_tree() {
+        free_profile();
+        if (ev_in) cudaEventDestroy(ev_in);
+        if (ev_t) cudaEventDestroy(ev_t);
+        if (side) cudaStreamDestroy(side);
+        if (h_stage) cudaFreeHost(h_stage);
+    }
     void free_profile() {
         for (cudaEvent_t e : prof_start) cudaEventDestroy(e);
         for (cudaEvent_t e : prof_stop) cudaEventDestroy(e);
@@ -592,12 +608,28 @@ eagle_status eagle_tree_step_host(eagle_tree *t, const void *h_root_feature, con
     const Layout &L = t->L;
     const int32_t B = c.batch, n = L.n_nodes, d = c.depth;
     const size_t tbytes = static_cast<size_t>(B) * n * c.vocab * (target_dtype == EAGLE_BF16 ? 2 : 4);
-    const auto H2D = cudaMemcpyHostToDevice;
-    const auto D2H = cudaMemcpyDeviceToHost;
-    EAGLE_CUDA(cudaMemcpyAsync(t->ws + L.st_feat, h_root_feature, static_cast<size_t>(B) * c.hidden * L.eb, H2D, st));
-    EAGLE_CUDA(cudaMemcpyAsync(t->ws + L.st_tok, h_root_token, sizeof(int32_t) * B, H2D, st));
-    if (h_pos_base) EAGLE_CUDA(cudaMemcpyAsync(t->ws + L.st_pos, h_pos_base, sizeof(int32_t) * B, H2D, st));
-    EAGLE_CUDA(cudaMemcpyAsync(d_target_staging, h_target_logits, tbytes, H2D, st));
+    if (!t->h_stage) {
+        if (cudaMallocHost(&t->h_stage, L.st_in_end - L.status) != cudaSuccess) {
+            t->h_stage = nullptr;
+            return EAGLE_ERR_CUDA;
+        }
+        EAGLE_CUDA(cudaStreamCreateWithFlags(&t->side, cudaStreamNonBlocking));
+        EAGLE_CUDA(cudaEventCreateWithFlags(&t->ev_in, cudaEventDisableTiming));
+        EAGLE_CUDA(cudaEventCreateWithFlags(&t->ev_t, cudaEventDisableTiming));
+    }
+    uint8_t *hs = t->h_stage;
+    const auto at = [&](size_t off) { return hs + (off - L.status); };
+    // inputs, and a cleared status word, in one copy
+    *reinterpret_cast<int32_t *>(hs) = 0;
+    std::memcpy(at(L.st_feat), h_root_feature, static_cast<size_t>(B) * c.hidden * L.eb);
+    std::memcpy(at(L.st_tok), h_root_token, sizeof(int32_t) * B);
+    if (h_pos_base) std::memcpy(at(L.st_pos), h_pos_base, sizeof(int32_t) * B);
+    EAGLE_CUDA(cudaMemcpyAsync(t->ws + L.status, hs, L.st_in_end - L.status, cudaMemcpyHostToDevice, st));
+    // the target logits arrive on the side stream while the draft runs; verify waits for them
+    EAGLE_CUDA(cudaEventRecord(t->ev_in, st));
+    EAGLE_CUDA(cudaStreamWaitEvent(t->side, t->ev_in, 0));
+    EAGLE_CUDA(cudaMemcpyAsync(d_target_staging, h_target_logits, tbytes, cudaMemcpyHostToDevice, t->side));
+    EAGLE_CUDA(cudaEventRecord(t->ev_t, t->side));
     eagle_status s;
     for (int32_t l = 0; l < d; ++l) {
         s = eagle_draft_level(t, l, t->ws + L.st_feat, t->at<int32_t>(L.st_tok), nullptr, stream);
@@ -607,19 +639,28 @@ eagle_status eagle_tree_step_host(eagle_tree *t, const void *h_root_feature, con
                                 t->at<int32_t>(L.st_parents), t->at<int32_t>(L.st_positions),
                                 t->at<uint32_t>(L.st_mask), nullptr, stream);
     if (s != EAGLE_OK) return s;
+    EAGLE_CUDA(cudaStreamWaitEvent(st, t->ev_t, 0));
     s = eagle_verify_greedy(t, t->at<int32_t>(L.st_tokens), t->at<int32_t>(L.st_parents), d_target_staging,
                             target_dtype, nullptr, t->at<int32_t>(L.st_acc_len), t->at<int32_t>(L.st_acc_nodes),
                             t->at<int32_t>(L.st_acc_tok), stream);
     if (s != EAGLE_OK) return s;
+    // the status word and every output in one copy
+    EAGLE_CUDA(cudaMemcpyAsync(hs, t->ws + L.status, L.st_out_end - L.status, cudaMemcpyDeviceToHost, st));
+    EAGLE_CUDA(cudaStreamSynchronize(st));
     const size_t nb = sizeof(int32_t) * B * n;
-    EAGLE_CUDA(cudaMemcpyAsync(h_tokens, t->ws + L.st_tokens, nb, D2H, st));
-    EAGLE_CUDA(cudaMemcpyAsync(h_parents, t->ws + L.st_parents, nb, D2H, st));
-    EAGLE_CUDA(cudaMemcpyAsync(h_positions, t->ws + L.st_positions, nb, D2H, st));
-    if (h_mask)
-        EAGLE_CUDA(cudaMemcpyAsync(h_mask, t->ws + L.st_mask, nb * L.mask_words, D2H, st));
-    EAGLE_CUDA(cudaMemcpyAsync(h_accept_len, t->ws + L.st_acc_len, sizeof(int32_t) * B, D2H, st));
-    EAGLE_CUDA(cudaMemcpyAsync(h_accept_tokens, t->ws + L.st_acc_tok, sizeof(int32_t) * B * (d + 1), D2H, st));
-    return eagle_tree_status(t, stream);
+    std::memcpy(h_tokens, at(L.st_tokens), nb);
+    std::memcpy(h_parents, at(L.st_parents), nb);
+    std::memcpy(h_positions, at(L.st_positions), nb);
+    if (h_mask) std::memcpy(h_mask, at(L.st_mask), nb * L.mask_words);
+    std::memcpy(h_accept_len, at(L.st_acc_len), sizeof(int32_t) * B);
+    std::memcpy(h_accept_tokens, at(L.st_acc_tok), sizeof(int32_t) * B * (d + 1));
+    const int32_t word = *reinterpret_cast<const int32_t *>(hs);
+    if (word != 0) {
+        EAGLE_CUDA(cudaMemset(t->status, 0, sizeof(int32_t)));  // read and cleared, as eagle_tree_status
+        if (word & kDevTimeout) return EAGLE_ERR_DEVICE_TIMEOUT;
+        return EAGLE_ERR_DEVICE_BOUNDS;
+    }
+    return EAGLE_OK;
 }
 
 eagle_status eagle_tree_profile(eagle_tree *t, int32_t max_launches) {

@@ -26,7 +26,8 @@
  * Conventions shared by every entry point:
  *   - All device memory is owned by the caller.  The library allocates no device memory: the
  *     handle works inside a caller-provided workspace, and weights are borrowed (they must
- *     outlive the handle).  Only the small host-side handle is allocated, by eagle_tree_init.
+ *     outlive the handle).  Only host-side objects are allocated: the handle, by eagle_tree_init,
+ *     and the pinned staging, side stream and events of eagle_tree_step_host, by its first call.
  *   - Every call that takes a stream only enqueues work on it: no host synchronisation, no
  *     allocation.  The exceptions are eagle_tree_init (which clears its workspace with a
  *     synchronous cudaMemset), eagle_tree_status and eagle_tree_step_host (which synchronise
@@ -184,9 +185,14 @@ EAGLE_API eagle_status eagle_tree_node_logits(eagle_tree *t, const void *d_root_
 /*
  * One whole step from host memory: copies the roots (and optional positions) and the target
  * logits to the device, runs levels 0..d-1, the rerank/build and the verify, copies the tree and
- * the verify results back, and synchronises `stream`.  Host buffers should be pinned for the
- * copies to be asynchronous.  d_target_staging is caller-owned device memory of
- * [B][m+1][V] elements of target_dtype that receives h_target_logits.
+ * the verify results back, and synchronises `stream`.  The roots go in one copy through a pinned
+ * staging image held by the handle; the target logits go on a side stream of the handle while
+ * the draft runs (h_target_logits should be pinned for that copy to be asynchronous); the
+ * outputs come back in one copy together with the device status word, which the step clears at
+ * its start and returns (like eagle_tree_status).  The first call allocates the pinned staging
+ * (cudaMallocHost), the side stream and two events; eagle_tree_destroy frees them.
+ * d_target_staging is caller-owned device memory of [B][m+1][V] elements of target_dtype that
+ * receives h_target_logits.
  *   h_root_feature [B][h] (cfg.dtype), h_root_token [B], h_pos_base [B] or NULL,
  *   h_target_logits [B][m+1][V]; outputs h_tokens/h_parents/h_positions [B][m+1],
  *   h_mask [B][m+1][W] (or NULL), h_accept_len [B], h_accept_tokens [B][d+1].
