@@ -203,14 +203,25 @@ struct eagle_tree {
     // host step: pinned image of the workspace range [status, inputs end), a side stream for the
     // target logits and two events (created by the first eagle_tree_step_host)
     uint8_t *h_stage = nullptr;
-    cudaStream_t side = nullptr;
-    cudaEvent_t ev_in = nullptr, ev_t = nullptr;
+    cudaStream_t own = nullptr, side = nullptr;  // the step's stream and the target-copy stream
+    cudaEvent_t ev_call = nullptr, ev_in = nullptr, ev_t = nullptr;
+    // the host step captured as a CUDA graph: replayed while (staging, dtype, positions given)
+    // stay the same; only the target copy's host source is patched per call
+    cudaGraphExec_t step_exec = nullptr;
+    cudaGraphNode_t step_tcopy = nullptr;
+    const void *graph_staging = nullptr;
+    int32_t graph_dtype = -1;
+    bool graph_pos = false, graph_failed = false;
+    int64_t graph_launches = 0;  // kernels one replay launches
 
     ~eagle_tree() {
         free_profile();
+        if (step_exec) cudaGraphExecDestroy(step_exec);
+        if (ev_call) cudaEventDestroy(ev_call);
         if (ev_in) cudaEventDestroy(ev_in);
         if (ev_t) cudaEventDestroy(ev_t);
         if (side) cudaStreamDestroy(side);
+        if (own) cudaStreamDestroy(own);
         if (h_stage) cudaFreeHost(h_stage);
     }
     void free_profile() {
@@ -590,6 +601,89 @@ eagle_status eagle_tree_status(eagle_tree *t, eagle_stream_t stream) {
     return EAGLE_OK;
 }
 
+// The device side of one host step, enqueued on `st`: one copy of [status = 0 | outputs | roots]
+// from the pinned image, the target logits on the side stream, levels 0..d-1, rerank/build,
+// verify (after the target copy), one copy of [status | outputs] back to the image.
+static eagle_status enqueue_host_step(eagle_tree *t, const void *h_target_logits, eagle_dtype target_dtype,
+                                      void *d_target_staging, bool with_pos, cudaStream_t st) {
+    const eagle_tree_config &c = t->cfg;
+    const Layout &L = t->L;
+    const int32_t B = c.batch, n = L.n_nodes;
+    const size_t tbytes = static_cast<size_t>(B) * n * c.vocab * (target_dtype == EAGLE_BF16 ? 2 : 4);
+    eagle_stream_t stream = reinterpret_cast<eagle_stream_t>(st);
+    EAGLE_CUDA(cudaMemcpyAsync(t->ws + L.status, t->h_stage, L.st_in_end - L.status, cudaMemcpyHostToDevice, st));
+    EAGLE_CUDA(cudaEventRecord(t->ev_in, st));
+    EAGLE_CUDA(cudaStreamWaitEvent(t->side, t->ev_in, 0));
+    EAGLE_CUDA(cudaMemcpyAsync(d_target_staging, h_target_logits, tbytes, cudaMemcpyHostToDevice, t->side));
+    EAGLE_CUDA(cudaEventRecord(t->ev_t, t->side));
+    eagle_status s;
+    for (int32_t l = 0; l < c.depth; ++l) {
+        s = eagle_draft_level(t, l, t->ws + L.st_feat, t->at<int32_t>(L.st_tok), nullptr, stream);
+        if (s != EAGLE_OK) return s;
+    }
+    s = eagle_rerank_build_tree(t, with_pos ? t->at<int32_t>(L.st_pos) : nullptr, t->at<int32_t>(L.st_tokens),
+                                t->at<int32_t>(L.st_parents), t->at<int32_t>(L.st_positions),
+                                t->at<uint32_t>(L.st_mask), nullptr, stream);
+    if (s != EAGLE_OK) return s;
+    EAGLE_CUDA(cudaStreamWaitEvent(st, t->ev_t, 0));
+    s = eagle_verify_greedy(t, t->at<int32_t>(L.st_tokens), t->at<int32_t>(L.st_parents), d_target_staging,
+                            target_dtype, nullptr, t->at<int32_t>(L.st_acc_len), t->at<int32_t>(L.st_acc_nodes),
+                            t->at<int32_t>(L.st_acc_tok), stream);
+    if (s != EAGLE_OK) return s;
+    EAGLE_CUDA(cudaMemcpyAsync(t->h_stage, t->ws + L.status, L.st_out_end - L.status, cudaMemcpyDeviceToHost, st));
+    return EAGLE_OK;
+}
+
+// Captures enqueue_host_step into a graph; on any failure the handle stays on eager launches.
+static void capture_host_step(eagle_tree *t, const void *h_target_logits, eagle_dtype target_dtype,
+                              void *d_target_staging, bool with_pos, cudaStream_t st) {
+    if (t->step_exec) {
+        cudaGraphExecDestroy(t->step_exec);
+        t->step_exec = nullptr;
+    }
+    const bool prof = t->prof_on;
+    t->prof_on = false;  // no profiling events inside the graph
+    const int64_t l0 = t->launches;
+    cudaGraph_t g = nullptr;
+    bool ok = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+    if (ok) {
+        const eagle_status s = enqueue_host_step(t, h_target_logits, target_dtype, d_target_staging, with_pos, st);
+        const cudaError_t e = cudaStreamEndCapture(st, &g);
+        ok = s == EAGLE_OK && e == cudaSuccess && g != nullptr;
+    }
+    t->prof_on = prof;
+    t->graph_launches = t->launches - l0;
+    t->launches = l0;
+    cudaGraphNode_t tcopy = nullptr;
+    if (ok) {
+        size_t nn = 0;
+        ok = cudaGraphGetNodes(g, nullptr, &nn) == cudaSuccess && nn > 0;
+        std::vector<cudaGraphNode_t> nodes(nn);
+        if (ok) ok = cudaGraphGetNodes(g, nodes.data(), &nn) == cudaSuccess;
+        for (size_t i = 0; ok && i < nn; ++i) {
+            cudaGraphNodeType ty;
+            if (cudaGraphNodeGetType(nodes[i], &ty) != cudaSuccess || ty != cudaGraphNodeTypeMemcpy) continue;
+            cudaMemcpy3DParms mp = {};
+            if (cudaGraphMemcpyNodeGetParams(nodes[i], &mp) == cudaSuccess && mp.dstPtr.ptr == d_target_staging)
+                tcopy = nodes[i];
+        }
+        ok = ok && tcopy != nullptr;
+    }
+    cudaGraphExec_t ex = nullptr;
+    if (ok) ok = cudaGraphInstantiate(&ex, g, 0) == cudaSuccess;
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();  // a failed capture leaves nothing behind
+    if (!ok) {
+        t->graph_failed = true;
+        return;
+    }
+    t->step_exec = ex;
+    t->step_tcopy = tcopy;
+    t->graph_staging = d_target_staging;
+    t->graph_dtype = target_dtype;
+    t->graph_pos = with_pos;
+}
+
 eagle_status eagle_tree_step_host(eagle_tree *t, const void *h_root_feature, const int32_t *h_root_token,
                                   const int32_t *h_pos_base, const void *h_target_logits, eagle_dtype target_dtype,
                                   void *d_target_staging, int32_t *h_tokens, int32_t *h_parents,
@@ -613,39 +707,45 @@ eagle_status eagle_tree_step_host(eagle_tree *t, const void *h_root_feature, con
             t->h_stage = nullptr;
             return EAGLE_ERR_CUDA;
         }
+        EAGLE_CUDA(cudaStreamCreateWithFlags(&t->own, cudaStreamNonBlocking));
         EAGLE_CUDA(cudaStreamCreateWithFlags(&t->side, cudaStreamNonBlocking));
+        EAGLE_CUDA(cudaEventCreateWithFlags(&t->ev_call, cudaEventDisableTiming));
         EAGLE_CUDA(cudaEventCreateWithFlags(&t->ev_in, cudaEventDisableTiming));
         EAGLE_CUDA(cudaEventCreateWithFlags(&t->ev_t, cudaEventDisableTiming));
     }
     uint8_t *hs = t->h_stage;
     const auto at = [&](size_t off) { return hs + (off - L.status); };
-    // inputs, and a cleared status word, in one copy
+    // the roots, and a cleared status word, into the pinned image
     *reinterpret_cast<int32_t *>(hs) = 0;
     std::memcpy(at(L.st_feat), h_root_feature, static_cast<size_t>(B) * c.hidden * L.eb);
     std::memcpy(at(L.st_tok), h_root_token, sizeof(int32_t) * B);
     if (h_pos_base) std::memcpy(at(L.st_pos), h_pos_base, sizeof(int32_t) * B);
-    EAGLE_CUDA(cudaMemcpyAsync(t->ws + L.status, hs, L.st_in_end - L.status, cudaMemcpyHostToDevice, st));
-    // the target logits arrive on the side stream while the draft runs; verify waits for them
-    EAGLE_CUDA(cudaEventRecord(t->ev_in, st));
-    EAGLE_CUDA(cudaStreamWaitEvent(t->side, t->ev_in, 0));
-    EAGLE_CUDA(cudaMemcpyAsync(d_target_staging, h_target_logits, tbytes, cudaMemcpyHostToDevice, t->side));
-    EAGLE_CUDA(cudaEventRecord(t->ev_t, t->side));
-    eagle_status s;
-    for (int32_t l = 0; l < d; ++l) {
-        s = eagle_draft_level(t, l, t->ws + L.st_feat, t->at<int32_t>(L.st_tok), nullptr, stream);
-        if (s != EAGLE_OK) return s;
+    const bool with_pos = h_pos_base != nullptr;
+    // The step runs on the handle's own stream, after everything already queued on the caller's
+    // (the legacy default stream cannot be captured into a graph; the call synchronises anyway).
+    EAGLE_CUDA(cudaEventRecord(t->ev_call, st));
+    st = t->own;
+    EAGLE_CUDA(cudaStreamWaitEvent(st, t->ev_call, 0));
+    if (!t->graph_failed &&
+        (!t->step_exec || t->graph_staging != d_target_staging || t->graph_dtype != target_dtype ||
+         t->graph_pos != with_pos))
+        capture_host_step(t, h_target_logits, target_dtype, d_target_staging, with_pos, st);
+    bool replayed = false;
+    if (t->step_exec && !t->graph_failed) {
+        // a source the graph cannot take (another kind of host memory) runs this call eagerly
+        if (cudaGraphExecMemcpyNodeSetParams1D(t->step_exec, t->step_tcopy, d_target_staging, h_target_logits,
+                                               tbytes, cudaMemcpyHostToDevice) == cudaSuccess) {
+            EAGLE_CUDA(cudaGraphLaunch(t->step_exec, st));
+            t->launches += t->graph_launches;
+            replayed = true;
+        } else {
+            cudaGetLastError();
+        }
     }
-    s = eagle_rerank_build_tree(t, h_pos_base ? t->at<int32_t>(L.st_pos) : nullptr, t->at<int32_t>(L.st_tokens),
-                                t->at<int32_t>(L.st_parents), t->at<int32_t>(L.st_positions),
-                                t->at<uint32_t>(L.st_mask), nullptr, stream);
-    if (s != EAGLE_OK) return s;
-    EAGLE_CUDA(cudaStreamWaitEvent(st, t->ev_t, 0));
-    s = eagle_verify_greedy(t, t->at<int32_t>(L.st_tokens), t->at<int32_t>(L.st_parents), d_target_staging,
-                            target_dtype, nullptr, t->at<int32_t>(L.st_acc_len), t->at<int32_t>(L.st_acc_nodes),
-                            t->at<int32_t>(L.st_acc_tok), stream);
-    if (s != EAGLE_OK) return s;
-    // the status word and every output in one copy
-    EAGLE_CUDA(cudaMemcpyAsync(hs, t->ws + L.status, L.st_out_end - L.status, cudaMemcpyDeviceToHost, st));
+    if (!replayed) {
+        const eagle_status s0 = enqueue_host_step(t, h_target_logits, target_dtype, d_target_staging, with_pos, st);
+        if (s0 != EAGLE_OK) return s0;
+    }
     EAGLE_CUDA(cudaStreamSynchronize(st));
     const size_t nb = sizeof(int32_t) * B * n;
     std::memcpy(h_tokens, at(L.st_tokens), nb);
@@ -728,6 +828,12 @@ eagle_status eagle_tree_profile_enable(eagle_tree *t, int32_t enable) {
 }
 
 int64_t eagle_tree_launch_count(const eagle_tree *t) { return t ? t->launches : 0; }
+
+int32_t eagle_tree_step_graphed(const eagle_tree *t) {
+    if (!t) return 0;
+    if (t->graph_failed) return -1;
+    return t->step_exec ? 1 : 0;
+}
 
 // ------------------------------------------------------------------------------------------------
 // Stateless entry points

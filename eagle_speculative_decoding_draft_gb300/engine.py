@@ -225,6 +225,11 @@ class EagleTree:
                         "kind": "lm_head" if (t >= 0 and t % 2) else "fc"})
         return out
 
+    def step_graphed(self) -> int:
+        """1: step_host replays a captured graph; 0: not yet; -1: capture failed and step_host
+        launches directly."""
+        return int(self.lib.eagle_tree_step_graphed(self._h))
+
     def launch_count(self) -> int:
         return int(self.lib.eagle_tree_launch_count(self._h))
 

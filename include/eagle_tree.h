@@ -185,12 +185,17 @@ EAGLE_API eagle_status eagle_tree_node_logits(eagle_tree *t, const void *d_root_
 /*
  * One whole step from host memory: copies the roots (and optional positions) and the target
  * logits to the device, runs levels 0..d-1, the rerank/build and the verify, copies the tree and
- * the verify results back, and synchronises `stream`.  The roots go in one copy through a pinned
+ * the verify results back, and returns when they are on the host.  The work runs on a stream of
+ * the handle, ordered after everything already queued on `stream`.  The roots go in one copy through a pinned
  * staging image held by the handle; the target logits go on a side stream of the handle while
  * the draft runs (h_target_logits should be pinned for that copy to be asynchronous); the
  * outputs come back in one copy together with the device status word, which the step clears at
  * its start and returns (like eagle_tree_status).  The first call allocates the pinned staging
- * (cudaMallocHost), the side stream and two events; eagle_tree_destroy frees them.
+ * (cudaMallocHost), two streams and three events; eagle_tree_destroy frees them.  The whole
+ * sequence is captured once into a CUDA graph (again whenever
+ * d_target_staging, target_dtype or the presence of h_pos_base changes) and replayed, with only
+ * the target copy's host source updated per call; where capture is not possible the same work
+ * is launched directly.
  * d_target_staging is caller-owned device memory of [B][m+1][V] elements of target_dtype that
  * receives h_target_logits.
  *   h_root_feature [B][h] (cfg.dtype), h_root_token [B], h_pos_base [B] or NULL,
@@ -269,6 +274,9 @@ EAGLE_API eagle_status eagle_tree_profile_read(eagle_tree *t, int32_t *launches,
 EAGLE_API eagle_status eagle_tree_profile_list(eagle_tree *t, int32_t cap, int32_t *n, float *ms,
                                                double *bytes, double *flops, int32_t *tag);
 EAGLE_API int64_t eagle_tree_launch_count(const eagle_tree *t);
+/* 1 when eagle_tree_step_host replays a captured graph, 0 before its first call, -1 when
+ * capture failed and the host step launches directly. */
+EAGLE_API int32_t eagle_tree_step_graphed(const eagle_tree *t);
 
 /* ------------------------------------------------------------------------------------------ */
 /* Stateless kernels of the path, for callers that keep their own state (and for tests).      */

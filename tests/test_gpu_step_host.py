@@ -60,5 +60,8 @@ def test_host_step_matches_the_device_step(dev, wl):
         assert torch.equal(host["accept_len"], ver["accept_len"].cpu())
         assert torch.equal(host["accept_tokens"], ver["accept_tokens"].cpu())
         assert torch.equal(staging.cpu(), T.cpu())
+        # every call after the first capture replays the graph
+        if it >= 1:
+            assert eng.step_graphed() == 1
     eng.status()
     eng.close()
