@@ -8,6 +8,8 @@
 #include <new>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/eagle_tree.h"
 #include "common.cuh"
 #include "kernels.cuh"
@@ -21,6 +23,14 @@ constexpr int32_t kMaxDepth = 32;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// NVTX range over one C-ABI call (host side only; free when no tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 int32_t round16(int32_t x) { return (x + 15) / 16 * 16; }
 
@@ -302,6 +312,7 @@ size_t eagle_tree_workspace_bytes(const eagle_tree_config *cfg) {
 }
 
 eagle_status eagle_tree_init(const eagle_tree_config *cfg, void *d_ws, size_t ws_bytes, eagle_tree **out) {
+    NvtxRange nvtx_range("eagle_tree_init");
     if (!out) return EAGLE_ERR_INVALID_ARG;
     *out = nullptr;
     if (!config_ok(cfg)) return EAGLE_ERR_INVALID_ARG;
@@ -384,6 +395,7 @@ eagle_status eagle_tree_get_layout(const eagle_tree *t, eagle_tree_layout *o) {
 
 eagle_status eagle_draft_level(eagle_tree *t, int32_t level, const void *d_root_feature,
                                const int32_t *d_root_token, float *d_logits_out, eagle_stream_t stream) {
+    NvtxRange nvtx_range("eagle_draft_level");
     if (!t) return EAGLE_ERR_INVALID_ARG;
     const eagle_tree_config &c = t->cfg;
     if (level < 0 || level >= c.depth) return EAGLE_ERR_INVALID_ARG;
@@ -474,6 +486,7 @@ eagle_status eagle_draft_level(eagle_tree *t, int32_t level, const void *d_root_
 eagle_status eagle_rerank_build_tree(eagle_tree *t, const int32_t *d_pos_base, int32_t *d_tokens,
                                      int32_t *d_parents, int32_t *d_positions, uint32_t *d_mask,
                                      float *d_logscore, eagle_stream_t stream) {
+    NvtxRange nvtx_range("eagle_rerank_build_tree");
     if (!t) return EAGLE_ERR_INVALID_ARG;
     if (t->next_level != t->cfg.depth) return EAGLE_ERR_STATE;
     const eagle_tree_config &c = t->cfg;
@@ -516,6 +529,7 @@ eagle_status eagle_verify_greedy(eagle_tree *t, const int32_t *d_tokens, const i
                                  const void *d_target_logits, eagle_dtype target_dtype,
                                  const int32_t *d_target_ids, int32_t *d_accept_len, int32_t *d_accept_nodes,
                                  int32_t *d_accept_tokens, eagle_stream_t stream) {
+    NvtxRange nvtx_range("eagle_verify_greedy");
     if (!t) return EAGLE_ERR_INVALID_ARG;
     const eagle_tree_config &c = t->cfg;
     if (c.batch == 0) return EAGLE_OK;
@@ -544,6 +558,7 @@ eagle_status eagle_verify_greedy(eagle_tree *t, const int32_t *d_tokens, const i
 
 eagle_status eagle_tree_node_logits(eagle_tree *t, const void *d_root_feature, float *d_node_logits,
                                     eagle_stream_t stream) {
+    NvtxRange nvtx_range("eagle_tree_node_logits");
     if (!t) return EAGLE_ERR_INVALID_ARG;
     if (!t->tree_built) return EAGLE_ERR_STATE;
     const eagle_tree_config &c = t->cfg;
@@ -689,6 +704,7 @@ eagle_status eagle_tree_step_host(eagle_tree *t, const void *h_root_feature, con
                                   void *d_target_staging, int32_t *h_tokens, int32_t *h_parents,
                                   int32_t *h_positions, uint32_t *h_mask, int32_t *h_accept_len,
                                   int32_t *h_accept_tokens, eagle_stream_t stream) {
+    NvtxRange nvtx_range("eagle_tree_step_host");
     if (!t) return EAGLE_ERR_INVALID_ARG;
     const eagle_tree_config &c = t->cfg;
     if (c.batch == 0) return EAGLE_OK;
@@ -829,6 +845,17 @@ eagle_status eagle_tree_profile_enable(eagle_tree *t, int32_t enable) {
 
 int64_t eagle_tree_launch_count(const eagle_tree *t) { return t ? t->launches : 0; }
 
+eagle_status eagle_test_bounded_wait(int64_t limit_ns, int32_t *d_status, eagle_stream_t stream) {
+    if (!d_status || limit_ns < 1 || limit_ns > 10000000000ll) return EAGLE_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    EAGLE_CUDA(launch_bounded_wait(static_cast<uint64_t>(limit_ns), d_status, st));
+    int32_t word = 0;
+    EAGLE_CUDA(cudaMemcpyAsync(&word, d_status, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+    EAGLE_CUDA(cudaMemsetAsync(d_status, 0, sizeof(int32_t), st));
+    EAGLE_CUDA(cudaStreamSynchronize(st));
+    return (word & kDevTimeout) ? EAGLE_ERR_DEVICE_TIMEOUT : EAGLE_OK;
+}
+
 int32_t eagle_tree_step_graphed(const eagle_tree *t) {
     if (!t) return 0;
     if (t->graph_failed) return -1;
@@ -841,6 +868,7 @@ int32_t eagle_tree_step_graphed(const eagle_tree *t) {
 
 eagle_status eagle_row_topk(const void *d_logits, eagle_dtype dtype, int32_t rows, int32_t vocab, int64_t ld,
                             int32_t k, int32_t *d_ids, float *d_vals, float *d_lse, eagle_stream_t stream) {
+    NvtxRange nvtx_range("eagle_row_topk");
     if (rows < 0 || vocab < 1 || ld < vocab || k < 1 || k > kMaxTopk || k > vocab) return EAGLE_ERR_INVALID_ARG;
     if (dtype != EAGLE_F32 && dtype != EAGLE_BF16) return EAGLE_ERR_INVALID_ARG;
     if (rows == 0) return EAGLE_OK;
@@ -854,6 +882,7 @@ eagle_status eagle_expand(int32_t level, int32_t batch, int32_t topk, int32_t de
                           const float *d_row_logp, const int32_t *d_front_cand_in, const float *d_front_S_in,
                           int32_t *d_front_cand_out, float *d_front_S_out, int32_t *d_pool_tok, float *d_pool_S,
                           int32_t *d_pool_parent, int32_t *d_pool_row, eagle_stream_t stream) {
+    NvtxRange nvtx_range("eagle_expand");
     if (batch < 0 || topk < 1 || topk > kMaxTopk || depth < 1 || depth > kMaxDepth || level < 0 || level >= depth)
         return EAGLE_ERR_INVALID_ARG;
     const int64_t nc = topk + static_cast<int64_t>(depth - 1) * topk * topk;
@@ -889,6 +918,7 @@ eagle_status eagle_build_tree(int32_t batch, int32_t topk, int32_t depth, int32_
                               const float *d_pool_S, const int32_t *d_pool_parent, const int32_t *d_root_token,
                               const int32_t *d_pos_base, int32_t *d_tokens, int32_t *d_parents, int32_t *d_positions,
                               uint32_t *d_mask, float *d_logscore, int32_t *d_status, eagle_stream_t stream) {
+    NvtxRange nvtx_range("eagle_build_tree");
     if (batch < 0 || topk < 1 || topk > kMaxTopk || depth < 1 || depth > kMaxDepth) return EAGLE_ERR_INVALID_ARG;
     const int64_t nc = topk + static_cast<int64_t>(depth - 1) * topk * topk;
     if (nc > kMaxCandidates || num_keep < 0 || num_keep > nc) return EAGLE_ERR_INVALID_ARG;
@@ -921,6 +951,7 @@ eagle_status eagle_build_tree(int32_t batch, int32_t topk, int32_t depth, int32_
 eagle_status eagle_verify_walk(int32_t batch, int32_t num_nodes, int32_t depth, const int32_t *d_tokens,
                                const int32_t *d_parents, const int32_t *d_target_ids, int32_t *d_accept_len,
                                int32_t *d_accept_nodes, int32_t *d_accept_tokens, eagle_stream_t stream) {
+    NvtxRange nvtx_range("eagle_verify_walk");
     if (batch < 0 || num_nodes < 1 || depth < 0) return EAGLE_ERR_INVALID_ARG;
     if (batch == 0) return EAGLE_OK;
     if (!d_tokens || !d_parents || !d_target_ids || !d_accept_len || !d_accept_nodes || !d_accept_tokens)
@@ -936,6 +967,7 @@ eagle_status eagle_verify_sample(int32_t batch, int32_t num_nodes, int32_t vocab
                                  const float *d_u_accept, const float *d_u_bonus, float *d_scratch,
                                  int32_t *d_accept_len, int32_t *d_accept_nodes, int32_t *d_accept_tokens,
                                  eagle_stream_t stream) {
+    NvtxRange nvtx_range("eagle_verify_sample");
     if (batch < 0 || num_nodes < 1 || num_nodes > kMaxCandidates + 1 || vocab < 1 || depth < 0 || depth > 64)
         return EAGLE_ERR_INVALID_ARG;
     if (!(temperature > 0.0f) || !(temperature < INFINITY) || (mode != 0 && mode != 1)) return EAGLE_ERR_INVALID_ARG;
@@ -960,6 +992,7 @@ size_t eagle_linear_workspace_bytes(int32_t out_features, int32_t rows) {
 eagle_status eagle_linear_bf16(const void *d_w, int64_t ldw, const void *d_x, int64_t ldx, const void *d_bias,
                                int32_t out_features, int32_t in_features, int32_t rows, void *d_y, int64_t ldy,
                                int32_t out_bf16, void *d_ws, size_t ws_bytes, eagle_stream_t stream) {
+    NvtxRange nvtx_range("eagle_linear_bf16");
     if (out_features < 1 || in_features < 1 || rows < 1 || rows > kLinearMaxRows) return EAGLE_ERR_INVALID_ARG;
     if (!d_w || !d_x || !d_y || !d_ws) return EAGLE_ERR_INVALID_ARG;
     if (ldw < in_features || ldx < in_features || ldy < out_features) return EAGLE_ERR_INVALID_ARG;

@@ -169,4 +169,8 @@ struct GatherArgs {
 };
 cudaError_t launch_gather(const GatherArgs &a, cudaStream_t st);
 
+// Test hook: a wait on an mbarrier nothing arrives on, bounded by limit_ns; latches the timeout
+// bit in *status.
+cudaError_t launch_bounded_wait(uint64_t limit_ns, int32_t *status, cudaStream_t st);
+
 }  // namespace eagle

@@ -336,6 +336,19 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
                          : __ldg(reinterpret_cast<const uint4 *>(esrc) + (i - vh));
 }
 
+// ---------------------------------------------------------------------------------------------
+// Test hook: one thread waits, with the bounded wait every device wait of the library uses, on an
+// mbarrier that nothing will ever arrive on; when the limit passes it latches the timeout bit in
+// the status word and returns.  Proves the timeout path without faulting or hanging anything.
+// ---------------------------------------------------------------------------------------------
+__global__ void bounded_wait_kernel(uint64_t limit_ns, int32_t *status) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    if (!mbar_wait(&bar, 0, nullptr, limit_ns)) latch(status, kDevTimeout);
+}
+
 }  // namespace
 
 cudaError_t launch_expand(const ExpandArgs &a, cudaStream_t st) {
@@ -375,6 +388,11 @@ cudaError_t launch_gather(const GatherArgs &a, cudaStream_t st) {
     int32_t y = static_cast<int32_t>((bytes + 4095) / 4096);
     if (y < 1) y = 1;
     return launch_pdl(gather_kernel, dim3(a.n_rows, y), dim3(256), 0, st, a);
+}
+
+cudaError_t launch_bounded_wait(uint64_t limit_ns, int32_t *status, cudaStream_t st) {
+    bounded_wait_kernel<<<1, 32, 0, st>>>(limit_ns, status);
+    return cudaGetLastError();
 }
 
 }  // namespace eagle

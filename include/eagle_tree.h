@@ -274,6 +274,16 @@ EAGLE_API eagle_status eagle_tree_profile_read(eagle_tree *t, int32_t *launches,
 EAGLE_API eagle_status eagle_tree_profile_list(eagle_tree *t, int32_t cap, int32_t *n, float *ms,
                                                double *bytes, double *flops, int32_t *tag);
 EAGLE_API int64_t eagle_tree_launch_count(const eagle_tree *t);
+/*
+ * Test hook (no counterpart on the pages): shows that a device wait gives up instead of hanging.
+ * One thread waits, through the bounded wait that every waiting kernel of this library uses, on
+ * an mbarrier nothing arrives on; after limit_ns (1 .. 10^10 ns) it sets the timeout bit in
+ * *d_status (a caller-owned int32 in device memory) and returns.  The call synchronises `stream`,
+ * reads and clears the word, and returns EAGLE_ERR_DEVICE_TIMEOUT when the bit was set (else
+ * EAGLE_OK).  INVALID_ARG for a limit out of range or a null pointer, CUDA on a launch error.
+ */
+EAGLE_API eagle_status eagle_test_bounded_wait(int64_t limit_ns, int32_t *d_status,
+                                               eagle_stream_t stream);
 /* 1 when eagle_tree_step_host replays a captured graph, 0 before its first call, -1 when
  * capture failed and the host step launches directly. */
 EAGLE_API int32_t eagle_tree_step_graphed(const eagle_tree *t);

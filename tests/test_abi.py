@@ -114,3 +114,11 @@ def test_verify_sample_rejects_bad_arguments_on_the_host(lib):
     assert ok(1, 5, 10, 1, *ptrs_in, 1.0, 0, 0.0, *([None] + ptrs_out[1:]), None) == 1
     assert ok(0, 5, 10, 1, *([None] * 4), 1.0, 0, 0.0, *([None] * 6), None) == 0  # empty batch
 
+
+def test_bounded_wait_hook_rejects_bad_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+    assert lib.eagle_test_bounded_wait(0, P(256), None) == 1
+    assert lib.eagle_test_bounded_wait(-5, P(256), None) == 1
+    assert lib.eagle_test_bounded_wait(10**11, P(256), None) == 1
+    assert lib.eagle_test_bounded_wait(1000, None, None) == 1
+
