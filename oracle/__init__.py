@@ -73,6 +73,8 @@ def lib():
             L.orc_draft_tree.argtypes = [ctypes.POINTER(Dims)] + [P] * 24
             L.orc_verify_greedy.restype = i32
             L.orc_verify_greedy.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
+            L.orc_draft_extend.restype = i32
+            L.orc_draft_extend.argtypes = [ctypes.POINTER(Dims)] + [P] * 5 + [i32] + [P] * 10
             L.orc_verify_sample.restype = i32
             L.orc_verify_sample.argtypes = [i32, i32, i32, i32, P, P, P, P, ctypes.c_double, i32,
                                             ctypes.c_double, P, P, P, P, P]
@@ -218,6 +220,37 @@ def draft_tree(w_fc, b_fc, w_lm, emb, root_feat, root_tok, depth: int, topk: int
         _ptr(g("node_z")))
     if rc != ORC_OK:
         raise RuntimeError(f"orc_draft_tree failed with code {rc}")
+    return out
+
+
+def draft_extend(w_fc, b_fc, w_lm, emb, node_feat, accept_len, accept_nodes, accept_tok,
+                 depth: int, topk: int, is_bf16: bool, logits: bool = True) -> dict:
+    """Draft extend over each request's accepted path (see orc_draft_extend).  node_feat
+    [B][n][h] (torch bf16 or fp32 tensor, or numpy fp32); accept_* from the verify.  Returns
+    next_feat [B][h] fp32, next_tok [B], path_fhat [B][d+1][h], path_z [B][d+1][V] (if logits),
+    ids / logp [B][k] and lse [B] of the last verified row."""
+    fc, bfc, lm, em = (raw(w_fc, is_bf16), raw(b_fc, is_bf16), raw(w_lm, is_bf16), raw(emb, is_bf16))
+    if hasattr(node_feat, "detach"):  # torch: widen bf16 exactly
+        F = np.ascontiguousarray(node_feat.detach().cpu().float().numpy())
+    else:
+        F = np.ascontiguousarray(node_feat, dtype=np.float32)
+    B, n, h = F.shape
+    V = lm.shape[0]
+    al = np.ascontiguousarray(accept_len, dtype=np.int32)
+    an = np.ascontiguousarray(accept_nodes, dtype=np.int32)
+    at = np.ascontiguousarray(accept_tok, dtype=np.int32)
+    dims = Dims(B, h, V, depth, topk, 0, int(is_bf16))
+    out = {"next_feat": np.zeros((B, h), np.float32), "next_tok": np.zeros(B, np.int32),
+           "path_fhat": np.zeros((B, depth + 1, h), np.float32),
+           "path_z": np.zeros((B, depth + 1, V), np.float32) if logits else None,
+           "ids": np.zeros((B, topk), np.int32), "logp": np.zeros((B, topk), np.float32),
+           "lse": np.zeros(B, np.float32)}
+    rc = lib().orc_draft_extend(ctypes.byref(dims), _ptr(fc), _ptr(bfc), _ptr(lm), _ptr(em), _ptr(F), n,
+                                _ptr(al), _ptr(an), _ptr(at), _ptr(out["next_feat"]),
+                                _ptr(out["next_tok"]), _ptr(out["path_fhat"]), _ptr(out["path_z"]),
+                                _ptr(out["ids"]), _ptr(out["logp"]), _ptr(out["lse"]))
+    if rc != ORC_OK:
+        raise RuntimeError(f"orc_draft_extend failed with code {rc}")
     return out
 
 

@@ -434,6 +434,75 @@ done:
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* Draft extend: the next round's root                                                        */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * [zdszero] "在 SGLang 里": one decode step is one target verify, (steps - 1) draft forwards and
+ * one draft extend; the draft's own features along the tree are guesses, so after the verify the
+ * draft runs again over the verified positions with the target's true hidden states and the
+ * accepted tokens, and the last verified position is where the next round starts (its top-k is
+ * the next round's first level).  [notes04] §6.2 and §12 item 3: the true features of the
+ * accepted path start the next round's draft.
+ * For request b, with path nodes a_0 = 0 (the root), a_1 .. a_L (L = accept_len[b]) and the
+ * tokens that follow them accept_tok[b][0..L] (the accepted tokens, then the bonus):
+ *   row i (0 <= i <= L) = [F[b][a_i] || E[accept_tok[b][i]]]
+ *   f^_i = FC(row i) (rounded once to bf16 for bf16), z_i = LM_head(f^_i)
+ *   next root: feature F[b][a_L], token accept_tok[b][L]; its level-0 row is row L, whose
+ *   log-softmax and top-k are returned (the next round's first level).
+ * Rows L < i <= depth of the [B][depth+1] outputs repeat row L.
+ *   node_feat [B][n_nodes][h] fp32 (bf16 features widened exactly), outputs: next_feat [B][h],
+ *   next_tok [B], path_fhat [B][depth+1][h], path_z [B][depth+1][V] (or NULL), ids / logp [B][k],
+ *   lse [B].
+ * Pins: row L equals orc_draft_tree's level-0 row for the root (F[b][a_L], bonus); the path rows
+ * against their construction by hand in the test.
+ */
+int32_t orc_draft_extend(const orc_dims *dm, const void *w_fc, const void *b_fc, const void *w_lm,
+                         const void *emb, const float *node_feat, int32_t n_nodes,
+                         const int32_t *accept_len, const int32_t *accept_nodes,
+                         const int32_t *accept_tok, float *next_feat, int32_t *next_tok,
+                         float *path_fhat, float *path_z, int32_t *ids, float *logp, float *lse) {
+    const int32_t B = dm->batch, h = dm->hidden, V = dm->vocab, d = dm->depth, k = dm->topk;
+    const int32_t bf = dm->is_bf16;
+    if (B < 0 || h < 1 || V < 1 || d < 1 || k < 1 || k > V || n_nodes < 1) return ORC_ERR_ARG;
+    float *z = (float *)malloc(sizeof(float) * (size_t)V);
+    float *fo = (float *)malloc(sizeof(float) * (size_t)h);
+    if (!z || !fo) {
+        free(z); free(fo);
+        return ORC_ERR_NOMEM;
+    }
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t L = accept_len[b];
+        if (L < 0 || L > d) {
+            free(z); free(fo);
+            return ORC_ERR_ARG;
+        }
+        for (int32_t i = 0; i <= d; ++i) {
+            const int32_t r = i <= L ? i : L;
+            const int32_t node = accept_nodes[(int64_t)b * (d + 1) + r];
+            const int32_t tok = accept_tok[(int64_t)b * (d + 1) + r];
+            if (node < 0 || node >= n_nodes || tok < 0 || tok >= V) {
+                free(z); free(fo);
+                return ORC_ERR_ARG;
+            }
+            const float *feat = node_feat + ((int64_t)b * n_nodes + node) * h;
+            orc_fc_row(h, bf, w_fc, b_fc, feat, emb, tok, fo);
+            orc_lm_head_row(h, V, bf, w_lm, fo, z);
+            memcpy(path_fhat + ((int64_t)b * (d + 1) + i) * h, fo, sizeof(float) * (size_t)h);
+            if (path_z) memcpy(path_z + ((int64_t)b * (d + 1) + i) * V, z, sizeof(float) * (size_t)V);
+            if (i == L) {
+                orc_log_softmax_topk(V, k, z, ids + (int64_t)b * k, logp + (int64_t)b * k, lse + b);
+                memcpy(next_feat + (int64_t)b * h, feat, sizeof(float) * (size_t)h);
+                next_tok[b] = tok;
+            }
+        }
+    }
+    free(z);
+    free(fo);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* Greedy tree verification                                                                   */
 /* ------------------------------------------------------------------------------------------ */
 
