@@ -438,6 +438,38 @@ def run_eagle(args, w):
     sample_us = s0.elapsed_time(s1) * 1e3 / S_CALLS
     sample_accept = float(torch.stack(sacc).float().mean().item())
 
+    # ---------------- the multi-round loop with draft extend ----------------
+    # Steady state of decoding: each round starts from the previous verify through
+    # eagle_draft_extend (the FC over every verified position, then level 0 of the next tree),
+    # then levels 1..d-1, the rerank/build and the greedy verify.  Target features of the tree
+    # nodes are synthetic N(0, 1); the target logits cycle over the input sets.
+    fgen = torch.Generator(device=dev)
+    fgen.manual_seed(99 + rank)
+    Fn = [torch.randn(B, n, h, generator=fgen, device=dev).to(fdt) for _ in range(N_INPUT_SETS)]
+    eng.step(feat0, tok0, T0, tree_out=tree_out, verify_out=ver_out)
+
+    def one_round(i):
+        _, _, Ti = sets[i % N_INPUT_SETS]
+        eng.extend(Fn[i % N_INPUT_SETS], ver_out["accept_len"], ver_out["accept_nodes"],
+                   ver_out["accept_tokens"])
+        for lvl in range(1, d):
+            eng.draft_level(lvl)
+        eng.rerank_build_tree(out=tree_out)
+        eng.verify_greedy(tree_out["tokens"], tree_out["parents"], Ti, out=ver_out)
+
+    for i in range(10):
+        one_round(i)
+    ROUNDS = max(100, K // 4)
+    torch.cuda.synchronize()
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record()
+    for i in range(ROUNDS):
+        one_round(i)
+    r1.record()
+    torch.cuda.synchronize()
+    round_ms = r0.elapsed_time(r1) / ROUNDS
+    eng.status()
+
     peak, peak_kind = hbm_peak()
     tpeak, tpeak_kind = tensor_peak()
     achieved = gemm_bytes / (gemm_ms * 1e-3) / 1e9 if gemm_ms > 0 else None
@@ -471,6 +503,11 @@ def run_eagle(args, w):
                 "how": "eagle_tree_step_host per step: pinned host inputs and target logits "
                        "copied in, tree and verify results copied out, stream synchronised"},
         "gpu_launches": int(sum_over_ranks(launches)),
+        "round_with_extend": {"value": 1e3 / round_ms, "unit": "rounds/s", "ms_per_round": round_ms,
+                              "rounds": ROUNDS,
+                              "how": "eagle_draft_extend from the previous verify (FC over every "
+                                     "verified position + the next tree's level 0), levels 1..d-1, "
+                                     "rerank/build, greedy verify; CUDA events, eager launches"},
         "sampling_verify": {"us_per_call": sample_us, "mean_accept_len": sample_accept,
                             "temperature": 1.0, "mode": "recursive rejection sampling",
                             "how": "eagle_verify_sample on the step's tree; q = draft logits of "

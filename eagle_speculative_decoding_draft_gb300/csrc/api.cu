@@ -37,7 +37,7 @@ int32_t round16(int32_t x) { return (x + 15) / 16 * 16; }
 struct Layout {
     size_t status, counters, partials, x, fhat, logits, row_ids, row_logp, row_lse;
     size_t pool_tok, pool_S, pool_par, pool_row, front_cand, front_S;
-    size_t root_tok, node_tok, node_src, g, node_x, node_fhat;
+    size_t root_tok, node_tok, node_src, g, node_x, node_fhat, ext_x, ext_fhat;
     size_t st_feat, st_tok, st_pos, st_tokens, st_parents, st_positions, st_mask, st_acc_len,
         st_acc_nodes, st_acc_tok, st_out_end, st_in_end;
     size_t total;
@@ -71,8 +71,9 @@ Layout make_layout(const eagle_tree_config *c, int32_t num_sms) {
     const int64_t node_rows = B * L.n_nodes;
     L.node_chunk = static_cast<int32_t>(node_rows < kLinearMaxRows ? (node_rows > 0 ? node_rows : 1)
                                                                    : kLinearMaxRows);
-    const int32_t max_rows = static_cast<int32_t>(
-        std::min<int64_t>(kLinearMaxRows, std::max<int64_t>(L.r_pad, L.node_chunk)));
+    const int64_t ext_rows = B * (d + 1);  // draft extend: every verified position of every request
+    const int32_t max_rows = static_cast<int32_t>(std::min<int64_t>(
+        kLinearMaxRows, std::max<int64_t>(std::max<int64_t>(L.r_pad, L.node_chunk), ext_rows)));
     if (c->dtype == EAGLE_BF16) {
         L.partials_bytes = linear_partials_bytes(num_sms, linear_n_tile(max_rows));
         L.counters_bytes = std::max(linear_counters_bytes(c->hidden), linear_counters_bytes(c->vocab));
@@ -119,6 +120,8 @@ Layout make_layout(const eagle_tree_config *c, int32_t num_sms) {
     L.g = take(static_cast<size_t>(node_rows) * 4);
     L.node_x = take(static_cast<size_t>(L.node_chunk) * 2 * h * L.eb);
     L.node_fhat = take(static_cast<size_t>(L.node_chunk) * h * L.eb);
+    L.ext_x = take(static_cast<size_t>(ext_rows) * 2 * h * L.eb);
+    L.ext_fhat = take(static_cast<size_t>(ext_rows) * h * L.eb);
     L.total = o;
     return L;
 }
@@ -204,6 +207,7 @@ struct eagle_tree {
     bool tree_built = false;
     int32_t front_current = 0;
     std::vector<LinearSeq> fc, lm;  // per level (bf16 only)
+    LinearSeq fc_ext;               // the draft extend's FC over B*(d+1) rows (bf16 only)
     int64_t launches = 0;           // kernels launched by this handle
     std::vector<cudaEvent_t> prof_start, prof_stop;
     std::vector<double> prof_bytes, prof_flops;
@@ -350,6 +354,12 @@ eagle_status eagle_tree_init(const eagle_tree_config *cfg, void *d_ws, size_t ws
         t->lm.resize(d);
         for (int32_t l = 0; l < d; ++l) {
             const int32_t R = t->rows_of(l);
+            if (l == 0 && !plan_seq(&t->fc_ext, cfg->fc_weight, 2 * h, h, 2 * h, t->ws + L.ext_x, 2 * h,
+                                    B * (d + 1), cfg->fc_bias, t->ws + L.ext_fhat, h, 1, 2, t->partials,
+                                    t->counters, t->status, sms)) {
+                delete t;
+                return EAGLE_ERR_UNSUPPORTED;
+            }
             if (!plan_seq(&t->fc[l], cfg->fc_weight, 2 * h, h, 2 * h, t->ws + L.x, 2 * h, R, cfg->fc_bias,
                           t->fhat_level(l), h, 1, 2, t->partials, t->counters, t->status, sms) ||
                 !plan_seq(&t->lm[l], cfg->lm_head, h, V, h, t->fhat_level(l), h, R, nullptr,
@@ -390,6 +400,62 @@ eagle_status eagle_tree_get_layout(const eagle_tree *t, eagle_tree_layout *o) {
     o->mask_words = L.mask_words;
     o->front_current = t->front_current;
     o->num_sms = t->num_sms;
+    return EAGLE_OK;
+}
+
+// The part of a draft level after its FC: LM head on the level's f^ rows, log-softmax + top-k of
+// every row, expand (pool, next frontier, next level's rows), and the level bookkeeping.
+static eagle_status level_tail(eagle_tree *t, int32_t level, float *d_logits_out, cudaStream_t st) {
+    const eagle_tree_config &c = t->cfg;
+    const Layout &L = t->L;
+    const int32_t B = c.batch, h = c.hidden, V = c.vocab, k = c.topk, d = c.depth;
+    const int32_t R = t->rows_of(level);
+    void *x = t->ws + L.x;
+    void *fh = t->fhat_level(level);
+    const bool bf16 = c.dtype == EAGLE_BF16;
+    // LM head: z = W_lm f^
+    float *lg = d_logits_out ? d_logits_out : t->at<float>(L.logits);
+    if (bf16) {
+        EAGLE_CUDA(t->run(t->lm[level], st, d_logits_out, V, 4, 2 * level + 1));
+    } else {
+        EAGLE_CUDA(launch_linear_f32(reinterpret_cast<const float *>(c.lm_head), h,
+                                     reinterpret_cast<const float *>(fh), h, nullptr, lg, V, V, h, R, st));
+        ++t->launches;
+    }
+    // log-softmax + top-k children of every row
+    EAGLE_CUDA(launch_row_topk(lg, 0, R, V, V, k, t->at<int32_t>(L.row_ids), t->at<float>(L.row_logp),
+                               t->at<float>(L.row_lse), st));
+    ++t->launches;
+    // expand: pool, next frontier, next level's rows
+    const size_t fstride = static_cast<size_t>(B) * k;
+    ExpandArgs e{};
+    e.level = level;
+    e.B = B;
+    e.k = k;
+    e.n_cand = L.n_cand;
+    e.h = h;
+    e.V = V;
+    e.elem_bytes = L.eb;
+    e.row_ids = t->at<int32_t>(L.row_ids);
+    e.row_logp = t->at<float>(L.row_logp);
+    const int32_t in_buf = (level + 1) % 2, out_buf = level % 2;
+    e.front_cand_in = level == 0 ? nullptr : t->at<int32_t>(L.front_cand) + in_buf * fstride;
+    e.front_S_in = level == 0 ? nullptr : t->at<float>(L.front_S) + in_buf * fstride;
+    const bool more = level < d - 1;
+    e.front_cand_out = more ? t->at<int32_t>(L.front_cand) + out_buf * fstride : nullptr;
+    e.front_S_out = more ? t->at<float>(L.front_S) + out_buf * fstride : nullptr;
+    e.pool_tok = t->at<int32_t>(L.pool_tok);
+    e.pool_S = t->at<float>(L.pool_S);
+    e.pool_parent = t->at<int32_t>(L.pool_par);
+    e.pool_row = t->at<int32_t>(L.pool_row);
+    e.fhat = fh;
+    e.emb = c.embedding;
+    e.x_next = more ? x : nullptr;
+    e.status = t->status;
+    EAGLE_CUDA(launch_expand(e, st));
+    ++t->launches;
+    t->next_level = level + 1;
+    if (more) t->front_current = out_buf;
     return EAGLE_OK;
 }
 
@@ -437,50 +503,70 @@ eagle_status eagle_draft_level(eagle_tree *t, int32_t level, const void *d_root_
                                      h, h, 2 * h, R, st));
         ++t->launches;
     }
-    // LM head: z = W_lm f^
-    float *lg = d_logits_out ? d_logits_out : t->at<float>(L.logits);
-    if (bf16) {
-        EAGLE_CUDA(t->run(t->lm[level], st, d_logits_out, V, 4, 2 * level + 1));
+    return level_tail(t, level, d_logits_out, st);
+}
+
+eagle_status eagle_draft_extend(eagle_tree *t, const void *d_node_features, const int32_t *d_accept_len,
+                               const int32_t *d_accept_nodes, const int32_t *d_accept_tokens,
+                               void *d_next_root_feature, int32_t *d_next_root_token, void *d_path_fhat,
+                               float *d_logits_out, eagle_stream_t stream) {
+    NvtxRange nvtx_range("eagle_draft_extend");
+    if (!t) return EAGLE_ERR_INVALID_ARG;
+    const eagle_tree_config &c = t->cfg;
+    const int32_t B = c.batch, h = c.hidden, d = c.depth;
+    if (B == 0) {
+        t->tree_built = false;
+        t->next_level = 1;
+        return EAGLE_OK;
+    }
+    if (!d_node_features || !d_accept_len || !d_accept_nodes || !d_accept_tokens || !d_next_root_feature ||
+        !d_next_root_token)
+        return EAGLE_ERR_INVALID_ARG;
+    if (!aligned16(d_node_features) || !aligned16(d_next_root_feature) || (d_path_fhat && !aligned16(d_path_fhat)))
+        return EAGLE_ERR_INVALID_ARG;
+    if (d_logits_out && (reinterpret_cast<uintptr_t>(d_logits_out) & 3u) != 0) return EAGLE_ERR_INVALID_ARG;
+    DeviceGuard guard(t->device);
+    if (!guard.ok) return EAGLE_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const Layout &L = t->L;
+    t->tree_built = false;
+    ExtendArgs e{};
+    e.B = B;
+    e.d = d;
+    e.n = L.n_nodes;
+    e.h = h;
+    e.V = c.vocab;
+    e.elem_bytes = L.eb;
+    e.node_feat = d_node_features;
+    e.accept_len = d_accept_len;
+    e.accept_nodes = d_accept_nodes;
+    e.accept_tok = d_accept_tokens;
+    e.emb = c.embedding;
+    e.x = t->ws + L.ext_x;
+    e.next_feat = d_next_root_feature;
+    e.next_tok = d_next_root_token;
+    e.root_tok = t->at<int32_t>(L.root_tok);
+    e.ext_fhat = t->ws + L.ext_fhat;
+    e.fhat0 = t->fhat_level(0);
+    e.path_fhat = d_path_fhat;
+    e.status = t->status;
+    // rows of every verified position, their FC, and level 0's rows out of the last ones
+    EAGLE_CUDA(launch_extend_gather(e, st));
+    ++t->launches;
+    if (c.dtype == EAGLE_BF16) {
+        EAGLE_CUDA(t->run(t->fc_ext, st, nullptr, h, 2, -1));
     } else {
-        EAGLE_CUDA(launch_linear_f32(reinterpret_cast<const float *>(c.lm_head), h,
-                                     reinterpret_cast<const float *>(fh), h, nullptr, lg, V, V, h, R, st));
+        EAGLE_CUDA(launch_linear_f32(reinterpret_cast<const float *>(c.fc_weight), 2 * h,
+                                     reinterpret_cast<const float *>(t->ws + L.ext_x), 2 * h,
+                                     reinterpret_cast<const float *>(c.fc_bias),
+                                     reinterpret_cast<float *>(t->ws + L.ext_fhat), h, h, 2 * h, B * (d + 1), st));
         ++t->launches;
     }
-    // log-softmax + top-k children of every row
-    EAGLE_CUDA(launch_row_topk(lg, 0, R, V, V, k, t->at<int32_t>(L.row_ids), t->at<float>(L.row_logp),
-                               t->at<float>(L.row_lse), st));
+    EAGLE_CUDA(launch_extend_select(e, st));
     ++t->launches;
-    // expand: pool, next frontier, next level's rows
-    const size_t fstride = static_cast<size_t>(B) * k;
-    ExpandArgs e{};
-    e.level = level;
-    e.B = B;
-    e.k = k;
-    e.n_cand = L.n_cand;
-    e.h = h;
-    e.V = V;
-    e.elem_bytes = L.eb;
-    e.row_ids = t->at<int32_t>(L.row_ids);
-    e.row_logp = t->at<float>(L.row_logp);
-    const int32_t in_buf = (level + 1) % 2, out_buf = level % 2;
-    e.front_cand_in = level == 0 ? nullptr : t->at<int32_t>(L.front_cand) + in_buf * fstride;
-    e.front_S_in = level == 0 ? nullptr : t->at<float>(L.front_S) + in_buf * fstride;
-    const bool more = level < d - 1;
-    e.front_cand_out = more ? t->at<int32_t>(L.front_cand) + out_buf * fstride : nullptr;
-    e.front_S_out = more ? t->at<float>(L.front_S) + out_buf * fstride : nullptr;
-    e.pool_tok = t->at<int32_t>(L.pool_tok);
-    e.pool_S = t->at<float>(L.pool_S);
-    e.pool_parent = t->at<int32_t>(L.pool_par);
-    e.pool_row = t->at<int32_t>(L.pool_row);
-    e.fhat = fh;
-    e.emb = c.embedding;
-    e.x_next = more ? x : nullptr;
-    e.status = t->status;
-    EAGLE_CUDA(launch_expand(e, st));
-    ++t->launches;
-    t->next_level = level + 1;
-    if (more) t->front_current = out_buf;
-    return EAGLE_OK;
+    // the rest of level 0 (LM head, top-k, expand): the next round continues at level 1
+    t->next_level = 0;
+    return level_tail(t, 0, d_logits_out, st);
 }
 
 eagle_status eagle_rerank_build_tree(eagle_tree *t, const int32_t *d_pos_base, int32_t *d_tokens,

@@ -169,6 +169,25 @@ struct GatherArgs {
 };
 cudaError_t launch_gather(const GatherArgs &a, cudaStream_t st);
 
+// Draft extend: path rows [F[b][a_j] || E[t_j]] (j = min(i, accept_len[b])) for i <= d, the next
+// round's root (feature, token) and root-token copy; then level 0's f^ rows from the last rows.
+struct ExtendArgs {
+    int32_t B, d, n, h, V, elem_bytes;
+    const void *node_feat;   // [B][n][h]
+    const int32_t *accept_len, *accept_nodes, *accept_tok;  // [B], [B][d+1], [B][d+1]
+    const void *emb;         // [V][h]
+    void *x;                 // [B*(d+1)][2h]
+    void *next_feat;         // [B][h]
+    int32_t *next_tok;       // [B]
+    int32_t *root_tok;       // [B]
+    const void *ext_fhat;    // [B*(d+1)][h]
+    void *fhat0;             // [B][h] level 0's f^
+    void *path_fhat;         // [B][d+1][h] or null
+    int32_t *status;
+};
+cudaError_t launch_extend_gather(const ExtendArgs &a, cudaStream_t st);
+cudaError_t launch_extend_select(const ExtendArgs &a, cudaStream_t st);
+
 // Test hook: a wait on an mbarrier nothing arrives on, bounded by limit_ns; latches the timeout
 // bit in *status.
 cudaError_t launch_bounded_wait(uint64_t limit_ns, int32_t *status, cudaStream_t st);

@@ -11,6 +11,8 @@
 // ranks before its children and the kept set is closed under parents.
 #include <climits>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -337,6 +339,69 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
 }
 
 // ---------------------------------------------------------------------------------------------
+// Draft extend (zdszero "在 SGLang 里"): row r = b (d+1) + i is [F[b][a_j] || E[t_j]] with
+// j = min(i, L_b), a_j / t_j the accepted path's j-th node and the token that follows it
+// (L_b = accept_len[b]).  The row of the last verified position also gives the next round's
+// root: its feature and token, and the root token kept for the tree build.
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) extend_gather_kernel(const ExtendArgs a) {
+    pdl_launch_dependents();  // dependents still wait for this grid to finish
+    pdl_wait();
+    const int32_t r = blockIdx.x, d1 = a.d + 1;
+    const int32_t b = r / d1, i = r - b * d1;
+    int32_t L = a.accept_len[b];
+    if (L < 0 || L > a.d) {
+        if (threadIdx.x == 0 && blockIdx.y == 0 && i == 0) latch(a.status, kDevBounds);
+        L = L < 0 ? 0 : a.d;
+    }
+    const int32_t j = i < L ? i : L;
+    int32_t node = a.accept_nodes[static_cast<int64_t>(b) * d1 + j];
+    int32_t tok = a.accept_tok[static_cast<int64_t>(b) * d1 + j];
+    if (node < 0 || node >= a.n || tok < 0 || tok >= a.V) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) latch(a.status, kDevBounds);
+        node = (node < 0 || node >= a.n) ? 0 : node;
+        tok = (tok < 0 || tok >= a.V) ? 0 : tok;
+    }
+    const int32_t eb = a.elem_bytes;
+    const int32_t vh = (a.h * eb) / 16, vpr = 2 * vh;
+    const uint4 *fsrc = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(a.node_feat) +
+                                                        (static_cast<int64_t>(b) * a.n + node) * a.h * eb);
+    const uint4 *esrc = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(a.emb) +
+                                                        static_cast<int64_t>(tok) * a.h * eb);
+    uint4 *to = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(a.x) + static_cast<int64_t>(r) * 2 * a.h * eb);
+    for (int32_t v = blockIdx.y * blockDim.x + threadIdx.x; v < vpr; v += gridDim.y * blockDim.x)
+        to[v] = (v < vh) ? __ldg(fsrc + v) : __ldg(esrc + (v - vh));
+    if (i == L) {
+        uint4 *nf = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(a.next_feat) + static_cast<int64_t>(b) * a.h * eb);
+        for (int32_t v = blockIdx.y * blockDim.x + threadIdx.x; v < vh; v += gridDim.y * blockDim.x) nf[v] = __ldg(fsrc + v);
+        if (threadIdx.x == 0 && blockIdx.y == 0) {
+            a.next_tok[b] = tok;
+            a.root_tok[b] = tok;
+        }
+    }
+}
+
+// Level 0's f^ row of request b = the extend's row of its last verified position; optionally every
+// path row to the caller.
+__global__ void __launch_bounds__(256) extend_select_kernel(const ExtendArgs a) {
+    pdl_launch_dependents();  // dependents still wait for this grid to finish
+    pdl_wait();
+    const int32_t b = blockIdx.x, d1 = a.d + 1;
+    int32_t L = a.accept_len[b];
+    L = L < 0 ? 0 : (L > a.d ? a.d : L);
+    const int32_t eb = a.elem_bytes, vh = (a.h * eb) / 16;
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.ext_fhat);
+    uint4 *lvl0 = reinterpret_cast<uint4 *>(a.fhat0);
+    for (int32_t v = blockIdx.y * blockDim.x + threadIdx.x; v < vh; v += gridDim.y * blockDim.x)
+        lvl0[static_cast<int64_t>(b) * vh + v] = src[(static_cast<int64_t>(b) * d1 + L) * vh + v];
+    if (a.path_fhat) {
+        uint4 *out = reinterpret_cast<uint4 *>(a.path_fhat);
+        for (int32_t v = blockIdx.y * blockDim.x + threadIdx.x; v < d1 * vh; v += gridDim.y * blockDim.x)
+            out[static_cast<int64_t>(b) * d1 * vh + v] = src[static_cast<int64_t>(b) * d1 * vh + v];
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
 // Test hook: one thread waits, with the bounded wait every device wait of the library uses, on an
 // mbarrier that nothing will ever arrive on; when the limit passes it latches the timeout bit in
 // the status word and returns.  Proves the timeout path without faulting or hanging anything.
@@ -393,6 +458,19 @@ cudaError_t launch_gather(const GatherArgs &a, cudaStream_t st) {
 cudaError_t launch_bounded_wait(uint64_t limit_ns, int32_t *status, cudaStream_t st) {
     bounded_wait_kernel<<<1, 32, 0, st>>>(limit_ns, status);
     return cudaGetLastError();
+}
+
+cudaError_t launch_extend_gather(const ExtendArgs &a, cudaStream_t st) {
+    const int32_t rows = a.B * (a.d + 1);
+    if (rows < 1) return cudaSuccess;
+    const int32_t y = std::max(1, std::min(8, (2 * a.h * a.elem_bytes) / 4096));
+    return launch_pdl(extend_gather_kernel, dim3(rows, y), dim3(256), 0, st, a);
+}
+
+cudaError_t launch_extend_select(const ExtendArgs &a, cudaStream_t st) {
+    if (a.B < 1) return cudaSuccess;
+    const int32_t y = std::max(1, std::min(8, (a.h * a.elem_bytes) / 4096));
+    return launch_pdl(extend_select_kernel, dim3(a.B, y), dim3(256), 0, st, a);
 }
 
 }  // namespace eagle

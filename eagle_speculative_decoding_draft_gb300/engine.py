@@ -167,6 +167,20 @@ class EagleTree:
                              None if logits_out is None else logits_out[level], stream)
         return self.rerank_build_tree(pos_base, tree_out, stream)
 
+    def extend(self, node_features, accept_len, accept_nodes, accept_tokens, path_fhat=None,
+               logits_out=None, stream=None):
+        """Draft extend after a verify: the FC over every verified position of the accepted
+        paths and the next round's level 0 (continue with draft_level(1, ...)).  Returns the next
+        round's root (feature, token)."""
+        B, h = self.batch, self.hidden
+        feat = torch.empty(B, h, dtype=node_features.dtype, device=self.device)
+        tok = torch.empty(B, dtype=torch.int32, device=self.device)
+        check(self.lib.eagle_draft_extend(
+            self._h, _ptr(_need(node_features, "node_features")), _ptr(accept_len),
+            _ptr(accept_nodes), _ptr(accept_tokens), _ptr(feat), _ptr(tok), _ptr(path_fhat),
+            _ptr(logits_out), self._s(stream)), "eagle_draft_extend")
+        return feat, tok
+
     def step(self, root_feature, root_token, target_logits, pos_base=None, tree_out=None,
              verify_out=None, stream=None):
         """One whole draft-tree step on device tensors: draft, rerank/build, greedy verify."""

@@ -134,6 +134,33 @@ EAGLE_API eagle_status eagle_draft_level(eagle_tree *t, int32_t level, const voi
                                          eagle_stream_t stream);
 
 /*
+ * Draft extend and the next round's root (zdszero "在 SGLang 里": after the verify, the draft runs
+ * again over the verified positions with the target's true hidden states and the accepted tokens;
+ * the last verified position starts the next round and its top-k is the next round's first
+ * level.  "EAGLE notes ch. 04" §6.2 and §12 item 3: the accepted path's true features start the
+ * next draft).  Inputs are the verify's outputs and the target's features of every tree node:
+ *   d_node_features [B][m+1][h] (cfg.dtype, 16-byte aligned), d_accept_len [B],
+ *   d_accept_nodes / d_accept_tokens [B][d+1] (as eagle_verify_greedy / eagle_verify_sample).
+ * Row i of request b (i = 0..d) is [F[b][a_j] || E[t_j]], j = min(i, accept_len[b]), a_j the j-th
+ * node of the accepted path and t_j the token after it (the bonus for j = accept_len); every row
+ * goes through the FC.  The last verified row is also the next round's level-0 row: its f^, LM
+ * head, log-softmax + top-k and expand are done here, exactly as eagle_draft_level(t, 0, ...)
+ * would with root feature F[b][a_L] and root token t_L, so the next round continues with
+ * eagle_draft_level(t, 1, ...).
+ *   d_next_root_feature [B][h] (cfg.dtype, 16-byte aligned), d_next_root_token [B]: that root
+ *   d_path_fhat  [B][d+1][h] or NULL: the FC output of every row (the draft features along the
+ *                accepted path; rows past accept_len repeat its row)
+ *   d_logits_out [B][V] fp32 or NULL: the level-0 logits
+ * Errors: INVALID_ARG, CUDA; a path entry outside the tree or the vocabulary latches
+ * EAGLE_ERR_DEVICE_BOUNDS.
+ */
+EAGLE_API eagle_status eagle_draft_extend(eagle_tree *t, const void *d_node_features,
+                                          const int32_t *d_accept_len, const int32_t *d_accept_nodes,
+                                          const int32_t *d_accept_tokens, void *d_next_root_feature,
+                                          int32_t *d_next_root_token, void *d_path_fhat,
+                                          float *d_logits_out, eagle_stream_t stream);
+
+/*
  * Rerank + tree build, after level d-1 ("EAGLE notes ch. 04" §10.3; zdszero "在 SGLang 里";
  * jsqmd "二、EAGLE-2" steps ① ②).  Per request keeps the top-m candidates by (S descending,
  * candidate ascending) and flattens root + kept nodes, in ascending candidate order, to
