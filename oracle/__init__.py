@@ -73,6 +73,8 @@ def lib():
             L.orc_draft_tree.argtypes = [ctypes.POINTER(Dims)] + [P] * 24
             L.orc_verify_greedy.restype = i32
             L.orc_verify_greedy.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
+            L.orc_draft_static.restype = i32
+            L.orc_draft_static.argtypes = [ctypes.POINTER(Dims)] + [P] * 7 + [i32] + [P] * 7
             L.orc_draft_extend.restype = i32
             L.orc_draft_extend.argtypes = [ctypes.POINTER(Dims)] + [P] * 5 + [i32] + [P] * 10
             L.orc_verify_sample.restype = i32
@@ -220,6 +222,33 @@ def draft_tree(w_fc, b_fc, w_lm, emb, root_feat, root_tok, depth: int, topk: int
         _ptr(g("node_z")))
     if rc != ORC_OK:
         raise RuntimeError(f"orc_draft_tree failed with code {rc}")
+    return out
+
+
+def draft_static(w_fc, b_fc, w_lm, emb, root_feat, root_tok, spec, is_bf16: bool, pos_base=None,
+                 node_fhat: bool = False) -> dict:
+    """EAGLE-1 static tree (see orc_draft_static).  spec: [N][2] (parent, rank) for drafted
+    nodes 1..N.  Returns tree_tok / tree_parent / tree_pos / tree_S [B][N+1], tree_mask
+    [B][N+1][W] (uint32) and node_fhat [B][N+1][h] (if asked)."""
+    w1, b1, w2, e = (raw(w_fc, is_bf16), raw(b_fc, is_bf16), raw(w_lm, is_bf16), raw(emb, is_bf16))
+    f = raw(root_feat, is_bf16)
+    rt = np.ascontiguousarray(root_tok, dtype=np.int32)
+    pb = None if pos_base is None else np.ascontiguousarray(pos_base, dtype=np.int32)
+    sp = np.ascontiguousarray(np.asarray(spec, dtype=np.int32).reshape(-1, 2))
+    h, V, B, N = w1.shape[0], w2.shape[0], rt.shape[0], sp.shape[0]
+    n = N + 1
+    W = (n + 31) // 32
+    out = {"tree_tok": np.zeros((B, n), np.int32), "tree_parent": np.zeros((B, n), np.int32),
+           "tree_pos": np.zeros((B, n), np.int32), "tree_mask": np.zeros((B, n, W), np.uint32),
+           "tree_S": np.zeros((B, n), np.float32),
+           "node_fhat": np.zeros((B, n, h), np.float32) if node_fhat else None}
+    dims = Dims(B, h, V, 1, 1, N, int(is_bf16))
+    rc = lib().orc_draft_static(ctypes.byref(dims), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(e), _ptr(f), _ptr(rt),
+                                _ptr(pb), N, _ptr(sp), _ptr(out["tree_tok"]), _ptr(out["tree_parent"]),
+                                _ptr(out["tree_pos"]), _ptr(out["tree_mask"]), _ptr(out["tree_S"]),
+                                _ptr(out["node_fhat"]))
+    if rc != ORC_OK:
+        raise RuntimeError(f"orc_draft_static failed with code {rc}")
     return out
 
 

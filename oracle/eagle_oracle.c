@@ -434,6 +434,121 @@ done:
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* EAGLE-1 static tree                                                                         */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * [notes04] §10.1 and §12 item 7: EAGLE-1 (like Medusa) drafts a tree of fixed shape, the same
+ * for every context - its shape is set by position only; [zdszero] "EAGLE：特征级自回归 + 前移一位
+ * 的 token": inference uses one static draft tree, verified with the ancestor-only mask.  The
+ * pages give no format for the shape; the reading here: drafted node j (1..N) is given as
+ * (parent p_j, rank r_j): the r_j-th most probable token (0-based, ties to the lower id) of the
+ * draft distribution at its parent.  Nodes are listed with parents first and depth
+ * non-decreasing; siblings carry distinct ranks.
+ * For request b: node 0 is the root (root feature, root token).  For every node j that has a child,
+ * its row [feat_in(j) || E[tok_j]] goes through FC -> LM head -> log-softmax + top-K_j (K_j = the
+ * largest rank among its children + 1); child c takes tok_c = ids[r_c], S_c = fl(S_j + logp[r_c])
+ * and feat_in(c) = f^_j (feat_in(root) = the root feature, S_root = 0).
+ * Outputs [B][N+1]: tree_tok, tree_parent (-1 for the root), tree_pos (depth + pos_base),
+ * tree_mask [B][N+1][W] (ancestor-only, LSB first), tree_S.  node_fhat [B][N+1][h] (f^ of the
+ * rows of nodes with children; zero elsewhere) optional.
+ * Pins: a rank-0 chain equals the dynamic tree with topk = 1; a depth-1 star of the top k equals
+ * the dynamic tree with depth 1 and m = k; a full binary tree against its construction in the
+ * test from the row functions.
+ */
+int32_t orc_draft_static(const orc_dims *dm, const void *w_fc, const void *b_fc, const void *w_lm,
+                         const void *emb, const void *root_feat, const int32_t *root_tok,
+                         const int32_t *pos_base, int32_t n_static, const int32_t *spec,
+                         int32_t *tree_tok, int32_t *tree_parent, int32_t *tree_pos,
+                         uint32_t *tree_mask, float *tree_S, float *node_fhat) {
+    const int32_t B = dm->batch, h = dm->hidden, V = dm->vocab, bf = dm->is_bf16;
+    const int32_t n = n_static + 1, W = (n + 31) / 32;
+    if (B < 0 || h < 1 || V < 1 || n_static < 0 || !spec) return ORC_ERR_ARG;
+    int32_t *dep = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+    int32_t *kmax = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+    float *fh = (float *)malloc(sizeof(float) * (size_t)n * (size_t)h);
+    float *feat = (float *)malloc(sizeof(float) * (size_t)h);
+    float *z = (float *)malloc(sizeof(float) * (size_t)V);
+    int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * 16);
+    float *logp = (float *)malloc(sizeof(float) * 16);
+    int32_t rc = ORC_OK;
+    if (!dep || !kmax || !fh || !feat || !z || !ids || !logp) {
+        rc = ORC_ERR_NOMEM;
+        goto done;
+    }
+    /* the shape: depths, and each node's number of top-k entries its children need */
+    dep[0] = 0;
+    for (int32_t j = 0; j < n; ++j) kmax[j] = 0;
+    for (int32_t j = 1; j < n; ++j) {
+        const int32_t p = spec[2 * (j - 1)], r = spec[2 * (j - 1) + 1];
+        if (p < 0 || p >= j || r < 0 || r >= 16 || r >= V) {
+            rc = ORC_ERR_ARG;
+            goto done;
+        }
+        dep[j] = dep[p] + 1;
+        if (dep[j] < dep[j - 1]) { /* depth must not decrease */
+            rc = ORC_ERR_ARG;
+            goto done;
+        }
+        for (int32_t i = 1; i < j; ++i)
+            if (spec[2 * (i - 1)] == p && spec[2 * (i - 1) + 1] == r) { /* sibling with the same rank */
+                rc = ORC_ERR_ARG;
+                goto done;
+            }
+        if (r + 1 > kmax[p]) kmax[p] = r + 1;
+    }
+    for (int32_t b = 0; b < B; ++b) {
+        int32_t *tt = tree_tok + (int64_t)b * n;
+        int32_t *tp = tree_parent + (int64_t)b * n;
+        float *tS = tree_S + (int64_t)b * n;
+        const int32_t pb = pos_base ? pos_base[b] : 0;
+        tt[0] = root_tok[b];
+        tp[0] = -1;
+        tS[0] = 0.0f;
+        for (int32_t j = 1; j < n; ++j) tp[j] = spec[2 * (j - 1)];
+        /* nodes in order: a node's row is evaluated before any of its children is read */
+        for (int32_t j = 0; j < n; ++j) {
+            /* tt[j] and tS[j] were set when its parent's row was evaluated */
+            if (kmax[j] == 0) continue;
+            const float *in;
+            if (j == 0) {
+                for (int32_t i = 0; i < h; ++i) feat[i] = load_elem(root_feat, bf, (int64_t)b * h + i);
+                in = feat;
+            } else {
+                in = fh + (int64_t)tp[j] * h;
+            }
+            if (tt[j] < 0 || tt[j] >= V) {
+                rc = ORC_ERR_ARG;
+                goto done;
+            }
+            orc_fc_row(h, bf, w_fc, b_fc, in, emb, tt[j], fh + (int64_t)j * h);
+            orc_lm_head_row(h, V, bf, w_lm, fh + (int64_t)j * h, z);
+            float lse;
+            orc_log_softmax_topk(V, kmax[j], z, ids, logp, &lse);
+            for (int32_t c = j + 1; c < n; ++c) {
+                if (spec[2 * (c - 1)] != j) continue;
+                const int32_t r = spec[2 * (c - 1) + 1];
+                tt[c] = ids[r];
+                tS[c] = tS[j] + logp[r];
+            }
+        }
+        for (int32_t j = 0; j < n; ++j) {
+            tree_pos[(int64_t)b * n + j] = dep[j] + pb;
+            uint32_t *mrow = tree_mask + ((int64_t)b * n + j) * W;
+            for (int32_t w = 0; w < W; ++w) mrow[w] = 0u;
+            for (int32_t x = j; x >= 0; x = tp[x]) mrow[x / 32] |= 1u << (x % 32);
+            if (node_fhat) {
+                float *o = node_fhat + ((int64_t)b * n + j) * h;
+                for (int32_t i = 0; i < h; ++i) o[i] = kmax[j] ? fh[(int64_t)j * h + i] : 0.0f;
+            }
+        }
+    }
+done:
+    free(dep); free(kmax); free(fh); free(feat); free(z); free(ids); free(logp);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* Draft extend: the next round's root                                                        */
 /* ------------------------------------------------------------------------------------------ */
 
