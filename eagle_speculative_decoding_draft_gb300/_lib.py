@@ -80,6 +80,9 @@ _SIGS = {
     "eagle_tree_launch_count": (c_int64, [c_void_p]),
     "eagle_tree_step_graphed": (c_int32, [c_void_p]),
     "eagle_draft_extend": (c_int, [c_void_p] * 10),
+    "eagle_tree_workspace_bytes_static": (c_size_t, [POINTER(TreeConfig), c_int32, c_void_p]),
+    "eagle_tree_init_static": (c_int, [POINTER(TreeConfig), c_int32, c_void_p, c_void_p, c_size_t,
+                                       POINTER(c_void_p)]),
     "eagle_test_bounded_wait": (c_int, [c_int64, c_void_p, c_void_p]),
     "eagle_linear_workspace_bytes": (c_size_t, [c_int32, c_int32]),
     "eagle_linear_noalloc_scratch_bytes": (c_size_t, []),

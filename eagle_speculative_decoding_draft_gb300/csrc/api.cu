@@ -38,12 +38,70 @@ struct Layout {
     size_t status, counters, partials, x, fhat, logits, row_ids, row_logp, row_lse;
     size_t pool_tok, pool_S, pool_par, pool_row, front_cand, front_S;
     size_t root_tok, node_tok, node_src, g, node_x, node_fhat, ext_x, ext_fhat;
+    // static tree (EAGLE-1) constants per node, and the drafted nodes' scores
+    size_t sp_node, sp_mask, node_S;
     size_t st_feat, st_tok, st_pos, st_tokens, st_parents, st_positions, st_mask, st_acc_len,
         st_acc_nodes, st_acc_tok, st_out_end, st_in_end;
     size_t total;
     size_t partials_bytes, counters_bytes;
     int32_t r_pad, n_cand, n_nodes, mask_words, node_chunk, eb;
+    int32_t kk;  // entries of each row's top-k (topk; for a static tree, its largest rank + 1)
 };
+
+// The shape of an EAGLE-1 static tree ("EAGLE notes ch. 04" §10.1 and §12 item 7: the shape is
+// fixed, set by position only): drafted node j (1..N) is (parent, rank), the rank-th most
+// probable draft token at its parent.  Everything below is derived on the host once.
+struct StaticShape {
+    int32_t N = 0, D = 0, K = 0;  // drafted nodes, depth, top-k entries a row needs
+    // per node (n = N + 1; the root is node 0): parent, rank, depth, index among the nodes of
+    // its depth that have children (-1 if none), and that index of its parent
+    std::vector<int32_t> par, rank, dep, eidx, peidx;
+    std::vector<int32_t> lo, cnt;  // per depth 0..D: first node and node count
+    std::vector<int32_t> E;        // per level 0..D-1: nodes of that depth with children
+    std::vector<uint32_t> mask;    // [n][W] ancestor-only, LSB first
+};
+
+// Validates a (parent, rank) list: parents first, depth non-decreasing, ranks in [0, 16) and
+// below V, distinct ranks among siblings.
+bool make_static_shape(int32_t N, const int32_t *spec, int32_t V, StaticShape *s) {
+    if (N < 1 || N > kMaxCandidates || !spec) return false;
+    const int32_t n = N + 1;
+    s->N = N;
+    s->par.assign(n, -1);
+    s->rank.assign(n, 0);
+    s->dep.assign(n, 0);
+    s->eidx.assign(n, -1);
+    s->peidx.assign(n, -1);
+    std::vector<uint32_t> used(n, 0u);  // ranks taken among each node's children
+    int32_t K = 1;
+    for (int32_t j = 1; j < n; ++j) {
+        const int32_t p = spec[2 * (j - 1)], r = spec[2 * (j - 1) + 1];
+        if (p < 0 || p >= j || r < 0 || r >= kMaxTopk || r >= V) return false;
+        if (used[p] & (1u << r)) return false;
+        used[p] |= 1u << r;
+        s->par[j] = p;
+        s->rank[j] = r;
+        s->dep[j] = s->dep[p] + 1;
+        if (s->dep[j] < s->dep[j - 1]) return false;
+        K = std::max(K, r + 1);
+    }
+    s->K = K;
+    s->D = s->dep[n - 1];
+    if (s->D < 1 || s->D > kMaxDepth) return false;
+    s->lo.assign(s->D + 1, 0);
+    s->cnt.assign(s->D + 1, 0);
+    for (int32_t j = n - 1; j >= 0; --j) s->lo[s->dep[j]] = j;
+    for (int32_t j = 0; j < n; ++j) ++s->cnt[s->dep[j]];
+    s->E.assign(s->D, 0);
+    for (int32_t j = 0; j < n; ++j)
+        if (used[j] != 0u) s->eidx[j] = s->E[s->dep[j]]++;
+    for (int32_t j = 1; j < n; ++j) s->peidx[j] = s->eidx[s->par[j]];
+    const int32_t W = (n + 31) / 32;
+    s->mask.assign(static_cast<size_t>(n) * W, 0u);
+    for (int32_t j = 0; j < n; ++j)
+        for (int32_t x = j; x >= 0; x = s->par[x]) s->mask[static_cast<size_t>(j) * W + x / 32] |= 1u << (x % 32);
+    return true;
+}
 
 bool config_ok(const eagle_tree_config *c) {
     if (!c) return false;
@@ -59,14 +117,31 @@ bool config_ok(const eagle_tree_config *c) {
     return true;
 }
 
-Layout make_layout(const eagle_tree_config *c, int32_t num_sms) {
+// A static tree's configuration: the shape fixes depth and m (cfg.topk is not used).
+bool static_config_ok(const eagle_tree_config *c, const StaticShape &s) {
+    if (!c) return false;
+    if (c->batch < 0 || c->hidden < 1 || c->vocab < 1) return false;
+    if (c->depth != s.D || c->num_keep != s.N) return false;
+    if (c->dtype != EAGLE_F32 && c->dtype != EAGLE_BF16) return false;
+    if (c->dtype == EAGLE_BF16 && c->hidden % 8 != 0) return false;
+    if (c->dtype == EAGLE_F32 && c->hidden % 4 != 0) return false;
+    return s.K <= c->vocab;
+}
+
+Layout make_layout(const eagle_tree_config *c, int32_t num_sms, const StaticShape *ss = nullptr) {
     Layout L{};
-    const int64_t B = c->batch, h = c->hidden, V = c->vocab, d = c->depth, k = c->topk;
+    const int64_t B = c->batch, h = c->hidden, V = c->vocab, d = c->depth;
+    const int64_t k = ss ? ss->K : c->topk;
+    L.kk = static_cast<int32_t>(k);
     L.eb = (c->dtype == EAGLE_BF16) ? 2 : 4;
-    L.n_cand = static_cast<int32_t>(k + (d - 1) * k * k);
+    L.n_cand = ss ? 0 : static_cast<int32_t>(k + (d - 1) * k * k);
     L.n_nodes = c->num_keep + 1;
     L.mask_words = (L.n_nodes + 31) / 32;
-    const int64_t R1 = B * k;
+    int64_t R1 = B * k;
+    if (ss) {
+        R1 = 0;
+        for (int32_t e : ss->E) R1 = std::max<int64_t>(R1, B * e);
+    }
     L.r_pad = round16(static_cast<int32_t>(std::max<int64_t>(1, std::max(R1, B))));
     const int64_t node_rows = B * L.n_nodes;
     L.node_chunk = static_cast<int32_t>(node_rows < kLinearMaxRows ? (node_rows > 0 ? node_rows : 1)
@@ -122,6 +197,9 @@ Layout make_layout(const eagle_tree_config *c, int32_t num_sms) {
     L.node_fhat = take(static_cast<size_t>(L.node_chunk) * h * L.eb);
     L.ext_x = take(static_cast<size_t>(ext_rows) * 2 * h * L.eb);
     L.ext_fhat = take(static_cast<size_t>(ext_rows) * h * L.eb);
+    L.sp_node = take(ss ? static_cast<size_t>(L.n_nodes) * 7 * 4 : 0);
+    L.sp_mask = take(ss ? static_cast<size_t>(L.n_nodes) * L.mask_words * 4 : 0);
+    L.node_S = take(ss ? static_cast<size_t>(node_rows) * 4 : 0);
     L.total = o;
     return L;
 }
@@ -206,6 +284,8 @@ struct eagle_tree {
     int32_t next_level = 0;  // the level eagle_draft_level accepts next (0 is always accepted)
     bool tree_built = false;
     int32_t front_current = 0;
+    bool is_static = false;         // EAGLE-1 static tree (shape below) instead of the dynamic one
+    StaticShape shape;
     std::vector<LinearSeq> fc, lm;  // per level (bf16 only)
     LinearSeq fc_ext;               // the draft extend's FC over B*(d+1) rows (bf16 only)
     int64_t launches = 0;           // kernels launched by this handle
@@ -285,7 +365,10 @@ struct eagle_tree {
     void *fhat_level(int32_t l) const {
         return ws + L.fhat + static_cast<size_t>(l) * L.r_pad * cfg.hidden * L.eb;
     }
-    int32_t rows_of(int32_t level) const { return level == 0 ? cfg.batch : cfg.batch * cfg.topk; }
+    int32_t rows_of(int32_t level) const {
+        if (is_static) return cfg.batch * shape.E[level];
+        return level == 0 ? cfg.batch : cfg.batch * cfg.topk;
+    }
 };
 
 #define EAGLE_CUDA(expr)                             \
@@ -315,11 +398,12 @@ size_t eagle_tree_workspace_bytes(const eagle_tree_config *cfg) {
     return make_layout(cfg, sms).total;
 }
 
-eagle_status eagle_tree_init(const eagle_tree_config *cfg, void *d_ws, size_t ws_bytes, eagle_tree **out) {
-    NvtxRange nvtx_range("eagle_tree_init");
+// Both kinds of handle; `shape` is null for the dynamic tree.
+static eagle_status init_handle(const eagle_tree_config *cfg, const StaticShape *shape, void *d_ws, size_t ws_bytes,
+                                eagle_tree **out) {
     if (!out) return EAGLE_ERR_INVALID_ARG;
     *out = nullptr;
-    if (!config_ok(cfg)) return EAGLE_ERR_INVALID_ARG;
+    if (shape ? !static_config_ok(cfg, *shape) : !config_ok(cfg)) return EAGLE_ERR_INVALID_ARG;
     if (!d_ws || (reinterpret_cast<uintptr_t>(d_ws) % kAlign) != 0) return EAGLE_ERR_INVALID_ARG;
     if (!cfg->fc_weight || !cfg->lm_head || !cfg->embedding) return EAGLE_ERR_INVALID_ARG;
     if (!aligned16(cfg->fc_weight) || !aligned16(cfg->lm_head) || !aligned16(cfg->embedding) ||
@@ -328,13 +412,17 @@ eagle_status eagle_tree_init(const eagle_tree_config *cfg, void *d_ws, size_t ws
     int dev = 0;
     const int32_t sms = current_num_sms(&dev);
     if (sms < 1) return EAGLE_ERR_CUDA;
-    const Layout L = make_layout(cfg, sms);
+    const Layout L = make_layout(cfg, sms, shape);
     if (ws_bytes < L.total) return EAGLE_ERR_INVALID_ARG;
     if (prepare_device() != cudaSuccess) return EAGLE_ERR_CUDA;
 
     eagle_tree *t = new (std::nothrow) eagle_tree();
     if (!t) return EAGLE_ERR_INVALID_ARG;
     t->cfg = *cfg;
+    if (shape) {
+        t->is_static = true;
+        t->shape = *shape;
+    }
     t->device = dev;
     t->num_sms = sms;
     t->L = L;
@@ -349,6 +437,26 @@ eagle_status eagle_tree_init(const eagle_tree_config *cfg, void *d_ws, size_t ws
         return EAGLE_ERR_CUDA;
     }
     const int32_t B = cfg->batch, h = cfg->hidden, V = cfg->vocab, d = cfg->depth;
+    if (shape) {
+        // the shape's per-node constants and mask, once
+        const int32_t n = L.n_nodes;
+        std::vector<int32_t> sp(static_cast<size_t>(kSpFields) * n, 0);
+        for (int32_t j = 0; j < n; ++j) {
+            sp[kSpPar * n + j] = shape->par[j];
+            sp[kSpRank * n + j] = shape->rank[j];
+            sp[kSpDep * n + j] = shape->dep[j];
+            sp[kSpEidx * n + j] = shape->eidx[j];
+            sp[kSpPeidx * n + j] = shape->peidx[j];
+            sp[kSpSrcOff * n + j] = j == 0 ? 0 : (shape->dep[j] - 1) * L.r_pad;
+            sp[kSpEStride * n + j] = j == 0 ? 0 : shape->E[shape->dep[j] - 1];
+        }
+        if (cudaMemcpy(t->ws + L.sp_node, sp.data(), sp.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaMemcpy(t->ws + L.sp_mask, shape->mask.data(), shape->mask.size() * 4, cudaMemcpyHostToDevice) !=
+                cudaSuccess) {
+            delete t;
+            return EAGLE_ERR_CUDA;
+        }
+    }
     if (cfg->dtype == EAGLE_BF16 && B > 0) {
         t->fc.resize(d);
         t->lm.resize(d);
@@ -371,6 +479,28 @@ eagle_status eagle_tree_init(const eagle_tree_config *cfg, void *d_ws, size_t ws
     }
     *out = t;
     return EAGLE_OK;
+}
+
+eagle_status eagle_tree_init(const eagle_tree_config *cfg, void *d_ws, size_t ws_bytes, eagle_tree **out) {
+    NvtxRange nvtx_range("eagle_tree_init");
+    return init_handle(cfg, nullptr, d_ws, ws_bytes, out);
+}
+
+size_t eagle_tree_workspace_bytes_static(const eagle_tree_config *cfg, int32_t num_nodes, const int32_t *h_spec) {
+    StaticShape shape;
+    if (!cfg || !make_static_shape(num_nodes, h_spec, cfg->vocab, &shape) || !static_config_ok(cfg, shape)) return 0;
+    const int32_t sms = current_num_sms(nullptr);
+    if (sms < 1) return 0;
+    return make_layout(cfg, sms, &shape).total;
+}
+
+eagle_status eagle_tree_init_static(const eagle_tree_config *cfg, int32_t num_nodes, const int32_t *h_spec,
+                                    void *d_ws, size_t ws_bytes, eagle_tree **out) {
+    NvtxRange nvtx_range("eagle_tree_init_static");
+    if (out) *out = nullptr;
+    StaticShape shape;
+    if (!cfg || !make_static_shape(num_nodes, h_spec, cfg->vocab, &shape)) return EAGLE_ERR_INVALID_ARG;
+    return init_handle(cfg, &shape, d_ws, ws_bytes, out);
 }
 
 void eagle_tree_destroy(eagle_tree *t) { delete t; }
@@ -423,9 +553,39 @@ static eagle_status level_tail(eagle_tree *t, int32_t level, float *d_logits_out
         ++t->launches;
     }
     // log-softmax + top-k children of every row
-    EAGLE_CUDA(launch_row_topk(lg, 0, R, V, V, k, t->at<int32_t>(L.row_ids), t->at<float>(L.row_logp),
+    EAGLE_CUDA(launch_row_topk(lg, 0, R, V, V, L.kk, t->at<int32_t>(L.row_ids), t->at<float>(L.row_logp),
                                t->at<float>(L.row_lse), st));
     ++t->launches;
+    if (t->is_static) {
+        // the nodes of depth level+1 take their ranked tokens; those with children get their rows
+        const StaticShape &sh = t->shape;
+        const bool more_s = level < d - 1;
+        StaticExpandArgs se{};
+        se.level = level;
+        se.B = B;
+        se.n = L.n_nodes;
+        se.K = L.kk;
+        se.E = sh.E[level];
+        se.E_next = more_s ? sh.E[level + 1] : 0;
+        se.h = h;
+        se.elem_bytes = L.eb;
+        se.lo = sh.lo[level + 1];
+        se.cnt = sh.cnt[level + 1];
+        se.V = V;
+        se.row_ids = t->at<int32_t>(L.row_ids);
+        se.row_logp = t->at<float>(L.row_logp);
+        se.sp = t->at<int32_t>(L.sp_node);
+        se.node_tok = t->at<int32_t>(L.node_tok);
+        se.node_S = t->at<float>(L.node_S);
+        se.fhat = fh;
+        se.emb = c.embedding;
+        se.x_next = more_s ? x : nullptr;
+        se.status = t->status;
+        EAGLE_CUDA(launch_static_expand(se, st));
+        ++t->launches;
+        t->next_level = level + 1;
+        return EAGLE_OK;
+    }
     // expand: pool, next frontier, next level's rows
     const size_t fstride = static_cast<size_t>(B) * k;
     ExpandArgs e{};
@@ -584,6 +744,29 @@ eagle_status eagle_rerank_build_tree(eagle_tree *t, const int32_t *d_pos_base, i
     DeviceGuard guard(t->device);
     if (!guard.ok) return EAGLE_ERR_CUDA;
     const Layout &L = t->L;
+    if (t->is_static) {
+        // the shape is fixed: copy it, with the drafted tokens and scores
+        StaticBuildArgs sb{};
+        sb.B = c.batch;
+        sb.n = L.n_nodes;
+        sb.W = L.mask_words;
+        sb.sp = t->at<int32_t>(L.sp_node);
+        sb.sp_mask = t->at<uint32_t>(L.sp_mask);
+        sb.root_tok = t->at<int32_t>(L.root_tok);
+        sb.pos_base = d_pos_base;
+        sb.node_tok = t->at<int32_t>(L.node_tok);
+        sb.node_S = t->at<float>(L.node_S);
+        sb.node_src = t->at<int32_t>(L.node_src);
+        sb.tokens = d_tokens;
+        sb.parents = d_parents;
+        sb.positions = d_positions;
+        sb.mask = d_mask;
+        sb.logscore = d_logscore;
+        EAGLE_CUDA(launch_static_build(sb, reinterpret_cast<cudaStream_t>(stream)));
+        ++t->launches;
+        t->tree_built = true;
+        return EAGLE_OK;
+    }
     BuildArgs a{};
     a.B = c.batch;
     a.k = c.topk;

@@ -188,6 +188,45 @@ struct ExtendArgs {
 cudaError_t launch_extend_gather(const ExtendArgs &a, cudaStream_t st);
 cudaError_t launch_extend_select(const ExtendArgs &a, cudaStream_t st);
 
+// EAGLE-1 static tree.  sp points at the per-node constants, field f of node j at sp[f * n + j]:
+// 0 parent, 1 rank, 2 depth, 3 index among the nodes of its depth with children (-1: none),
+// 4 that index of its parent, 5 level offset of its parent's row ((depth - 1) * r_pad), 6 rows
+// per request at its parent's level.
+constexpr int kSpPar = 0, kSpRank = 1, kSpDep = 2, kSpEidx = 3, kSpPeidx = 4, kSpSrcOff = 5, kSpEStride = 6;
+constexpr int kSpFields = 7;
+
+// Nodes of depth level+1 (first lo, cnt of them): token = the parent row's top-k id at the node's
+// rank, score = parent's + that logp; a node with children also gets its row of the next level.
+struct StaticExpandArgs {
+    int32_t level, B, n, K, E, E_next, h, elem_bytes, lo, cnt, V;
+    const int32_t *row_ids;  // [B*E][K]
+    const float *row_logp;
+    const int32_t *sp;
+    int32_t *node_tok;       // [B][n]
+    float *node_S;           // [B][n]
+    const void *fhat;        // this level's f^ rows [B*E][h]
+    const void *emb;
+    void *x_next;            // [B*E_next][2h] or null
+    int32_t *status;
+};
+cudaError_t launch_static_expand(const StaticExpandArgs &a, cudaStream_t st);
+
+// The static tree's outputs from the constants and the drafted tokens and scores.
+struct StaticBuildArgs {
+    int32_t B, n, W;
+    const int32_t *sp;
+    const uint32_t *sp_mask;   // [n][W]
+    const int32_t *root_tok;   // [B]
+    const int32_t *pos_base;   // [B] or null
+    int32_t *node_tok;         // [B][n]: drafted tokens in, the root written at 0
+    const float *node_S;       // [B][n]
+    int32_t *node_src;         // [B][n] f^ row feeding each node (node logits)
+    int32_t *tokens, *parents, *positions;
+    uint32_t *mask;
+    float *logscore;           // or null
+};
+cudaError_t launch_static_build(const StaticBuildArgs &a, cudaStream_t st);
+
 // Test hook: a wait on an mbarrier nothing arrives on, bounded by limit_ns; latches the timeout
 // bit in *status.
 cudaError_t launch_bounded_wait(uint64_t limit_ns, int32_t *status, cudaStream_t st);

@@ -402,6 +402,60 @@ __global__ void __launch_bounds__(256) extend_select_kernel(const ExtendArgs a) 
 }
 
 // ---------------------------------------------------------------------------------------------
+// EAGLE-1 static tree ("EAGLE notes ch. 04" §10.1, §12 item 7): block (b, c) handles node
+// lo + c of depth level+1 for request b.
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) static_expand_kernel(const StaticExpandArgs a) {
+    pdl_launch_dependents();  // dependents still wait for this grid to finish
+    pdl_wait();
+    const int32_t b = blockIdx.x, j = a.lo + blockIdx.y, n = a.n;
+    const int32_t p = a.sp[kSpPar * n + j], r = a.sp[kSpRank * n + j];
+    const int32_t row = b * a.E + a.sp[kSpPeidx * n + j];
+    int32_t tok = a.row_ids[static_cast<int64_t>(row) * a.K + r];
+    if (tok < 0 || tok >= a.V) {
+        if (threadIdx.x == 0) latch(a.status, kDevBounds);
+        tok = 0;
+    }
+    if (threadIdx.x == 0) {
+        const float Sp = (a.level == 0) ? 0.0f : a.node_S[static_cast<int64_t>(b) * n + p];
+        a.node_tok[static_cast<int64_t>(b) * n + j] = tok;
+        a.node_S[static_cast<int64_t>(b) * n + j] = Sp + a.row_logp[static_cast<int64_t>(row) * a.K + r];
+    }
+    const int32_t e = a.sp[kSpEidx * n + j];
+    if (a.x_next == nullptr || e < 0) return;
+    const int32_t eb = a.elem_bytes, vh = (a.h * eb) / 16;
+    const uint4 *f = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(a.fhat) +
+                                                     static_cast<int64_t>(row) * a.h * eb);
+    const uint4 *em = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(a.emb) +
+                                                      static_cast<int64_t>(tok) * a.h * eb);
+    uint4 *to = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(a.x_next) +
+                                          static_cast<int64_t>(b * a.E_next + e) * 2 * a.h * eb);
+    for (int32_t v = threadIdx.x; v < 2 * vh; v += blockDim.x) to[v] = (v < vh) ? __ldg(f + v) : __ldg(em + (v - vh));
+}
+
+__global__ void __launch_bounds__(256) static_build_kernel(const StaticBuildArgs a) {
+    pdl_launch_dependents();  // dependents still wait for this grid to finish
+    pdl_wait();
+    const int32_t b = blockIdx.x, n = a.n;
+    const int64_t ob = static_cast<int64_t>(b) * n;
+    const int32_t pos0 = a.pos_base ? a.pos_base[b] : 0;
+    for (int32_t j = threadIdx.x; j < n; j += blockDim.x) {
+        const int32_t tok = (j == 0) ? a.root_tok[b] : a.node_tok[ob + j];
+        a.tokens[ob + j] = tok;
+        a.parents[ob + j] = a.sp[kSpPar * n + j];
+        a.positions[ob + j] = a.sp[kSpDep * n + j] + pos0;
+        if (a.logscore) a.logscore[ob + j] = (j == 0) ? 0.0f : a.node_S[ob + j];
+        for (int32_t w = 0; w < a.W; ++w) a.mask[(ob + j) * a.W + w] = a.sp_mask[static_cast<int64_t>(j) * a.W + w];
+        if (j == 0) {
+            a.node_tok[ob] = tok;
+            a.node_src[ob] = -1 - b;
+        } else {
+            a.node_src[ob + j] = a.sp[kSpSrcOff * n + j] + b * a.sp[kSpEStride * n + j] + a.sp[kSpPeidx * n + j];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
 // Test hook: one thread waits, with the bounded wait every device wait of the library uses, on an
 // mbarrier that nothing will ever arrive on; when the limit passes it latches the timeout bit in
 // the status word and returns.  Proves the timeout path without faulting or hanging anything.
@@ -471,6 +525,16 @@ cudaError_t launch_extend_select(const ExtendArgs &a, cudaStream_t st) {
     if (a.B < 1) return cudaSuccess;
     const int32_t y = std::max(1, std::min(8, (a.h * a.elem_bytes) / 4096));
     return launch_pdl(extend_select_kernel, dim3(a.B, y), dim3(256), 0, st, a);
+}
+
+cudaError_t launch_static_expand(const StaticExpandArgs &a, cudaStream_t st) {
+    if (a.B < 1 || a.cnt < 1) return cudaSuccess;
+    return launch_pdl(static_expand_kernel, dim3(a.B, a.cnt), dim3(128), 0, st, a);
+}
+
+cudaError_t launch_static_build(const StaticBuildArgs &a, cudaStream_t st) {
+    if (a.B < 1) return cudaSuccess;
+    return launch_pdl(static_build_kernel, dim3(a.B), dim3(256), 0, st, a);
 }
 
 }  // namespace eagle

@@ -48,7 +48,11 @@ class EagleTree:
     references).  w_fc [h][2h], b_fc [h] or None, w_lm [V][h], emb [V][h], all bf16 or all fp32.
     """
 
-    def __init__(self, w_fc, b_fc, w_lm, emb, batch: int, depth: int, topk: int, num_keep: int):
+    def __init__(self, w_fc, b_fc, w_lm, emb, batch: int, depth: int, topk: int, num_keep: int,
+                 static_spec=None):
+        """static_spec: None for the dynamic EAGLE-2 tree, or an EAGLE-1 static shape as
+        [(parent, rank), ...] for drafted nodes 1..N (then depth and num_keep must be its depth
+        and N; topk is not used)."""
         self.lib = _lib.load()
         dt = w_fc.dtype
         for name, t in (("w_fc", w_fc), ("w_lm", w_lm), ("emb", emb)):
@@ -67,15 +71,29 @@ class EagleTree:
                                    _dtype_code(dt), w_fc.data_ptr(),
                                    None if b_fc is None else b_fc.data_ptr(), w_lm.data_ptr(),
                                    emb.data_ptr())
+        self.static_spec = None
+        if static_spec is not None:
+            import numpy as np
+            sp = np.ascontiguousarray(np.asarray(static_spec, dtype=np.int32).reshape(-1, 2))
+            self.static_spec = sp
+            spp = sp.ctypes.data_as(ctypes.c_void_p)
         with torch.cuda.device(self.device):
-            nbytes = self.lib.eagle_tree_workspace_bytes(ctypes.byref(self.cfg))
+            if self.static_spec is None:
+                nbytes = self.lib.eagle_tree_workspace_bytes(ctypes.byref(self.cfg))
+            else:
+                nbytes = self.lib.eagle_tree_workspace_bytes_static(ctypes.byref(self.cfg), sp.shape[0], spp)
             if nbytes == 0:
                 raise ValueError("invalid draft-tree configuration")
             self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
             h = ctypes.c_void_p()
-            check(self.lib.eagle_tree_init(ctypes.byref(self.cfg),
-                                           ctypes.c_void_p(self.workspace.data_ptr()), nbytes,
-                                           ctypes.byref(h)), "eagle_tree_init")
+            if self.static_spec is None:
+                check(self.lib.eagle_tree_init(ctypes.byref(self.cfg),
+                                               ctypes.c_void_p(self.workspace.data_ptr()), nbytes,
+                                               ctypes.byref(h)), "eagle_tree_init")
+            else:
+                check(self.lib.eagle_tree_init_static(ctypes.byref(self.cfg), sp.shape[0], spp,
+                                                      ctypes.c_void_p(self.workspace.data_ptr()), nbytes,
+                                                      ctypes.byref(h)), "eagle_tree_init_static")
         self._h = h
         self.layout = _lib.TreeLayout()
         check(self.lib.eagle_tree_get_layout(self._h, ctypes.byref(self.layout)),

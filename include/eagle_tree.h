@@ -114,6 +114,26 @@ EAGLE_API eagle_status eagle_tree_init(const eagle_tree_config *cfg, void *d_wor
                                        size_t workspace_bytes, eagle_tree **out);
 
 /*
+ * EAGLE-1 static tree ("EAGLE notes ch. 04" §10.1 and §12 item 7: EAGLE-1 drafts a tree whose shape
+ * is fixed and set by position only; zdszero "EAGLE": one static draft tree, verified with the
+ * ancestor-only mask).  The shape is h_spec [num_nodes][2] (host memory): drafted node j (1..N)
+ * is (parent, rank), the rank-th most probable draft token (0-based, ties to the lower id) at its
+ * parent; parents come first, depth never decreases, ranks are in [0, 16) and distinct among
+ * siblings.  cfg->depth must be the shape's depth and cfg->num_keep must be N; cfg->topk is not
+ * used.  The handle then works as the dynamic one: eagle_draft_level runs, per level, only the
+ * rows of nodes that have children (row top-k of the largest rank + 1, children take their
+ * ranked tokens, scores add up as in the dynamic tree); eagle_rerank_build_tree outputs the
+ * fixed shape (tokens drafted, parents, depth positions, ancestor mask, scores); verify, node
+ * logits, draft extend and the host step are unchanged.  Init copies the shape's constants into
+ * the workspace (synchronously).  Errors: INVALID_ARG for a malformed shape or mismatching cfg.
+ */
+EAGLE_API size_t eagle_tree_workspace_bytes_static(const eagle_tree_config *cfg, int32_t num_nodes,
+                                                   const int32_t *h_spec);
+EAGLE_API eagle_status eagle_tree_init_static(const eagle_tree_config *cfg, int32_t num_nodes,
+                                              const int32_t *h_spec, void *d_ws, size_t ws_bytes,
+                                              eagle_tree **out);
+
+/*
  * One draft level ("EAGLE notes ch. 04" §6.1 and §10.3; zdszero "EAGLE-2").
  * level 0 starts a new step: its rows are the B roots, row b = [d_root_feature[b] ||
  *   E[d_root_token[b]]] (d_root_feature [B][h] of cfg.dtype, d_root_token [B]); the root's k

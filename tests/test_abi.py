@@ -122,3 +122,25 @@ def test_bounded_wait_hook_rejects_bad_arguments_on_the_host(lib):
     assert lib.eagle_test_bounded_wait(10**11, P(256), None) == 1
     assert lib.eagle_test_bounded_wait(1000, None, None) == 1
 
+
+@pytest.mark.parametrize("spec", [[[1, 0]], [[0, 0], [0, 0]], [[0, 0], [1, 0], [0, 1]], [[0, 16]], []])
+def test_static_init_rejects_malformed_shapes_on_the_host(lib, spec):
+    import numpy as np
+    sp = np.ascontiguousarray(np.asarray(spec, dtype=np.int32).reshape(-1, 2))
+    cfg = _cfg(depth=2, num_keep=max(1, len(spec)))
+    h = ctypes.c_void_p()
+    ptr = sp.ctypes.data_as(ctypes.c_void_p)
+    assert lib.eagle_tree_workspace_bytes_static(ctypes.byref(cfg), len(spec), ptr) == 0
+    assert lib.eagle_tree_init_static(ctypes.byref(cfg), len(spec), ptr, ctypes.c_void_p(4096), 1 << 30,
+                                      ctypes.byref(h)) == 1
+
+
+def test_static_init_checks_depth_and_size_against_the_shape(lib):
+    import numpy as np
+    sp = np.ascontiguousarray(np.array([[0, 0], [0, 1], [1, 0]], dtype=np.int32))
+    ptr = sp.ctypes.data_as(ctypes.c_void_p)
+    h = ctypes.c_void_p()
+    for cfg in (_cfg(depth=3, num_keep=3), _cfg(depth=2, num_keep=4), _cfg(depth=2, num_keep=3, vocab=1)):
+        assert lib.eagle_tree_init_static(ctypes.byref(cfg), 3, ptr, ctypes.c_void_p(4096), 1 << 30,
+                                          ctypes.byref(h)) == 1
+
