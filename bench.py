@@ -96,6 +96,35 @@ def tensor_peak():
         return FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
 
 
+def static_widths(depth: int, topk: int):
+    """Children per depth of the bench's static tree: topk at the root's depth, one fewer per
+    level below, at least 1."""
+    return [max(1, topk - l) for l in range(depth)]
+
+
+def static_shape(depth: int, topk: int):
+    """A static (EAGLE-1-style) tree for the bench: the nodes of each depth (its width) are shared
+    out over the previous depth's nodes, best first: the i-th (0-based) gets about width / 2^(i+1)
+    children (at least 1) until the width is used up, the last one the rest.  Returns (parent,
+    rank) pairs."""
+    spec = []
+    prev = [0]  # nodes of the previous depth, best first
+    for width in static_widths(depth, topk):
+        cur = []
+        budget = width
+        for i, p in enumerate(prev):
+            if budget <= 0:
+                break
+            last = i == len(prev) - 1
+            kids = budget if last else min(budget, max(1, (width + (1 << (i + 1)) - 1) >> (i + 1)))
+            for r in range(kids):
+                spec.append((p, r))
+                cur.append(len(spec))
+            budget -= kids
+        prev = cur
+    return spec
+
+
 def per_level(plist, hbm, tflops):
     """Mean duration, GB/s and TFLOP/s of the timed GEMM launches, by (level, kind)."""
     agg = {}
@@ -470,6 +499,32 @@ def run_eagle(args, w):
     round_ms = r0.elapsed_time(r1) / ROUNDS
     eng.status()
 
+    # ---------------- an EAGLE-1 static tree on the same weights ----------------
+    spec = static_shape(d, w.topk)
+    st_eng = EagleTree(g(inp.w_fc), g(inp.b_fc) if w.bias else None, g(inp.w_lm), g(inp.emb), B,
+                       d, 1, len(spec), static_spec=spec)
+    st_n = len(spec) + 1
+    st_T = [torch.randn(B, st_n, V, generator=fgen, device=dev) for _ in range(2)]
+    st_tree, st_ver = st_eng.new_tree_outputs(), st_eng.new_verify_outputs()
+
+    def static_step(i):
+        feat_i, tok_i, _ = sets[i % N_INPUT_SETS]
+        st_eng.step(feat_i, tok_i, st_T[i % 2], tree_out=st_tree, verify_out=st_ver)
+
+    for i in range(10):
+        static_step(i)
+    torch.cuda.synchronize()
+    s_0, s_1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    S_STEPS = max(100, K // 4)
+    s_0.record()
+    for i in range(S_STEPS):
+        static_step(i)
+    s_1.record()
+    torch.cuda.synchronize()
+    static_ms = s_0.elapsed_time(s_1) / S_STEPS
+    st_eng.status()
+    st_eng.close()
+
     peak, peak_kind = hbm_peak()
     tpeak, tpeak_kind = tensor_peak()
     achieved = gemm_bytes / (gemm_ms * 1e-3) / 1e9 if gemm_ms > 0 else None
@@ -508,6 +563,10 @@ def run_eagle(args, w):
                               "how": "eagle_draft_extend from the previous verify (FC over every "
                                      "verified position + the next tree's level 0), levels 1..d-1, "
                                      "rerank/build, greedy verify; CUDA events, eager launches"},
+        "static_tree": {"value": 1e3 / static_ms, "unit": "steps/s", "ms_per_step": static_ms,
+                        "drafted_nodes": len(spec), "depth": d, "shape": "widths " + str(static_widths(d, w.topk)),
+                        "how": "eagle_tree_init_static handle on the same weights: levels, build, greedy "
+                               "verify against N(0,1) target logits; CUDA events, eager launches"},
         "sampling_verify": {"us_per_call": sample_us, "mean_accept_len": sample_accept,
                             "temperature": 1.0, "mode": "recursive rejection sampling",
                             "how": "eagle_verify_sample on the step's tree; q = draft logits of "
