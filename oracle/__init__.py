@@ -45,6 +45,13 @@ class Dims(ctypes.Structure):
                 ("is_bf16", ctypes.c_int32)]
 
 
+class LayerDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("nodes", ctypes.c_int32), ("prefix", ctypes.c_int32),
+                ("hidden", ctypes.c_int32), ("heads", ctypes.c_int32), ("kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("inter", ctypes.c_int32), ("rope_theta", ctypes.c_float),
+                ("rms_eps", ctypes.c_float)]
+
+
 def lib():
     global _lib
     with _lock:
@@ -73,6 +80,8 @@ def lib():
             L.orc_draft_tree.argtypes = [ctypes.POINTER(Dims)] + [P] * 24
             L.orc_verify_greedy.restype = i32
             L.orc_verify_greedy.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
+            L.orc_decoder_layer.restype = i32
+            L.orc_decoder_layer.argtypes = [ctypes.POINTER(LayerDims)] + [P] * 13
             L.orc_draft_static.restype = i32
             L.orc_draft_static.argtypes = [ctypes.POINTER(Dims)] + [P] * 7 + [i32] + [P] * 7
             L.orc_draft_extend.restype = i32
@@ -223,6 +232,38 @@ def draft_tree(w_fc, b_fc, w_lm, emb, root_feat, root_tok, depth: int, topk: int
     if rc != ORC_OK:
         raise RuntimeError(f"orc_draft_tree failed with code {rc}")
     return out
+
+
+def decoder_layer(x, w_qkv, w_o, w_norm, w_gu, w_d, k_cache, v_cache, pos, mask, heads: int,
+                  kv_heads: int, rope_theta: float = 10000.0, rms_eps: float = 1e-6,
+                  new_kv: bool = False) -> dict:
+    """One draft decoder layer over each request's tree (see orc_decoder_layer).  Tensors are bf16
+    (torch) except pos [B][n] int32 and mask [B][n][W] (int32/uint32).  x [B][n][h], k_cache /
+    v_cache [B][P][Hkv][D].  Returns out [B][n][h] as float32 (bf16 values) and, if new_kv, the
+    tree's rotated keys and values [B][n][Hkv][D]."""
+    X = raw(x, True)
+    B, n, h = X.shape
+    KC = raw(k_cache, True)
+    P, D = KC.shape[1], KC.shape[3]
+    wgu = raw(w_gu, True)
+    I = wgu.shape[0] // 2
+    dims = LayerDims(B, n, P, h, heads, kv_heads, D, I, rope_theta, rms_eps)
+    out = np.zeros((B, n, h), np.uint16)
+    kn = np.zeros((B, n, kv_heads, D), np.uint16) if new_kv else None
+    vn = np.zeros((B, n, kv_heads, D), np.uint16) if new_kv else None
+    pz = np.ascontiguousarray(pos, dtype=np.int32)
+    mz = np.ascontiguousarray(np.asarray(mask).view(np.uint32) if np.asarray(mask).dtype == np.int32
+                              else np.asarray(mask, dtype=np.uint32))
+    rc = lib().orc_decoder_layer(ctypes.byref(dims), _ptr(X), _ptr(raw(w_qkv, True)), _ptr(raw(w_o, True)),
+                                 _ptr(raw(w_norm, True)), _ptr(wgu), _ptr(raw(w_d, True)), _ptr(KC),
+                                 _ptr(raw(v_cache, True)), _ptr(pz), _ptr(mz), _ptr(out), _ptr(kn), _ptr(vn))
+    if rc != ORC_OK:
+        raise RuntimeError(f"orc_decoder_layer failed with code {rc}")
+    f = lambda a: (a.astype(np.uint32) << 16).view(np.float32)
+    res = {"out": f(out)}
+    if new_kv:
+        res["k_new"], res["v_new"] = f(kn), f(vn)
+    return res
 
 
 def draft_static(w_fc, b_fc, w_lm, emb, root_feat, root_tok, spec, is_bf16: bool, pos_base=None,

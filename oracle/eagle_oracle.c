@@ -434,6 +434,178 @@ done:
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* Draft decoder layer with tree attention over a draft KV cache                              */
+/* ------------------------------------------------------------------------------------------ */
+
+typedef struct {
+    int32_t batch;     /* B */
+    int32_t nodes;     /* n: tree nodes (root first, parents before children) */
+    int32_t prefix;    /* P: cached positions before the tree */
+    int32_t hidden;    /* h */
+    int32_t heads;     /* H query heads */
+    int32_t kv_heads;  /* Hkv, divides H */
+    int32_t head_dim;  /* D, even */
+    int32_t inter;     /* I: MLP width */
+    float rope_theta;  /* RoPE base */
+    float rms_eps;     /* RMSNorm epsilon */
+} orc_layer_dims;
+
+static float bf16r(float x) { return orc_bf16_to_f32(orc_f32_to_bf16(x)); }
+
+/* y[o] = sum_i W[o][i] x[i], fp32, ascending i; W bf16 [out][in]. */
+static void orc_matvec_bf16(const uint16_t *W, int32_t out, int32_t in, const float *x, float *y) {
+#pragma omp parallel for schedule(static)
+    for (int32_t o = 0; o < out; ++o) {
+        float acc = 0.0f;
+        for (int32_t i = 0; i < in; ++i) acc = acc + orc_bf16_to_f32(W[(int64_t)o * in + i]) * x[i];
+        y[o] = acc;
+    }
+}
+
+/* Llama's rotary embedding ("rotate half"): for j < D/2, angle = pos * theta^(-2j/D), and the
+ * pair (x[j], x[j + D/2]) is rotated by it.  Angles, sines and cosines in double precision. */
+static void orc_rope(float *x, int32_t D, int32_t pos, double theta) {
+    const int32_t half = D / 2;
+    for (int32_t j = 0; j < half; ++j) {
+        const double ang = (double)pos * pow(theta, -2.0 * j / (double)D);
+        const double c = cos(ang), sn = sin(ang);
+        const double a = x[j], b = x[j + half];
+        x[j] = (float)(a * c - b * sn);
+        x[j + half] = (float)(b * c + a * sn);
+    }
+}
+
+/*
+ * [zdszero] "在 SGLang 里" (the draft model: embedding, fc = Linear(2h, h, bias), one Llama decoder
+ * layer whose first input_layernorm is the identity, no final norm, the target's lm_head) and
+ * [notes04] §4.1 (FC, then a light decoder layer predicts the next feature) and §12.5 (tree
+ * attention: each node sees its ancestors only; positions shared per depth).  One decoder layer over
+ * the n nodes of each request's tree; each node attends to the P cached positions (keys stored
+ * already rotated) and to the tree nodes its mask row marks (itself and its ancestors).  Rounding
+ * points (a bf16 model): each projection's output, the attention output, each residual sum, the
+ * normed activation and the MLP product are rounded to bf16; dot products, softmax and norms are fp32.
+ *   x_i   -> qkv = Wqkv x_i (rows: H*D q, Hkv*D k, Hkv*D v), q and k rotated at pos[i]
+ *   attn  -> for head hq (kv head hq / (H / Hkv)): s_j = q.k_j / sqrt(D) over visible keys,
+ *            p = softmax(s), o = sum p_j v_j
+ *   h1    =  x_i + Wo o
+ *   r     =  RMSNorm(h1) * w_norm      (post-attention norm; the input norm is the identity)
+ *   a     =  silu(g) * u,  [g; u] = Wgu r
+ *   out_i =  h1 + Wd a
+ * Inputs (bf16 as uint16): x [B][n][h], Wqkv [(H+2Hkv)D][h], Wo [h][H D], w_norm [h], Wgu [2I][h],
+ * Wd [h][I], k_cache / v_cache [B][P][Hkv][D], pos [B][n], mask [B][n][W] (bit t of row i: node t
+ * visible to node i).  Outputs: out [B][n][h] (bf16 bits), and optionally the tree's rotated keys
+ * and values k_new / v_new [B][n][Hkv][D] (bf16 bits), which extend the cache.
+ * Pins: attention over a chain with no prefix against float64 causal attention; RoPE's relative
+ * position property; the whole layer against a float64 restatement within bf16 tolerances.
+ */
+int32_t orc_decoder_layer(const orc_layer_dims *L, const uint16_t *x, const uint16_t *Wqkv,
+                          const uint16_t *Wo, const uint16_t *w_norm, const uint16_t *Wgu,
+                          const uint16_t *Wd, const uint16_t *k_cache, const uint16_t *v_cache,
+                          const int32_t *pos, const uint32_t *mask, uint16_t *out,
+                          uint16_t *k_new, uint16_t *v_new) {
+    const int32_t B = L->batch, n = L->nodes, P = L->prefix, h = L->hidden, H = L->heads;
+    const int32_t Hk = L->kv_heads, D = L->head_dim, I = L->inter, W = (n + 31) / 32;
+    if (B < 0 || n < 1 || P < 0 || h < 1 || H < 1 || Hk < 1 || H % Hk || D < 2 || D % 2 || I < 1)
+        return ORC_ERR_ARG;
+    const int32_t nq = H * D, nk = Hk * D, nqkv = nq + 2 * nk, grp = H / Hk;
+    float *xin = (float *)malloc(sizeof(float) * (size_t)h);
+    float *qkv = (float *)malloc(sizeof(float) * (size_t)n * nqkv);  /* one request's tree */
+    float *o = (float *)malloc(sizeof(float) * (size_t)nq);
+    float *t = (float *)malloc(sizeof(float) * (size_t)(h > 2 * I ? h : 2 * I));
+    float *h1 = (float *)malloc(sizeof(float) * (size_t)h);
+    float *r = (float *)malloc(sizeof(float) * (size_t)h);
+    float *a = (float *)malloc(sizeof(float) * (size_t)I);
+    float *sc = (float *)malloc(sizeof(float) * (size_t)(P + n));
+    int32_t rc = ORC_OK;
+    if (!xin || !qkv || !o || !t || !h1 || !r || !a || !sc) {
+        rc = ORC_ERR_NOMEM;
+        goto done;
+    }
+    const float inv_sqrt_d = 1.0f / sqrtf((float)D);
+    for (int32_t b = 0; b < B; ++b) {
+        /* projections and rotations of every node of this tree */
+        for (int32_t i = 0; i < n; ++i) {
+            const uint16_t *xr = x + ((int64_t)b * n + i) * h;
+            for (int32_t e = 0; e < h; ++e) xin[e] = orc_bf16_to_f32(xr[e]);
+            float *q = qkv + (int64_t)i * nqkv;
+            orc_matvec_bf16(Wqkv, nqkv, h, xin, q);
+            for (int32_t e = 0; e < nqkv; ++e) q[e] = bf16r(q[e]);
+            const int32_t p = pos[(int64_t)b * n + i];
+            for (int32_t hh = 0; hh < H; ++hh) orc_rope(q + hh * D, D, p, L->rope_theta);
+            for (int32_t hh = 0; hh < Hk; ++hh) orc_rope(q + nq + hh * D, D, p, L->rope_theta);
+            for (int32_t e = 0; e < nq + nk; ++e) q[e] = bf16r(q[e]);
+            if (k_new && v_new)
+                for (int32_t e = 0; e < nk; ++e) {
+                    k_new[((int64_t)b * n + i) * nk + e] = orc_f32_to_bf16(q[nq + e]);
+                    v_new[((int64_t)b * n + i) * nk + e] = orc_f32_to_bf16(q[nq + nk + e]);
+                }
+        }
+        for (int32_t i = 0; i < n; ++i) {
+            const float *q = qkv + (int64_t)i * nqkv;
+            const uint32_t *mrow = mask + ((int64_t)b * n + i) * W;
+            for (int32_t hq = 0; hq < H; ++hq) {
+                const int32_t hk = hq / grp;
+                /* scores over the visible keys: the cache, then the marked tree nodes */
+                float mx = -HUGE_VALF;
+                int32_t cnt = 0;
+                for (int32_t j = 0; j < P; ++j) {
+                    const uint16_t *kr = k_cache + (((int64_t)b * P + j) * Hk + hk) * D;
+                    float s = 0.0f;
+                    for (int32_t e = 0; e < D; ++e) s = s + q[hq * D + e] * orc_bf16_to_f32(kr[e]);
+                    sc[cnt++] = s * inv_sqrt_d;
+                }
+                for (int32_t tn = 0; tn < n; ++tn) {
+                    if (!((mrow[tn / 32] >> (tn % 32)) & 1u)) continue;
+                    const float *kr = qkv + (int64_t)tn * nqkv + nq + hk * D;
+                    float s = 0.0f;
+                    for (int32_t e = 0; e < D; ++e) s = s + q[hq * D + e] * kr[e];
+                    sc[cnt++] = s * inv_sqrt_d;
+                }
+                for (int32_t j = 0; j < cnt; ++j)
+                    if (sc[j] > mx) mx = sc[j];
+                float den = 0.0f;
+                for (int32_t j = 0; j < cnt; ++j) {
+                    sc[j] = expf(sc[j] - mx);
+                    den = den + sc[j];
+                }
+                for (int32_t e = 0; e < D; ++e) {
+                    float acc = 0.0f;
+                    int32_t c = 0;
+                    for (int32_t j = 0; j < P; ++j, ++c)
+                        acc = acc + sc[c] * orc_bf16_to_f32(v_cache[(((int64_t)b * P + j) * Hk + hk) * D + e]);
+                    for (int32_t tn = 0; tn < n; ++tn) {
+                        if (!((mrow[tn / 32] >> (tn % 32)) & 1u)) continue;
+                        acc = acc + sc[c++] * qkv[(int64_t)tn * nqkv + nq + nk + hk * D + e];
+                    }
+                    o[hq * D + e] = bf16r(acc / den);
+                }
+            }
+            /* output projection and residual */
+            const uint16_t *xr = x + ((int64_t)b * n + i) * h;
+            orc_matvec_bf16(Wo, h, nq, o, t);
+            for (int32_t e = 0; e < h; ++e) h1[e] = bf16r(orc_bf16_to_f32(xr[e]) + t[e]);
+            /* post-attention RMSNorm */
+            float ss = 0.0f;
+            for (int32_t e = 0; e < h; ++e) ss = ss + h1[e] * h1[e];
+            const float inv = 1.0f / sqrtf(ss / (float)h + L->rms_eps);
+            for (int32_t e = 0; e < h; ++e) r[e] = bf16r(h1[e] * inv * orc_bf16_to_f32(w_norm[e]));
+            /* SwiGLU MLP and residual */
+            orc_matvec_bf16(Wgu, 2 * I, h, r, t);
+            for (int32_t e = 0; e < I; ++e) {
+                const float g = bf16r(t[e]), u = bf16r(t[I + e]);
+                a[e] = bf16r(g / (1.0f + expf(-g)) * u);
+            }
+            orc_matvec_bf16(Wd, h, I, a, t);
+            uint16_t *orow = out + ((int64_t)b * n + i) * h;
+            for (int32_t e = 0; e < h; ++e) orow[e] = orc_f32_to_bf16(h1[e] + t[e]);
+        }
+    }
+done:
+    free(xin); free(qkv); free(o); free(t); free(h1); free(r); free(a); free(sc);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* EAGLE-1 static tree                                                                         */
 /* ------------------------------------------------------------------------------------------ */
 
