@@ -265,6 +265,67 @@ def cpu_baseline(w, inp, budget_s):
                       f"{r} of {w.batch} request(s), {el:.1f} s wall; value scaled to whole steps"}
 
 
+def layer_dims(w):
+    """(heads, kv_heads, head_dim, inter) of the target model's decoder layer that the draft layer
+    copies, by workload shape; None for the fp32 toy (the layer is bf16 only)."""
+    if not w.is_bf16:
+        return None
+    if w.hidden == 8192:
+        return 64, 8, 128, 28672      # Llama-2-70B
+    if w.vocab >= 128000:
+        return 32, 8, 128, 14336      # Llama-3-8B
+    return 32, 32, 128, 11008         # Llama-2-7B / Vicuna-7B
+
+
+DECODER_PREFIX = 1024  # cached tokens per request in front of the tree
+
+
+def decoder_layer_figure(w, dev, tree_out, rank, calls=200):
+    """The draft decoder layer over the step's tree: every node of every request, its mask and
+    depth positions from the tree build, a DECODER_PREFIX-token KV cache per request.  Synthetic
+    bf16 weights N(0, 1/sqrt(fan-in)), inputs and caches N(0, 1).  CUDA events over `calls` calls
+    (weights and caches exceed L2, so every call reads them from HBM)."""
+    import torch
+    from eagle_speculative_decoding_draft_gb300.engine import DecoderLayer
+    dims = layer_dims(w)
+    if dims is None:
+        return None
+    H, Hk, D, I = dims
+    h, B, n, P = w.hidden, w.batch, w.num_nodes, DECODER_PREFIX
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242 + rank)
+    bf = lambda *shape, s=1.0: (torch.randn(*shape, generator=gen, device=dev) * s).to(torch.bfloat16)
+    lay = DecoderLayer(bf((H + 2 * Hk) * D, h, s=h ** -0.5), bf(h, H * D, s=(H * D) ** -0.5),
+                       (1 + 0.1 * torch.randn(h, generator=gen, device=dev)).to(torch.bfloat16),
+                       bf(2 * I, h, s=h ** -0.5), bf(h, I, s=I ** -0.5), H, Hk)
+    x = bf(B, n, h)
+    kc, vc = bf(B, P, Hk, D), bf(B, P, Hk, D)
+    pos = (tree_out["positions"] + P).contiguous()
+    mask = tree_out["mask"].contiguous()
+    out = torch.empty_like(x)
+    for _ in range(5):
+        lay(x, kc, vc, pos, mask, out=out, new_kv=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(calls):
+        lay(x, kc, vc, pos, mask, out=out, new_kv=True)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / calls
+    rows = B * n
+    weight_bytes = 2 * h * ((H + 2 * Hk) * D + H * D + 3 * I)
+    cache_bytes = 2 * 2 * B * P * Hk * D
+    io_bytes = 2 * 2 * rows * h + 2 * 2 * rows * Hk * D + 4 * rows + 4 * rows * mask.shape[-1]
+    total = weight_bytes + cache_bytes + io_bytes
+    return {"us_per_call": us, "achieved_gbs": total / (us * 1e-6) / 1e9,
+            "algorithmic_bytes_per_call": total, "rows": rows, "prefix": P,
+            "layer": {"heads": H, "kv_heads": Hk, "head_dim": D, "inter": I},
+            "how": "eagle_decoder_layer over the step's tree (mask and positions from the build), "
+                   f"new keys/values written; CUDA events, {calls} calls; bytes = weights + KV cache "
+                   "+ layer input/output + new keys/values + positions/mask"}
+
+
 def workload_config(w):
     mb = (2 * w.hidden * w.hidden + w.vocab * w.hidden) * (2 if w.is_bf16 else 4) / 1e6
     l2 = (f"inputs larger than L2: each level streams {mb:.0f} MB of weights (L2 is 129 MB); "
@@ -525,8 +586,14 @@ def run_eagle(args, w):
     st_eng.status()
     st_eng.close()
 
+    # ---------------- the draft decoder layer over the step's tree ----------------
+    eng.step(feat0, tok0, T0, tree_out=tree_out, verify_out=ver_out)
+    dec_fig = decoder_layer_figure(w, dev, tree_out, rank)
+
     peak, peak_kind = hbm_peak()
     tpeak, tpeak_kind = tensor_peak()
+    if dec_fig is not None:
+        dec_fig["frac_of_hbm"] = dec_fig["achieved_gbs"] / peak
     achieved = gemm_bytes / (gemm_ms * 1e-3) / 1e9 if gemm_ms > 0 else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
@@ -572,6 +639,7 @@ def run_eagle(args, w):
                             "how": "eagle_verify_sample on the step's tree; q = draft logits of "
                                    "every node, p = the synthetic target; CUDA events, "
                                    f"{S_CALLS} calls"},
+        "draft_decoder_layer": dec_fig,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)

@@ -46,6 +46,12 @@ class TreeLayout(ctypes.Structure):
                                        "front_current", "num_sms")]
 
 
+class DecoderLayerWeights(ctypes.Structure):
+    _fields_ = [(n, c_int32) for n in ("hidden", "heads", "kv_heads", "head_dim", "inter")] + \
+               [("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float)] + \
+               [(n, c_void_p) for n in ("w_qkv", "w_o", "w_norm", "w_gu", "w_d")]
+
+
 _SIGS = {
     "eagle_tree_workspace_bytes": (c_size_t, [POINTER(TreeConfig)]),
     "eagle_tree_init": (c_int, [POINTER(TreeConfig), c_void_p, c_size_t, POINTER(c_void_p)]),
@@ -85,6 +91,9 @@ _SIGS = {
                                        POINTER(c_void_p)]),
     "eagle_test_bounded_wait": (c_int, [c_int64, c_void_p, c_void_p]),
     "eagle_linear_workspace_bytes": (c_size_t, [c_int32, c_int32]),
+    "eagle_decoder_layer_workspace_bytes": (c_size_t, [POINTER(DecoderLayerWeights), c_int32, c_int32]),
+    "eagle_decoder_layer": (c_int, [POINTER(DecoderLayerWeights), c_int32, c_int32, c_int32]
+                            + [c_void_p] * 9 + [c_size_t, c_void_p]),
     "eagle_linear_noalloc_scratch_bytes": (c_size_t, []),
     "eagle_linear_bf16_noalloc": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int32,
                                           c_int32, c_int32, c_void_p, c_int64, c_int32, c_void_p]),

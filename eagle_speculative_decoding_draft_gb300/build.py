@@ -16,7 +16,7 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 OUT_DIR = PKG / "lib"
 LIB = OUT_DIR / "libeagle_tree.so"
-SOURCES = ["api.cu", "gemm.cu", "topk.cu", "tree.cu", "sample.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "gemm.cu", "topk.cu", "tree.cu", "sample.cu", "noalloc.cu", "decoder.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

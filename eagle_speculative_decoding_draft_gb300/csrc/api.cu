@@ -8,7 +8,6 @@
 #include <new>
 #include <vector>
 
-#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/eagle_tree.h"
 #include "common.cuh"
@@ -25,13 +24,6 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // NVTX range over one C-ABI call (host side only; free when no tool is attached).
-struct NvtxRange {
-    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
-    ~NvtxRange() { nvtxRangePop(); }
-    NvtxRange(const NvtxRange &) = delete;
-    NvtxRange &operator=(const NvtxRange &) = delete;
-};
-
 int32_t round16(int32_t x) { return (x + 15) / 16 * 16; }
 
 struct Layout {

@@ -6,8 +6,17 @@
 #include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 namespace eagle {
+
+// Names the calls of one entry point for profilers (NVTX push/pop around the enqueue).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 // Launches `kernel` allowing programmatic dependent launch: it may start while the previous
 // kernel in the stream is still running.  Every kernel of this library calls griddepcontrol.wait

@@ -404,3 +404,69 @@ def linear_bf16(w, x, bias=None, out_bf16=False, stream=None):
                                 _ptr(y), y.stride(0), int(out_bf16), _ptr(ws), nbytes,
                                 _stream(dev, stream)), "eagle_linear_bf16")
     return y
+
+
+class DecoderLayer:
+    """The draft decoder layer (eagle_decoder_layer): one Llama layer over each request's tree
+    nodes with tree attention over a KV cache.  Weights are bf16 CUDA tensors: w_qkv
+    [(H + 2 Hkv) D][h], w_o [h][H D], w_norm [h], w_gu [2 I][h], w_d [h][I].  The scratch is
+    allocated (zero-filled) on first use and grown as needed."""
+
+    def __init__(self, w_qkv, w_o, w_norm, w_gu, w_d, heads: int, kv_heads: int,
+                 rope_theta: float = 10000.0, rms_eps: float = 1e-6):
+        self._lib = _lib.load()
+        for t, name in ((w_qkv, "w_qkv"), (w_o, "w_o"), (w_norm, "w_norm"), (w_gu, "w_gu"), (w_d, "w_d")):
+            _need(t, name, torch.bfloat16)
+        h = w_norm.shape[0]
+        D = w_qkv.shape[0] // (heads + 2 * kv_heads)
+        inter = w_gu.shape[0] // 2
+        if w_qkv.shape != (D * (heads + 2 * kv_heads), h) or w_o.shape != (h, heads * D) \
+                or w_gu.shape != (2 * inter, h) or w_d.shape != (h, inter):
+            raise ValueError("decoder layer weight shapes do not agree")
+        self._keep = (w_qkv, w_o, w_norm, w_gu, w_d)
+        self.w = _lib.DecoderLayerWeights(h, heads, kv_heads, D, inter, rope_theta, rms_eps,
+                                          w_qkv.data_ptr(), w_o.data_ptr(), w_norm.data_ptr(),
+                                          w_gu.data_ptr(), w_d.data_ptr())
+        self.hidden, self.heads, self.kv_heads, self.head_dim, self.inter = h, heads, kv_heads, D, inter
+        self.device = w_qkv.device
+        self._ws = None
+
+    def workspace(self, batch: int, nodes: int):
+        nbytes = self._lib.eagle_decoder_layer_workspace_bytes(ctypes.byref(self.w), batch, nodes)
+        if nbytes == 0:
+            raise ValueError(f"unusable decoder layer sizes (batch={batch}, nodes={nodes})")
+        if self._ws is None or self._ws.numel() < nbytes:
+            self._ws = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+        return self._ws, nbytes
+
+    def __call__(self, x, k_cache, v_cache, positions, mask, out=None, new_kv: bool = False, stream=None):
+        """x [B][n][h] bf16, k_cache / v_cache [B][P][Hkv][D] bf16 (rotated keys), positions
+        [B][n] int32, mask [B][n][ceil(n/32)] int32 ancestor bits.  Returns out [B][n][h] bf16
+        (and k_new, v_new [B][n][Hkv][D] if new_kv)."""
+        _need(x, "x", torch.bfloat16)
+        B, n, h = x.shape
+        if h != self.hidden:
+            raise ValueError("x hidden size does not match the weights")
+        P = 0 if k_cache is None else k_cache.shape[1]
+        if P:
+            _need(k_cache, "k_cache", torch.bfloat16)
+            _need(v_cache, "v_cache", torch.bfloat16)
+            if k_cache.shape != (B, P, self.kv_heads, self.head_dim) or v_cache.shape != k_cache.shape:
+                raise ValueError("cache shape does not match")
+        _need(positions, "positions", torch.int32)
+        _need(mask, "mask", torch.int32)
+        if positions.shape != (B, n) or mask.shape != (B, n, (n + 31) // 32):
+            raise ValueError("positions / mask shape does not match")
+        if out is None:
+            out = torch.empty_like(x)
+        kn = vn = None
+        if new_kv:
+            kn = torch.empty(B, n, self.kv_heads, self.head_dim, dtype=torch.bfloat16, device=x.device)
+            vn = torch.empty_like(kn)
+        ws, nbytes = self.workspace(max(B, 1), n)
+        check(self._lib.eagle_decoder_layer(ctypes.byref(self.w), B, n, P, _ptr(x),
+                                            _ptr(k_cache) if P else None, _ptr(v_cache) if P else None,
+                                            _ptr(positions), _ptr(mask), _ptr(out), _ptr(kn), _ptr(vn),
+                                            _ptr(ws), nbytes, _stream(x.device, stream)),
+              "eagle_decoder_layer")
+        return (out, kn, vn) if new_kv else out

@@ -441,6 +441,64 @@ EAGLE_API eagle_status eagle_linear_bf16(const void *d_w, int64_t ldw, const voi
                                          size_t ws_bytes, eagle_stream_t stream);
 
 /*
+ * The draft decoder layer.  zdszero, "在 SGLang 里": after the FC, the draft model runs one Llama
+ * decoder layer (its first input_layernorm is the identity; no final norm) and hands its output
+ * to the target's LM head.  EAGLE notes ch. 04 §4.1 (the light decoder layer predicts the next
+ * feature) and §12.5 (tree attention: each node sees the cached context and its own ancestors).
+ * One call runs the layer over the `nodes` tree nodes of each of `batch` requests:
+ *   qkv_i = Wqkv x_i (q: heads*head_dim rows, k and v: kv_heads*head_dim rows each);
+ *   q_i, k_i rotated by Llama rotate-half RoPE at positions[b][i] (pair (j, j + D/2) turned by
+ *   positions * rope_theta^(-2j/D));
+ *   o_i = softmax_j(q_i . k_j / sqrt(D)) v_j over the `prefix` cached keys of request b and the
+ *   tree nodes that mask row i marks (query head hq reads kv head hq / (heads / kv_heads));
+ *   h1 = x_i + Wo o_i;  r = RMSNorm(h1; rms_eps) * w_norm;  [g; u] = Wgu r;
+ *   out_i = h1 + Wd (silu(g) * u).
+ * Each projection output, the attention output, both residual sums, r and silu(g) * u are bf16
+ * (round to nearest even); dot products, the softmax and the norm accumulate in fp32.
+ * Weights (bf16, row-major, device, 16-byte aligned): w_qkv [(heads + 2 kv_heads) head_dim]
+ * [hidden] (q rows, then k rows, then v rows); w_o [hidden][heads head_dim]; w_norm [hidden];
+ * w_gu [2 inter][hidden] (gate rows, then up rows); w_d [hidden][inter].
+ * Limits: hidden and inter multiples of 8; head_dim a multiple of 32 and at most 128; heads a
+ * multiple of kv_heads; nodes in [1, 4097]; rope_theta > 0; rms_eps >= 0.
+ */
+typedef struct {
+    int32_t hidden, heads, kv_heads, head_dim, inter;
+    float rope_theta, rms_eps;
+    const void *w_qkv, *w_o, *w_norm, *w_gu, *w_d;
+} eagle_decoder_layer_weights;
+
+/*
+ * Device scratch bytes for eagle_decoder_layer at these sizes on the current device (0 on
+ * unusable sizes or without a device).
+ */
+EAGLE_API size_t eagle_decoder_layer_workspace_bytes(const eagle_decoder_layer_weights *w,
+                                                     int32_t batch, int32_t nodes);
+/*
+ * Every device array is 16-byte aligned.
+ * Inputs (device): d_x [batch][nodes][hidden] bf16; d_k_cache / d_v_cache
+ * [batch][prefix][kv_heads][head_dim] bf16, keys already rotated (may be null when prefix == 0);
+ * d_positions [batch][nodes] int32; d_mask [batch][nodes][W] uint32 with W = ceil(nodes / 32),
+ * bit t of row i set when node t is visible to node i (the tree's ancestor mask).
+ * Outputs (device): d_out [batch][nodes][hidden] bf16; d_k_new / d_v_new [batch][nodes][kv_heads]
+ * [head_dim] bf16, the tree's rotated keys and values for the caller's cache (both null to skip).
+ * d_ws: eagle_decoder_layer_workspace_bytes bytes, 256-byte aligned, zero-filled once before the
+ * first call (the GEMM's tile tickets; every call leaves them zero).  A query row with nothing
+ * visible gives o = 0.  Calls on one workspace must not overlap.  batch == 0 does nothing.
+ * Kernels: the four projections on the streamed-weight tcgen05 GEMM; RoPE (angles reduced in
+ * double, one cos/sin per row and pair); tree attention on mma.sync bf16 tensor-core tiles of 64
+ * keys with an online softmax (key splits merged by a second kernel when few CTAs); fused
+ * residual + RMSNorm; SwiGLU; residual.
+ * Returns EAGLE_ERR_INVALID_ARG on bad sizes, null or misaligned pointers or a short workspace,
+ * EAGLE_ERR_CUDA when a launch fails.  Asynchronous on `stream`.
+ */
+EAGLE_API eagle_status eagle_decoder_layer(const eagle_decoder_layer_weights *w, int32_t batch,
+                                           int32_t nodes, int32_t prefix, const void *d_x,
+                                           const void *d_k_cache, const void *d_v_cache,
+                                           const int32_t *d_positions, const uint32_t *d_mask,
+                                           void *d_out, void *d_k_new, void *d_v_new, void *d_ws,
+                                           size_t ws_bytes, eagle_stream_t stream);
+
+/*
  * The streamed-weight GEMM of eagle_linear_bf16 without caller-provided scratch.  The pages have
  * no counterpart: this is an engineering variant for callers that cannot allocate device memory
  * (code where cudaMalloc is not allowed or not wanted because it synchronises the device and can

@@ -144,3 +144,34 @@ def test_static_init_checks_depth_and_size_against_the_shape(lib):
         assert lib.eagle_tree_init_static(ctypes.byref(cfg), 3, ptr, ctypes.c_void_p(4096), 1 << 30,
                                           ctypes.byref(h)) == 1
 
+
+
+def test_decoder_layer_rejects_bad_arguments_on_the_host(lib):
+    from eagle_speculative_decoding_draft_gb300._lib import DecoderLayerWeights
+    P = ctypes.c_void_p
+
+    def weights(**kw):
+        f = dict(hidden=256, heads=4, kv_heads=2, head_dim=64, inter=512, rope_theta=1e4, rms_eps=1e-6,
+                 w_qkv=256, w_o=256, w_norm=256, w_gu=256, w_d=256)
+        f.update(kw)
+        return DecoderLayerWeights(*(f[k] for k, _ in DecoderLayerWeights._fields_))
+
+    def call(w, batch=2, nodes=9, prefix=5, x=P(256), kc=P(256), vc=P(256), kn=None, vn=None, ws=P(256)):
+        return lib.eagle_decoder_layer(ctypes.byref(w), batch, nodes, prefix, x, kc, vc, P(256), P(256), P(256),
+                                       kn, vn, ws, 1 << 30, None)
+
+    good = weights()
+    for bad in (weights(head_dim=48), weights(head_dim=256), weights(heads=3), weights(hidden=252),
+                weights(inter=100), weights(rope_theta=0.0), weights(rms_eps=-1.0), weights(w_o=0),
+                weights(w_gu=264)):
+        assert call(bad) == 1
+        assert lib.eagle_decoder_layer_workspace_bytes(ctypes.byref(bad), 2, 9) == 0
+    assert call(good, nodes=0) == 1
+    assert call(good, nodes=4098) == 1
+    assert call(good, prefix=-1) == 1
+    assert call(good, x=P(264)) == 1                 # x not 16-byte aligned
+    assert call(good, kc=None) == 1                  # a cache is needed when prefix > 0
+    assert call(good, kn=P(256)) == 1                # k_new without v_new
+    assert call(good, ws=P(128)) == 1                # workspace not 256-byte aligned
+    assert call(good, batch=0, x=None, kc=None, vc=None, ws=None) == 0  # empty batch
+    assert lib.eagle_decoder_layer_workspace_bytes(ctypes.byref(good), 2, 0) == 0
