@@ -209,3 +209,22 @@ def test_7b_draft_layer_on_sampled_nodes(dev):
                       absterms[:, -1:], exact_share=0.5)
             sk, sv = kv_slack(w["x"][b, node], w, d)
             check_kv(kn[b, node], vn[b, node], orc["k_new"][0, -1], orc["v_new"][0, -1], sk, sv)
+
+
+def test_small_activations_where_the_norm_epsilon_counts(dev):
+    """Inputs near 1e-3: the mean square of h1 is near the epsilon, which then moves the normed
+    activation by a large factor."""
+    B, n, P = 2, 7, 9
+    rng = np.random.default_rng(11)
+    w, d = layer(B=B, n=n, P=P, h=128, H=2, Hk=2, D=64, I=256, seed=6, fan_in=True)
+    w["x"] = (w["x"].float() * 1e-3).to(torch.bfloat16)
+    trees = [random_tree(n, 3, rng) for _ in range(B)]
+    masks = np.stack([tree_mask(t[0]) for t in trees])
+    pos = np.array([[P + dep for dep in t[1]] for t in trees], np.int32)
+    out = gpu_layer(dev, w, d, masks, pos, new_kv=False)
+    orc = oracle.decoder_layer(w["x"], w["w_qkv"], w["w_o"], w["w_norm"], w["w_gu"], w["w_d"], w["k_cache"],
+                               w["v_cache"], pos, masks, 2, 2)["out"]
+    for b in range(B):
+        wb = {k: v[b:b + 1] if k in ("x", "k_cache", "v_cache") else v for k, v in w.items()}
+        ref, h1, absterms = reference_layer(wb, dict(d, B=1), trees[b][0], pos[b:b + 1])
+        check_out(out[b:b + 1], orc[b:b + 1], ref, h1, absterms)

@@ -105,3 +105,15 @@ def test_a_node_ignores_nodes_outside_its_ancestry():
     got = run(w2, d)["out"]
     assert np.array_equal(got[:, :4], base[:, :4])
     assert not np.array_equal(got[:, 4], base[:, 4])
+
+
+def test_the_norm_epsilon_counts_for_small_activations():
+    """With inputs near 1e-3 the mean square of h1 is near the epsilon (1e-6), so the epsilon
+    moves the normed activation by a large factor; the output must still follow the float64
+    restatement."""
+    w, d = layer(seed=5)
+    w["x"] = (w["x"].float() * 1e-3).to(torch.bfloat16)
+    w["w_o"] = torch.zeros_like(w["w_o"])
+    got = run(w, d)["out"]
+    ref, h1, absterms = reference_at(w, d)
+    assert np.all(np.abs(got - ref) <= tolerance(h1, ref, absterms))
