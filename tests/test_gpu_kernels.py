@@ -38,9 +38,10 @@ def bf16_tensor(rng, shape, std):
     return torch.from_numpy((rng.standard_normal(shape) * std).astype(np.float32)).to(torch.bfloat16)
 
 
+# Ragged M and K, 1..256 rows (padded to the MMA's N in steps of 16), M below one 128-row tile.
 LINEAR_CASES = [(128, 64, 1), (200, 200, 17), (1000, 512, 256), (300, 64, 33), (128, 128, 16),
                 (4096, 8192, 10), (32000, 4096, 10), (777, 1000, 100), (130, 72, 255),
-                (4096, 8192, 256)]
+                (4096, 8192, 256), (300, 64, 64), (513, 1000, 49), (70, 4104, 80), (2000, 2048, 128)]
 
 
 @pytest.mark.parametrize("M,K,rows", LINEAR_CASES)
@@ -72,17 +73,21 @@ def test_linear_within_fp32_bound_of_oracle(dev, M, K, rows, out_bf16):
 @pytest.mark.parametrize("M,K", [(4096, 8192), (32000, 4096), (300, 640)])
 def test_linear_split_sums_do_not_depend_on_the_row_count(dev, M, K):
     """Up to 16 rows the last CTA of a split tile sums the partials; above, a second launch does.
-    Both add the same partials in the same CTA order, so shared rows agree bit for bit."""
+    Both add the same partials in the same CTA order, so shared rows agree bit for bit, whatever
+    the row count of the launch."""
     from eagle_speculative_decoding_draft_gb300.engine import linear_bf16
     rng = np.random.default_rng(M + K)
     W = bf16_tensor(rng, (M, K), 1 / np.sqrt(K)).to(dev)
-    X = bf16_tensor(rng, (64, K), 1.0).to(dev)
+    X = bf16_tensor(rng, (256, K), 1.0).to(dev)
     bias = bf16_tensor(rng, (M,), 0.1).to(dev)
     for out_bf16 in (False, True):
         few = linear_bf16(W, X[:16].contiguous(), bias, out_bf16=out_bf16)
-        many = linear_bf16(W, X, bias, out_bf16=out_bf16)
+        more = linear_bf16(W, X[:48].contiguous(), bias, out_bf16=out_bf16)
+        wide = linear_bf16(W, X[:64].contiguous(), bias, out_bf16=out_bf16)
+        widest = linear_bf16(W, X, bias, out_bf16=out_bf16)
         torch.cuda.synchronize()
-        assert torch.equal(few, many[:16])
+        assert torch.equal(few, more[:16])
+        assert torch.equal(wide, widest[:64])
 
 
 TOPK_CASES = [(10, 32000, 10, "f32"), (3, 1000, 16, "f32"), (4, 128256, 8, "f32"),
