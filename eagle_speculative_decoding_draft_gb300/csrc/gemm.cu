@@ -15,7 +15,13 @@
 //   stream-K    all k-blocks of all tiles are one sequence split evenly over one CTA per SM, so
 //               every SM streams the same number of weight bytes whatever the tile count; a tile
 //               cut between CTAs is summed by the last CTA to arrive (atomic ticket, no waiting),
-//               which adds the partials in ascending CTA order so results are deterministic.
+//               which adds the partials in ascending CTA order so results are deterministic;
+//   cluster-K   when the weight tiles are few (at most half the SMs: the FC, M = h), the grid is
+//               tiles x C CTAs in thread-block clusters of C; CTA r of a cluster takes the r-th
+//               slice of the tile's k-blocks, stages its fp32 accumulator in its own (then idle)
+//               ring, and after a cluster barrier sums a 1/C share of the tile's outputs over the
+//               C CTAs in rank order through distributed shared memory: no partials in global
+//               memory, no tickets, no second launch.
 #include <cstdio>
 #include <mutex>
 
@@ -50,6 +56,7 @@ struct LinearArgs {
     int64_t ldo;
     int32_t out_bf16;
     int32_t defer;  // split tiles: write partials only; linear_reduce_kernel sums them
+    int32_t cluster_k;  // > 1: split-K over a cluster of this many CTAs per tile (no stream-K)
     float *partials;
     int32_t *counters;
     int32_t *status;
@@ -93,7 +100,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t G = gridDim.x, g = blockIdx.x;
     const int64_t nkb = a.num_kb;
     const int64_t total = static_cast<int64_t>(a.num_tiles) * nkb;
-    const int64_t kb_begin = div_nonneg(total * g, G), kb_end = div_nonneg(total * (g + 1), G);
+    int64_t kb_begin = div_nonneg(total * g, G), kb_end = div_nonneg(total * (g + 1), G);
+    const int32_t CK = a.cluster_k;
+    if (CK > 1) {  // tile g / CK, k-slice g % CK (the CTA's rank in its cluster)
+        const int64_t t0 = static_cast<int64_t>(g / CK) * nkb;
+        const int32_t r = g % CK;
+        kb_begin = t0 + (nkb * r) / CK;
+        kb_end = t0 + (nkb * (r + 1)) / CK;
+    }
 
     pdl_launch_dependents();
     if (threadIdx.x == 0) {
@@ -246,6 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        acc * static_cast<uint32_t>(a.n_tile);
                 float *part = a.partials + static_cast<size_t>(g * 2 + (first ? 0 : 1)) *
                                                a.n_tile * BM;
+                // cluster-K: the accumulator goes to this CTA's ring (every stage is consumed)
+                float *stage_acc = reinterpret_cast<float *>(base);
                 for (int32_t n0 = 0; n0 < a.rows; n0 += 16) {
                     uint32_t r[16];
                     __syncwarp();
@@ -256,7 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int32_t n = n0 + j;
                         if (n < a.rows) {
                             const float v = __uint_as_float(r[j]);
-                            if (full) {
+                            if (CK > 1) {
+                                stage_acc[static_cast<size_t>(n) * BM + m_local] = v;
+                            } else if (full) {
                                 if (o_ok) store_y(a, n, o, v + bias_o);
                             } else {
                                 part[static_cast<size_t>(n) * BM + m_local] = v;
@@ -268,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0 && got) mbar_arrive(&ctl->acc_empty[acc]);
-            if (!full && !a.defer) {
+            if (!full && !a.defer && CK == 1) {
                 named_barrier_sync(1, 128);  // this CTA's partials of the tile are written
                 const int32_t gf = cta_of(t0, total, G), gl = cta_of(t0 + nkb - 1, total, G);
                 if (threadIdx.x == 64) {
@@ -374,6 +392,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+    }
+    if (CK > 1) {
+        // Every CTA of the cluster reaches both barriers, also after a timeout (then the sums
+        // are garbage, and the status word says so).  CTA r adds, for weight rows
+        // 128 r / CK .. 128 (r + 1) / CK - 1 of the tile and every row, the C staged accumulators
+        // in rank order, four outputs per thread and step, reading them through distributed
+        // shared memory.
+        __syncwarp();
+        cluster_sync();
+        if (warp >= 2 && !*abort_flag) {
+            const int32_t et = static_cast<int32_t>(threadIdx.x) - 64;
+            const int32_t rank = g % CK, tile = g / CK;
+            const int32_t per = (BM / 4) / CK;  // 4-wide groups of this CTA's share, per row
+            const int32_t groups = per * a.rows;
+            const float *stage_acc = reinterpret_cast<const float *>(base);
+            constexpr int kUnroll = 4;
+            for (int32_t e0 = et; e0 < groups; e0 += 128 * kUnroll) {
+                float4 sum[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int32_t e = e0 + u * 128;
+                    const int32_t n = e / per, m4 = (rank * per + e % per) * 4;
+#pragma unroll 1
+                    for (int32_t c = 0; c < CK; ++c) {
+                        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        if (e < groups) v = ld_peer_v4(peer_addr(stage_acc + static_cast<size_t>(n) * BM + m4, c));
+                        if (c == 0) {
+                            sum[u] = v;
+                        } else {
+                            sum[u].x += v.x;
+                            sum[u].y += v.y;
+                            sum[u].z += v.z;
+                            sum[u].w += v.w;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int32_t e = e0 + u * 128;
+                    if (e >= groups) continue;
+                    const int32_t n = e / per, m4 = (rank * per + e % per) * 4;
+                    const float v[4] = {sum[u].x, sum[u].y, sum[u].z, sum[u].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int32_t o = tile * BM + m4 + q;
+                        if (o < a.M) store_y(a, n, o, v[q] + (a.bias != nullptr ? __bfloat162float(a.bias[o]) : 0.0f));
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        cluster_sync();  // no CTA leaves while another still reads its shared memory
     }
     if (warp == 1) {
         __syncwarp();
@@ -546,6 +616,8 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     p->num_tiles = (M + BM - 1) / BM;
     const int64_t total = static_cast<int64_t>(p->num_kb) * p->num_tiles;
     p->grid = static_cast<int32_t>(total < num_sms ? total : num_sms);
+    p->cluster_k = linear_cluster_k(p->num_tiles, p->num_kb, num_sms);
+    if (p->cluster_k > 1) p->grid = p->num_tiles * p->cluster_k;
     const size_t stage_bytes = kABytes + static_cast<size_t>(p->n_tile) * 128;
     size_t stages = (kMaxDynSmem - 1024 - sizeof(SmemCtl)) / stage_bytes;
     if (stages > kMaxStages) stages = kMaxStages;
@@ -561,7 +633,10 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     p->out_bf16 = out_bf16;
     // Many rows: one CTA per tile cannot sum the partials fast enough (it reads CTAs x rows x 128
     // floats); a separate launch spreads the sum over tiles x row blocks.
-    p->defer = rows > kLinearMaxFixupRows ? 1 : 0;
+    p->defer = (rows > kLinearMaxFixupRows && p->cluster_k == 1) ? 1 : 0;
+    // cluster-K stages the accumulator (rows x 128 fp32) in the ring
+    if (p->cluster_k > 1 && static_cast<size_t>(p->n_tile) * BM * sizeof(float) > stages * stage_bytes)
+        return false;
     p->partials = partials;
     p->counters = counters;
     p->status = status;
@@ -572,6 +647,50 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
                         static_cast<uint64_t>(ldx), BK, static_cast<uint32_t>(p->n_tile)))
         return false;
     return true;
+}
+
+// Split-K over thread-block clusters when the weight tiles are at most half the SMs: C CTAs per
+// tile (a power of two, at most 8, at least 2 k-blocks each), used only when every cluster of the
+// launch can be resident at once with the largest shared-memory request (checked once per C and
+// device; the choice does not depend on the row count, so neither do the results).
+int32_t linear_cluster_k(int32_t num_tiles, int32_t num_kb, int32_t num_sms) {
+    int32_t c = 1;
+    while (c < 8 && num_tiles * (2 * c) <= num_sms && num_kb >= 2 * (2 * c)) c *= 2;
+    if (c == 1) return 1;
+    static std::mutex mu;
+    static int cached[64][4] = {};  // [device][log2 C - 1]: 0 unknown, else max active clusters + 1
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (prepare_kernels() != cudaSuccess) return 1;  // the occupancy query needs the smem attribute
+    for (; c > 1; c /= 2) {
+        const int slot = (c == 2) ? 0 : (c == 4) ? 1 : 2;
+        int active;
+        {
+            std::lock_guard<std::mutex> lock(mu);
+            if (cached[dev][slot] == 0) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(num_tiles * c);
+                cfg.blockDim = dim3(kThreads);
+                cfg.dynamicSmemBytes = kMaxDynSmem;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = c;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, linear_bf16_tc_kernel, &cfg) != cudaSuccess) {
+                    cudaGetLastError();
+                    n = 0;
+                }
+                cached[dev][slot] = n + 1;
+            }
+            active = cached[dev][slot] - 1;
+        }
+        if (active >= num_tiles) return c;
+    }
+    return 1;
 }
 
 cudaError_t prepare_kernels() {
@@ -596,11 +715,16 @@ cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
     a.ldo = p.ldo;
     a.out_bf16 = p.out_bf16;
     a.defer = p.defer;
+    a.cluster_k = p.cluster_k;
     a.partials = p.partials;
     a.counters = p.counters;
     a.status = p.status;
-    cudaError_t e = launch_pdl(linear_bf16_tc_kernel, dim3(p.grid), dim3(kThreads), p.smem_bytes, st, p.tmap_w,
-                               p.tmap_x, a);
+    cudaError_t e = p.cluster_k > 1
+                        ? launch_pdl_cluster(linear_bf16_tc_kernel, dim3(p.grid), dim3(kThreads),
+                                             static_cast<unsigned>(p.cluster_k), p.smem_bytes, st, p.tmap_w,
+                                             p.tmap_x, a)
+                        : launch_pdl(linear_bf16_tc_kernel, dim3(p.grid), dim3(kThreads), p.smem_bytes, st,
+                                     p.tmap_w, p.tmap_x, a);
     if (e != cudaSuccess || !p.defer) return e;
     return launch_pdl(linear_reduce_kernel, dim3(p.num_tiles, (p.rows + kReduceRows - 1) / kReduceRows),
                       dim3(256), 0, st, a, p.grid);

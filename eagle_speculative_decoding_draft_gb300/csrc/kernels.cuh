@@ -81,6 +81,7 @@ struct LinearPlan {
     int64_t ldo;
     int32_t out_bf16;
     int32_t defer;     // rows > kLinearMaxFixupRows: a second launch sums the split tiles
+    int32_t cluster_k; // > 1: split-K over clusters of this many CTAs per tile, summed on chip
     float *partials;   // [grid][2][n_tile][128]
     int32_t *counters; // [num_tiles], zero before and after
     int32_t *status;
@@ -90,6 +91,8 @@ struct LinearPlan {
 size_t linear_partials_bytes(int32_t grid, int32_t n_tile);
 size_t linear_counters_bytes(int32_t M);
 int32_t linear_n_tile(int32_t rows);
+// CTAs per tile of the cluster split-K (1: stream-K over one CTA per SM).
+int32_t linear_cluster_k(int32_t num_tiles, int32_t num_kb, int32_t num_sms);
 
 // Fills `plan` (tensor maps included).  Returns false on an unusable argument (alignment,
 // strides, sizes) or when the driver's tensor-map encoder is unavailable.
