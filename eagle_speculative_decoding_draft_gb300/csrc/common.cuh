@@ -29,6 +29,13 @@ __device__ __forceinline__ int32_t atomic_add_acq_rel_gpu(int32_t *p, int32_t v)
     return old;
 }
 
+// Load with acquire semantics at GPU scope (pairs with a release by another CTA).
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void latch(int32_t *status, int32_t bits) {
     if (status) atomicOr(status, bits);
 }
@@ -177,6 +184,20 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *map, uin
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
         : "memory");
 }
+
+// 1-D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to
+// shared memory; completion is counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses (shared and global) before its later
+// async-proxy operations (bulk copies), and the other way round.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------------------------
 // tcgen05 (5th-generation tensor core, accumulators in tensor memory)

@@ -43,10 +43,12 @@ struct SmemCtl {
     uint64_t empty[kMaxStages];  // MMA -> TMA: stage consumed
     uint64_t acc_full[2];        // MMA -> epilogue: accumulator ready
     uint64_t acc_empty[2];       // epilogue -> MMA: accumulator drained (4 warps arrive)
+    uint64_t fix;                // split-tile owner: the other CTA's partial staged in the ring
     uint64_t drain;              // used only when unwinding after a timeout
     uint32_t tmem_base;
     int32_t abort;
     int32_t is_last;
+    int32_t fix_chunks;          // staged copies issued on `fix` (phases), for unwinding
 };
 
 struct LinearArgs {
@@ -57,6 +59,7 @@ struct LinearArgs {
     int32_t out_bf16;
     int32_t defer;  // split tiles: write partials only; linear_reduce_kernel sums them
     int32_t cluster_k;  // > 1: split-K over a cluster of this many CTAs per tile (no stream-K)
+    int32_t owner_fix;  // split tiles summed in the launch by the CTA that finds its partner done
     float *partials;
     int32_t *counters;
     int32_t *status;
@@ -83,6 +86,87 @@ __device__ __forceinline__ void store_y(const LinearArgs &a, int32_t r, int32_t 
         reinterpret_cast<float *>(a.out)[static_cast<int64_t>(r) * a.ldo + o] = v;
 }
 
+// Sums a split tile's partials in ascending CTA order (the order of every other path) and writes
+// Y (+ bias), for the CTA at its last segment, whose ring is then idle: the partials of the other
+// CTAs gf .. gl are copied into the ring by the bulk-copy engine, as many rows at a time as fit
+// (one round trip per chunk instead of one per row), and this CTA's own values come from its
+// TMEM accumulator (t_row).  Run by the 128 epilogue threads; returns false when a copy did not
+// land in time.
+__device__ __forceinline__ bool staged_fixup(const LinearArgs &a, SmemCtl *ctl, uint8_t *ring, uint32_t ring_bytes,
+                                             int32_t gf, int32_t gl, int32_t self, bool gf_second,
+                                             uint32_t t_row, int32_t et, int32_t m_local, int32_t o, bool o_ok,
+                                             float bias_o, volatile int32_t *abort_flag) {
+    const int32_t np = gl - gf;  // partials read from global memory
+    const uint32_t row_bytes = BM * 4u;
+    int32_t cr = static_cast<int32_t>(ring_bytes / (static_cast<uint32_t>(np) * row_bytes)) & ~15;
+    cr = min(cr, a.n_tile);
+    const int32_t nch = (a.rows + cr - 1) / cr;
+    cr = (((a.rows + nch - 1) / nch) + 15) & ~15;
+    const float *staged = reinterpret_cast<const float *>(ring);
+    for (int32_t c = 0; c < nch; ++c) {
+        const int32_t r0 = c * cr, rc = min(cr, a.rows - r0);
+        if (et == 0) {
+            fence_proxy_async();  // earlier accesses of the ring before the new copies
+            ctl->fix_chunks = c + 1;  // at most one staged sum per launch: phase c
+            mbar_arrive_expect_tx(&ctl->fix, static_cast<uint32_t>(np * rc) * row_bytes);
+            int32_t pi = 0;
+            for (int32_t gg = gf; gg <= gl; ++gg) {
+                if (gg == self) continue;
+                const int32_t slot = (gg == gf && gf_second) ? 1 : 0;
+                const uint8_t *src = reinterpret_cast<const uint8_t *>(
+                    a.partials + static_cast<size_t>(gg * 2 + slot) * a.n_tile * BM + static_cast<size_t>(r0) * BM);
+                uint8_t *dst = ring + static_cast<size_t>(pi) * cr * row_bytes;
+                const uint32_t bytes = static_cast<uint32_t>(rc) * row_bytes;
+                for (uint32_t off = 0; off < bytes; off += 32768u)
+                    bulk_load(dst + off, src + off, min(32768u, bytes - off), &ctl->fix);
+                ++pi;
+            }
+        }
+        if (!mbar_wait(&ctl->fix, static_cast<uint32_t>(c) & 1u, abort_flag)) {
+            *abort_flag = 1;
+            latch(a.status, kDevTimeout);
+        }
+        named_barrier_sync(1, 128);
+        if (*abort_flag) return false;
+        for (int32_t n0 = r0; n0 < r0 + rc; n0 += 16) {
+            uint32_t r[16];
+            __syncwarp();
+            tmem_ld_16(t_row + static_cast<uint32_t>(n0), r);
+            tmem_wait_ld();
+            // 16 rows at a time: every load of the group, then every add, then every store
+            const float *src0 = staged + static_cast<size_t>(n0 - r0) * BM + m_local;
+            float sum[16];
+            int32_t pi = 0;
+            for (int32_t gg = gf; gg <= gl; ++gg) {
+                float v[16];
+                if (gg == self) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+                } else {
+                    const float *src = src0 + static_cast<size_t>(pi) * cr * BM;  // rows of the chunk
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = src[static_cast<size_t>(j) * BM];
+                    ++pi;
+                }
+                if (gg == gf) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) sum[j] = v[j];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) sum[j] += v[j];
+                }
+            }
+            if (o_ok) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (n0 + j < r0 + rc) store_y(a, n0 + j, o, sum[j] + bias_o);
+            }
+        }
+        named_barrier_sync(1, 128);  // every thread is done with the chunk
+    }
+    return true;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     linear_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                           const __grid_constant__ CUtensorMap tmap_x, const LinearArgs a) {
@@ -94,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *a_tiles = base;
     uint8_t *b_tiles = base + static_cast<size_t>(stages) * kABytes;
     SmemCtl *ctl = reinterpret_cast<SmemCtl *>(b_tiles + static_cast<size_t>(stages) * b_bytes);
+    const uint32_t ring_bytes = static_cast<uint32_t>(stages) * (kABytes + b_bytes);
     volatile int32_t *abort_flag = &ctl->abort;
 
     const int32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -119,9 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ctl->acc_full[i], 1);
             mbar_init(&ctl->acc_empty[i], 4);
         }
+        mbar_init(&ctl->fix, 1);
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
         ctl->is_last = 0;
+        ctl->fix_chunks = 0;
         fence_barrier_init();
         prefetch_tensormap(&tmap_w);
         prefetch_tensormap(&tmap_x);
@@ -253,8 +340,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t o = tile * BM + m_local;
             const bool o_ok = o < a.M;
             const float bias_o = (a.bias != nullptr && o_ok) ? __bfloat162float(a.bias[o]) : 0.0f;
+            // A tile cut between CTAs gf .. gl and summed in this launch.  With owner_fix, the CTA
+            // at its last segment that finds every other CTA's ticket in (usually: the head of a
+            // tile whose tail the next CTA computed first) owns the sum and takes its own values
+            // straight from TMEM; the other CTAs leave partials and tickets.
+            const bool split = !full && !a.defer && CK == 1;
+            int32_t gf = g, gl = g;
+            bool owner = false;
+            if (split) {
+                gf = cta_of(t0, total, G);
+                gl = cta_of(t0 + nkb - 1, total, G);
+                if (a.owner_fix) {
+                    const bool fits = static_cast<uint32_t>(gl - gf) * 16u * BM * 4u <= ring_bytes;
+                    if (threadIdx.x == 64)  // acquire: the other CTAs' partials, for the copies
+                        ctl->is_last = (got && !*abort_flag && fits && k1 == kb_end &&
+                                        ld_acquire_gpu(&a.counters[tile]) == gl - gf) ? 1 : 0;
+                    named_barrier_sync(1, 128);
+                    owner = ctl->is_last != 0;
+                }
+            }
+            // CTAs gf < g <= gl start inside the tile, so it is their first segment (slot 0); CTA
+            // gf wrote slot 1 unless its range starts with this tile.
+            const bool gf_second = div_nonneg(total * gf, G) < t0;
             __syncwarp();
-            if (got) {
+            if (got && owner) {
+                tc_fence_after();
+                const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       acc * static_cast<uint32_t>(a.n_tile);
+                staged_fixup(a, ctl, base, ring_bytes, gf, gl, g, gf_second, t_row, threadIdx.x - 64, m_local, o,
+                             o_ok, bias_o, abort_flag);
+            } else if (got) {
                 tc_fence_after();
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        acc * static_cast<uint32_t>(a.n_tile);
@@ -286,9 +401,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0 && got) mbar_arrive(&ctl->acc_empty[acc]);
-            if (!full && !a.defer && CK == 1) {
+            if (split && owner) {
+                if (threadIdx.x == 64) a.counters[tile] = 0;  // ready for the next launch
+                named_barrier_sync(1, 128);                  // ctl->is_last is reused
+            } else if (split) {
                 named_barrier_sync(1, 128);  // this CTA's partials of the tile are written
-                const int32_t gf = cta_of(t0, total, G), gl = cta_of(t0 + nkb - 1, total, G);
                 if (threadIdx.x == 64) {
                     int32_t last = 0;
                     if (!*abort_flag) {
@@ -302,9 +419,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 named_barrier_sync(1, 128);
                 if (ctl->is_last) {
-                    // CTAs gf < g <= gl start inside this tile, so it is their first segment
-                    // (slot 0); CTA gf wrote slot 1 unless its range starts with this tile.
-                    const bool gf_second = div_nonneg(total * gf, G) < t0;
                     // Sum the partials in ascending CTA order.  Thread e of the 128 sums outputs
                     // 4(e % 32) .. +3 of rows e / 32, +4, +8, ...; all loads of a batch of rows x
                     // CTAs are issued before any is used, so the fix-up costs one L2 round trip
@@ -383,6 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 0 && lane == 0) {
             for (int s = 0; s < stages; ++s)
                 if ((issued >> s) & 1u) mbar_wait(&ctl->full[s], (issued_parity >> s) & 1u, nullptr);
+            if (ctl->fix_chunks > 0)
+                mbar_wait(&ctl->fix, static_cast<uint32_t>(ctl->fix_chunks - 1) & 1u, nullptr);
         }
         if (warp == 1 && lane == 0) {
             mma_commit(&ctl->drain);
@@ -633,7 +749,13 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     p->out_bf16 = out_bf16;
     // Many rows: one CTA per tile cannot sum the partials fast enough (it reads CTAs x rows x 128
     // floats); a separate launch spreads the sum over tiles x row blocks.
-    p->defer = (rows > kLinearMaxFixupRows && p->cluster_k == 1) ? 1 : 0;
+    // Above 16 rows, split tiles are summed inside the launch when every CTA covers at least a
+    // whole tile's k-blocks (then a tile is shared by at most two CTAs, and the one that reaches
+    // it at the end of its range finds the other's partial in and owns the sum), else by a
+    // second launch.
+    const int64_t per_cta = total / p->grid;  // fewest k-blocks of any CTA
+    p->owner_fix = (rows > kLinearMaxFixupRows && p->cluster_k == 1 && per_cta >= p->num_kb) ? 1 : 0;
+    p->defer = (rows > kLinearMaxFixupRows && p->cluster_k == 1 && !p->owner_fix) ? 1 : 0;
     // cluster-K stages the accumulator (rows x 128 fp32) in the ring
     if (p->cluster_k > 1 && static_cast<size_t>(p->n_tile) * BM * sizeof(float) > stages * stage_bytes)
         return false;
@@ -716,6 +838,7 @@ cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
     a.out_bf16 = p.out_bf16;
     a.defer = p.defer;
     a.cluster_k = p.cluster_k;
+    a.owner_fix = p.owner_fix;
     a.partials = p.partials;
     a.counters = p.counters;
     a.status = p.status;

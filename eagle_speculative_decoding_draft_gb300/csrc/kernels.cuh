@@ -82,6 +82,7 @@ struct LinearPlan {
     int32_t out_bf16;
     int32_t defer;     // rows > kLinearMaxFixupRows: a second launch sums the split tiles
     int32_t cluster_k; // > 1: split-K over clusters of this many CTAs per tile, summed on chip
+    int32_t owner_fix; // > 16 rows, at most two CTAs per tile: summed in the launch by its owner
     float *partials;   // [grid][2][n_tile][128]
     int32_t *counters; // [num_tiles], zero before and after
     int32_t *status;
