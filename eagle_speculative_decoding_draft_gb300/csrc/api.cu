@@ -343,7 +343,7 @@ struct eagle_tree {
         for (size_t i = 0; i < s.plans.size(); ++i) {
             LinearPlan p = s.plans[i];
             if (out_override)
-                p.out = reinterpret_cast<uint8_t *>(out_override) + static_cast<int64_t>(s.row0[i]) * ldo * ob;
+                linear_retarget_out(&p, reinterpret_cast<uint8_t *>(out_override) + static_cast<int64_t>(s.row0[i]) * ldo * ob);
             cudaError_t e = gemm(p, st, tag);
             if (e != cudaSuccess) return e;
         }

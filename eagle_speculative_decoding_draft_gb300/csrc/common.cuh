@@ -199,6 +199,28 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, 
 // async-proxy operations (bulk copies), and the other way round.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
+// 2-D tiled store of box {x.., y..} from shared memory (bulk-group completion); elements outside
+// the tensor are not written.  x (the innermost coordinate) must be a multiple of 16 bytes' worth
+// of elements and both coordinates >= 0.
+__device__ __forceinline__ void tma_store_2d(const void *map, const void *smem_src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N committed bulk groups still read their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until every committed bulk group has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Orders this thread's shared-memory writes before later async-proxy reads of them (a TMA store).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------------------------
 // tcgen05 (5th-generation tensor core, accumulators in tensor memory)
 // ---------------------------------------------------------------------------------------------

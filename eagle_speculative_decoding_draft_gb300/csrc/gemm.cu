@@ -60,6 +60,7 @@ struct LinearArgs {
     int32_t defer;  // split tiles: write partials only; linear_reduce_kernel sums them
     int32_t cluster_k;  // > 1: split-K over a cluster of this many CTAs per tile (no stream-K)
     int32_t owner_fix;  // split tiles summed in the launch by the CTA that finds its partner done
+    int32_t y_tma;      // Y is written by TMA stores from the owner's fix-up (tmap_y valid)
     float *partials;
     int32_t *counters;
     int32_t *status;
@@ -92,17 +93,24 @@ __device__ __forceinline__ void store_y(const LinearArgs &a, int32_t r, int32_t 
 // (one round trip per chunk instead of one per row), and this CTA's own values come from its
 // TMEM accumulator (t_row).  Run by the 128 epilogue threads; returns false when a copy did not
 // land in time.
-__device__ __forceinline__ bool staged_fixup(const LinearArgs &a, SmemCtl *ctl, uint8_t *ring, uint32_t ring_bytes,
-                                             int32_t gf, int32_t gl, int32_t self, bool gf_second,
-                                             uint32_t t_row, int32_t et, int32_t m_local, int32_t o, bool o_ok,
-                                             float bias_o, volatile int32_t *abort_flag) {
+__device__ __forceinline__ bool staged_fixup(const LinearArgs &a, const CUtensorMap *tmap_y, SmemCtl *ctl,
+                                             uint8_t *ring, uint32_t ring_bytes, int32_t tile, int32_t gf,
+                                             int32_t gl, int32_t self, bool gf_second, uint32_t t_row, int32_t et,
+                                             int32_t m_local, int32_t o, bool o_ok, float bias_o,
+                                             volatile int32_t *abort_flag) {
     const int32_t np = gl - gf;  // partials read from global memory
     const uint32_t row_bytes = BM * 4u;
-    int32_t cr = static_cast<int32_t>(ring_bytes / (static_cast<uint32_t>(np) * row_bytes)) & ~15;
+    // With TMA stores, each group of 16 output rows is assembled in one of two buffers at the end
+    // of the ring and written by one bulk tensor store (512 contiguous bytes a row).
+    const uint32_t out_bytes = 16u * BM * (a.out_bf16 ? 2u : 4u);
+    const uint32_t stage_room = a.y_tma ? ring_bytes - 2u * out_bytes - 1024u : ring_bytes;
+    int32_t cr = static_cast<int32_t>(stage_room / (static_cast<uint32_t>(np) * row_bytes)) & ~15;
     cr = min(cr, a.n_tile);
     const int32_t nch = (a.rows + cr - 1) / cr;
     cr = (((a.rows + nch - 1) / nch) + 15) & ~15;
     const float *staged = reinterpret_cast<const float *>(ring);
+    uint8_t *out_stage = ring + ((static_cast<uint32_t>(np * cr) * row_bytes + 1023u) & ~1023u);
+    int32_t gi = 0;  // output groups written so far
     for (int32_t c = 0; c < nch; ++c) {
         const int32_t r0 = c * cr, rc = min(cr, a.rows - r0);
         if (et == 0) {
@@ -127,7 +135,10 @@ __device__ __forceinline__ bool staged_fixup(const LinearArgs &a, SmemCtl *ctl, 
             latch(a.status, kDevTimeout);
         }
         named_barrier_sync(1, 128);
-        if (*abort_flag) return false;
+        if (*abort_flag) {
+            if (et == 0 && a.y_tma) bulk_wait_all();
+            return false;
+        }
         for (int32_t n0 = r0; n0 < r0 + rc; n0 += 16) {
             uint32_t r[16];
             __syncwarp();
@@ -156,7 +167,27 @@ __device__ __forceinline__ bool staged_fixup(const LinearArgs &a, SmemCtl *ctl, 
                     for (int j = 0; j < 16; ++j) sum[j] += v[j];
                 }
             }
-            if (o_ok) {
+            if (a.y_tma) {
+                uint8_t *buf = out_stage + static_cast<size_t>(gi & 1) * out_bytes;
+                if (et == 0 && gi >= 2) bulk_wait_read<1>();  // the store of group gi - 2 read buf
+                named_barrier_sync(1, 128);
+                if (a.out_bf16) {
+                    __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(buf);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) ob[j * BM + m_local] = __float2bfloat16_rn(sum[j] + bias_o);
+                } else {
+                    float *ob = reinterpret_cast<float *>(buf);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) ob[j * BM + m_local] = sum[j] + bias_o;
+                }
+                fence_proxy_async_smem();  // the writes above, before the TMA store reads them
+                named_barrier_sync(1, 128);
+                if (et == 0) {  // rows >= rows and columns >= M fall outside the tensor map
+                    tma_store_2d(tmap_y, buf, tile * BM, n0);
+                    bulk_commit();
+                }
+                ++gi;
+            } else if (o_ok) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     if (n0 + j < r0 + rc) store_y(a, n0 + j, o, sum[j] + bias_o);
@@ -164,12 +195,14 @@ __device__ __forceinline__ bool staged_fixup(const LinearArgs &a, SmemCtl *ctl, 
         }
         named_barrier_sync(1, 128);  // every thread is done with the chunk
     }
+    if (et == 0 && a.y_tma) bulk_wait_all();
     return true;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     linear_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                          const __grid_constant__ CUtensorMap tmap_x, const LinearArgs a) {
+                          const __grid_constant__ CUtensorMap tmap_x,
+                          const __grid_constant__ CUtensorMap tmap_y, const LinearArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -351,7 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 gf = cta_of(t0, total, G);
                 gl = cta_of(t0 + nkb - 1, total, G);
                 if (a.owner_fix) {
-                    const bool fits = static_cast<uint32_t>(gl - gf) * 16u * BM * 4u <= ring_bytes;
+                    const uint32_t room = a.y_tma ? ring_bytes - 2u * 16u * BM * (a.out_bf16 ? 2u : 4u) - 1024u
+                                                  : ring_bytes;  // as staged_fixup divides the ring
+                    const bool fits = static_cast<uint32_t>(gl - gf) * 16u * BM * 4u <= room;
                     if (threadIdx.x == 64)  // acquire: the other CTAs' partials, for the copies
                         ctl->is_last = (got && !*abort_flag && fits && k1 == kb_end &&
                                         ld_acquire_gpu(&a.counters[tile]) == gl - gf) ? 1 : 0;
@@ -367,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        acc * static_cast<uint32_t>(a.n_tile);
-                staged_fixup(a, ctl, base, ring_bytes, gf, gl, g, gf_second, t_row, threadIdx.x - 64, m_local, o,
-                             o_ok, bias_o, abort_flag);
+                staged_fixup(a, &tmap_y, ctl, base, ring_bytes, tile, gf, gl, g, gf_second, t_row, threadIdx.x - 64,
+                             m_local, o, o_ok, bias_o, abort_flag);
             } else if (got) {
                 tc_fence_after();
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -706,6 +741,24 @@ bool encode_bf16_2d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Y [rows][ldo] (fp32 or bf16) for TMA stores of {128 columns, 16 rows}, no swizzle.
+bool encode_out_2d(CUtensorMap *map, const void *ptr, int32_t out_bf16, uint64_t inner, uint64_t outer,
+                   uint64_t row_stride_elems) {
+    EncodeTiledFn fn = encoder();
+    if (!fn) return false;
+    const uint64_t es = out_bf16 ? 2 : 4;
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return false;
+    if ((row_stride_elems * es) % 16 != 0) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_elems * es};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BM), 16};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+              const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 int32_t linear_n_tile(int32_t rows) { return ((rows + 15) / 16) * 16; }
@@ -765,6 +818,10 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     if (!encode_bf16_2d(&p->tmap_w, w, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
                         static_cast<uint64_t>(ldw), BK, BM))
         return false;
+    p->y_tma = (p->owner_fix && encode_out_2d(&p->tmap_y, out, out_bf16, static_cast<uint64_t>(M),
+                                              static_cast<uint64_t>(rows), static_cast<uint64_t>(ldo)))
+                   ? 1
+                   : 0;
     if (!encode_bf16_2d(&p->tmap_x, x, static_cast<uint64_t>(K), static_cast<uint64_t>(rows),
                         static_cast<uint64_t>(ldx), BK, static_cast<uint32_t>(p->n_tile)))
         return false;
@@ -822,6 +879,15 @@ cudaError_t prepare_kernels() {
     return e;
 }
 
+void linear_retarget_out(LinearPlan *p, void *out) {
+    p->out = out;
+    if (p->y_tma)
+        p->y_tma = encode_out_2d(&p->tmap_y, out, p->out_bf16, static_cast<uint64_t>(p->M),
+                                 static_cast<uint64_t>(p->rows), static_cast<uint64_t>(p->ldo))
+                       ? 1
+                       : 0;
+}
+
 cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
     LinearArgs a;
     a.M = p.M;
@@ -839,15 +905,16 @@ cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
     a.defer = p.defer;
     a.cluster_k = p.cluster_k;
     a.owner_fix = p.owner_fix;
+    a.y_tma = p.y_tma;
     a.partials = p.partials;
     a.counters = p.counters;
     a.status = p.status;
     cudaError_t e = p.cluster_k > 1
                         ? launch_pdl_cluster(linear_bf16_tc_kernel, dim3(p.grid), dim3(kThreads),
                                              static_cast<unsigned>(p.cluster_k), p.smem_bytes, st, p.tmap_w,
-                                             p.tmap_x, a)
+                                             p.tmap_x, p.tmap_y, a)
                         : launch_pdl(linear_bf16_tc_kernel, dim3(p.grid), dim3(kThreads), p.smem_bytes, st,
-                                     p.tmap_w, p.tmap_x, a);
+                                     p.tmap_w, p.tmap_x, p.tmap_y, a);
     if (e != cudaSuccess || !p.defer) return e;
     return launch_pdl(linear_reduce_kernel, dim3(p.num_tiles, (p.rows + kReduceRows - 1) / kReduceRows),
                       dim3(256), 0, st, a, p.grid);

@@ -74,6 +74,7 @@ constexpr int kLinearMaxFixupRows = 16;  // above this, split tiles are summed b
 struct LinearPlan {
     CUtensorMap tmap_w;  // W [M][K] bf16, box {64, 128}, 128-byte swizzle
     CUtensorMap tmap_x;  // X [rows][K] bf16, box {64, n_tile}, 128-byte swizzle
+    CUtensorMap tmap_y;  // Y [rows][ldo], box {128, 16}, no swizzle (valid when y_tma)
     int32_t M, K, rows, n_tile, num_kb, num_tiles, stages, tmem_cols, grid;
     size_t smem_bytes;
     const void *bias;  // [M] bf16 or null
@@ -83,6 +84,7 @@ struct LinearPlan {
     int32_t defer;     // rows > kLinearMaxFixupRows: a second launch sums the split tiles
     int32_t cluster_k; // > 1: split-K over clusters of this many CTAs per tile, summed on chip
     int32_t owner_fix; // > 16 rows, at most two CTAs per tile: summed in the launch by its owner
+    int32_t y_tma;     // the owner writes Y with TMA stores
     float *partials;   // [grid][2][n_tile][128]
     int32_t *counters; // [num_tiles], zero before and after
     int32_t *status;
@@ -102,6 +104,9 @@ bool plan_linear_bf16(LinearPlan *plan, const void *w, int64_t ldw, int32_t M, i
                       int64_t ldo, int32_t out_bf16, float *partials, int32_t *counters,
                       int32_t *status, int32_t num_sms);
 cudaError_t launch_linear_bf16(const LinearPlan &plan, cudaStream_t st);
+// Points a plan's output at another buffer of the same layout (re-encodes the output tensor map
+// of the TMA stores, or falls back to plain stores when the new buffer does not suit it).
+void linear_retarget_out(LinearPlan *plan, void *out);
 // One-time per-device kernel attributes (large dynamic shared memory).
 cudaError_t prepare_kernels();
 
