@@ -208,6 +208,14 @@ __device__ __forceinline__ void tma_store_2d(const void *map, const void *smem_s
                  "r"(smem_u32(smem_src)), "r"(x), "r"(y)
                  : "memory");
 }
+// 1-D bulk store of `bytes` (a multiple of 16; both addresses 16-byte aligned) from shared to
+// global memory (bulk-group completion).
+__device__ __forceinline__ void bulk_store(void *gmem_dst, const void *smem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(gmem_dst)),
+                 "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N committed bulk groups still read their shared-memory source.
 template <int N>

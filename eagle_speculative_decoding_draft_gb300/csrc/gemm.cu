@@ -37,6 +37,8 @@ constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB weight tile
 constexpr int kMaxStages = 16;
 constexpr int kThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
 constexpr size_t kMaxDynSmem = 232448;  // 227 KB per CTA on sm_100-class parts
+constexpr uint32_t kGroupBytes = 16u * BM * 4u;  // one 16-row group of a 128-wide tile in fp32
+constexpr uint32_t kOutStageBytes = 2u * kGroupBytes;  // two staging buffers for bulk stores
 
 struct SmemCtl {
     uint64_t full[kMaxStages];   // TMA -> MMA: stage loaded
@@ -60,7 +62,8 @@ struct LinearArgs {
     int32_t defer;  // split tiles: write partials only; linear_reduce_kernel sums them
     int32_t cluster_k;  // > 1: split-K over a cluster of this many CTAs per tile (no stream-K)
     int32_t owner_fix;  // split tiles summed in the launch by the CTA that finds its partner done
-    int32_t y_tma;      // Y is written by TMA stores from the owner's fix-up (tmap_y valid)
+    int32_t y_tma;      // 16-row groups of Y and of partials go out by bulk stores (tmap_y valid)
+    int32_t out_stage_bytes;  // shared-memory staging of those groups (after the ring)
     float *partials;
     int32_t *counters;
     int32_t *status;
@@ -87,6 +90,38 @@ __device__ __forceinline__ void store_y(const LinearArgs &a, int32_t r, int32_t 
         reinterpret_cast<float *>(a.out)[static_cast<int64_t>(r) * a.ldo + o] = v;
 }
 
+// Writes rows n0 .. n0 + 15 of this thread's column (m_local) of a 128-wide tile through one of two
+// shared-memory staging buffers; thread et 0 sends the group with one bulk store: a TMA tensor
+// store into Y (to_y: rows and columns outside Y are dropped; bf16 when Y is bf16) or a 1-D bulk
+// store of the rows into the partial slot `part` (fp32, [row][128]).  All 128 epilogue threads.
+__device__ __forceinline__ void group_store(const LinearArgs &a, const CUtensorMap *tmap_y, uint8_t *out_stage,
+                                            int32_t &gi, int32_t et, int32_t m_local, const float (&v)[16],
+                                            bool to_y, float *part, int32_t tile, int32_t n0) {
+    uint8_t *buf = out_stage + static_cast<size_t>(gi & 1) * kGroupBytes;
+    if (et == 0 && gi >= 2) bulk_wait_read<1>();  // the store of group gi - 2 has read buf
+    named_barrier_sync(1, 128);
+    if (to_y && a.out_bf16) {
+        __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(buf);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ob[j * BM + m_local] = __float2bfloat16_rn(v[j]);
+    } else {
+        float *ob = reinterpret_cast<float *>(buf);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ob[j * BM + m_local] = v[j];
+    }
+    fence_proxy_async_smem();  // the writes above, before the bulk store reads them
+    named_barrier_sync(1, 128);
+    if (et == 0) {
+        if (to_y)
+            tma_store_2d(tmap_y, buf, tile * BM, n0);
+        else
+            bulk_store(part + static_cast<size_t>(n0) * BM, buf,
+                       static_cast<uint32_t>(min(16, a.rows - n0)) * BM * 4u);
+        bulk_commit();
+    }
+    ++gi;
+}
+
 // Sums a split tile's partials in ascending CTA order (the order of every other path) and writes
 // Y (+ bias), for the CTA at its last segment, whose ring is then idle: the partials of the other
 // CTAs gf .. gl are copied into the ring by the bulk-copy engine, as many rows at a time as fit
@@ -94,23 +129,17 @@ __device__ __forceinline__ void store_y(const LinearArgs &a, int32_t r, int32_t 
 // TMEM accumulator (t_row).  Run by the 128 epilogue threads; returns false when a copy did not
 // land in time.
 __device__ __forceinline__ bool staged_fixup(const LinearArgs &a, const CUtensorMap *tmap_y, SmemCtl *ctl,
-                                             uint8_t *ring, uint32_t ring_bytes, int32_t tile, int32_t gf,
-                                             int32_t gl, int32_t self, bool gf_second, uint32_t t_row, int32_t et,
-                                             int32_t m_local, int32_t o, bool o_ok, float bias_o,
-                                             volatile int32_t *abort_flag) {
+                                             uint8_t *ring, uint32_t ring_bytes, uint8_t *out_stage, int32_t &gi,
+                                             int32_t tile, int32_t gf, int32_t gl, int32_t self, bool gf_second,
+                                             uint32_t t_row, int32_t et, int32_t m_local, int32_t o, bool o_ok,
+                                             float bias_o, volatile int32_t *abort_flag) {
     const int32_t np = gl - gf;  // partials read from global memory
     const uint32_t row_bytes = BM * 4u;
-    // With TMA stores, each group of 16 output rows is assembled in one of two buffers at the end
-    // of the ring and written by one bulk tensor store (512 contiguous bytes a row).
-    const uint32_t out_bytes = 16u * BM * (a.out_bf16 ? 2u : 4u);
-    const uint32_t stage_room = a.y_tma ? ring_bytes - 2u * out_bytes - 1024u : ring_bytes;
-    int32_t cr = static_cast<int32_t>(stage_room / (static_cast<uint32_t>(np) * row_bytes)) & ~15;
+    int32_t cr = static_cast<int32_t>(ring_bytes / (static_cast<uint32_t>(np) * row_bytes)) & ~15;
     cr = min(cr, a.n_tile);
     const int32_t nch = (a.rows + cr - 1) / cr;
     cr = (((a.rows + nch - 1) / nch) + 15) & ~15;
     const float *staged = reinterpret_cast<const float *>(ring);
-    uint8_t *out_stage = ring + ((static_cast<uint32_t>(np * cr) * row_bytes + 1023u) & ~1023u);
-    int32_t gi = 0;  // output groups written so far
     for (int32_t c = 0; c < nch; ++c) {
         const int32_t r0 = c * cr, rc = min(cr, a.rows - r0);
         if (et == 0) {
@@ -135,10 +164,7 @@ __device__ __forceinline__ bool staged_fixup(const LinearArgs &a, const CUtensor
             latch(a.status, kDevTimeout);
         }
         named_barrier_sync(1, 128);
-        if (*abort_flag) {
-            if (et == 0 && a.y_tma) bulk_wait_all();
-            return false;
-        }
+        if (*abort_flag) return false;
         for (int32_t n0 = r0; n0 < r0 + rc; n0 += 16) {
             uint32_t r[16];
             __syncwarp();
@@ -168,25 +194,9 @@ __device__ __forceinline__ bool staged_fixup(const LinearArgs &a, const CUtensor
                 }
             }
             if (a.y_tma) {
-                uint8_t *buf = out_stage + static_cast<size_t>(gi & 1) * out_bytes;
-                if (et == 0 && gi >= 2) bulk_wait_read<1>();  // the store of group gi - 2 read buf
-                named_barrier_sync(1, 128);
-                if (a.out_bf16) {
-                    __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(buf);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) ob[j * BM + m_local] = __float2bfloat16_rn(sum[j] + bias_o);
-                } else {
-                    float *ob = reinterpret_cast<float *>(buf);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) ob[j * BM + m_local] = sum[j] + bias_o;
-                }
-                fence_proxy_async_smem();  // the writes above, before the TMA store reads them
-                named_barrier_sync(1, 128);
-                if (et == 0) {  // rows >= rows and columns >= M fall outside the tensor map
-                    tma_store_2d(tmap_y, buf, tile * BM, n0);
-                    bulk_commit();
-                }
-                ++gi;
+                for (int j = 0; j < 16; ++j) sum[j] += bias_o;
+                group_store(a, tmap_y, out_stage, gi, et, m_local, sum, true, nullptr, tile, n0);
             } else if (o_ok) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
@@ -195,7 +205,6 @@ __device__ __forceinline__ bool staged_fixup(const LinearArgs &a, const CUtensor
         }
         named_barrier_sync(1, 128);  // every thread is done with the chunk
     }
-    if (et == 0 && a.y_tma) bulk_wait_all();
     return true;
 }
 
@@ -210,7 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_bytes = static_cast<uint32_t>(a.n_tile) * 128u;
     uint8_t *a_tiles = base;
     uint8_t *b_tiles = base + static_cast<size_t>(stages) * kABytes;
-    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(b_tiles + static_cast<size_t>(stages) * b_bytes);
+    uint8_t *out_stage = b_tiles + static_cast<size_t>(stages) * b_bytes;  // bulk-store staging
+    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(out_stage + a.out_stage_bytes);
     const uint32_t ring_bytes = static_cast<uint32_t>(stages) * (kABytes + b_bytes);
     volatile int32_t *abort_flag = &ctl->abort;
 
@@ -360,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t m_local = q * 32 + lane;
         uint32_t acc = 0, acc_phase = 0;
         bool first = true;
+        int32_t gi = 0;  // 16-row groups sent by bulk stores
         for (int64_t kb = kb_begin; kb < kb_end;) {
             const int32_t tile = static_cast<int32_t>(div_nonneg(kb, nkb));
             const int64_t t0 = static_cast<int64_t>(tile) * nkb;
@@ -384,9 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 gf = cta_of(t0, total, G);
                 gl = cta_of(t0 + nkb - 1, total, G);
                 if (a.owner_fix) {
-                    const uint32_t room = a.y_tma ? ring_bytes - 2u * 16u * BM * (a.out_bf16 ? 2u : 4u) - 1024u
-                                                  : ring_bytes;  // as staged_fixup divides the ring
-                    const bool fits = static_cast<uint32_t>(gl - gf) * 16u * BM * 4u <= room;
+                    const bool fits = static_cast<uint32_t>(gl - gf) * 16u * BM * 4u <= ring_bytes;
                     if (threadIdx.x == 64)  // acquire: the other CTAs' partials, for the copies
                         ctl->is_last = (got && !*abort_flag && fits && k1 == kb_end &&
                                         ld_acquire_gpu(&a.counters[tile]) == gl - gf) ? 1 : 0;
@@ -402,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        acc * static_cast<uint32_t>(a.n_tile);
-                staged_fixup(a, &tmap_y, ctl, base, ring_bytes, tile, gf, gl, g, gf_second, t_row, threadIdx.x - 64,
-                             m_local, o, o_ok, bias_o, abort_flag);
+                staged_fixup(a, &tmap_y, ctl, base, ring_bytes, out_stage, gi, tile, gf, gl, g, gf_second, t_row,
+                             threadIdx.x - 64, m_local, o, o_ok, bias_o, abort_flag);
             } else if (got) {
                 tc_fence_after();
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -417,6 +426,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     tmem_ld_16(t_row + static_cast<uint32_t>(n0), r);
                     tmem_wait_ld();
+                    if (a.y_tma && CK == 1) {  // a whole tile into Y, or this CTA's partial
+                        float v[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) + (full ? bias_o : 0.0f);
+                        group_store(a, &tmap_y, out_stage, gi, threadIdx.x - 64, m_local, v, full, part, tile, n0);
+                        continue;
+                    }
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int32_t n = n0 + j;
@@ -442,6 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (split) {
                 named_barrier_sync(1, 128);  // this CTA's partials of the tile are written
                 if (threadIdx.x == 64) {
+                    if (a.y_tma) {  // the partial went out by bulk stores: complete them first
+                        bulk_wait_all();
+                        fence_proxy_async();
+                    }
                     int32_t last = 0;
                     if (!*abort_flag) {
                         // release: the partials written before the barrier; acquire: the other
@@ -520,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (acc == 0) acc_phase ^= 1u;
             kb = k1;
         }
+        if (threadIdx.x == 64 && a.y_tma) bulk_wait_all();  // before the staging buffers go away
     }
 
     // ---------------- teardown ----------------
@@ -788,11 +809,14 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     p->cluster_k = linear_cluster_k(p->num_tiles, p->num_kb, num_sms);
     if (p->cluster_k > 1) p->grid = p->num_tiles * p->cluster_k;
     const size_t stage_bytes = kABytes + static_cast<size_t>(p->n_tile) * 128;
-    size_t stages = (kMaxDynSmem - 1024 - sizeof(SmemCtl)) / stage_bytes;
+    // above 16 rows (stream-K), outputs and partials leave in 16-row groups by bulk stores
+    const bool want_y_tma = rows > kLinearMaxFixupRows && p->cluster_k == 1;
+    p->out_stage_bytes = want_y_tma ? static_cast<int32_t>(kOutStageBytes) : 0;
+    size_t stages = (kMaxDynSmem - 1024 - sizeof(SmemCtl) - p->out_stage_bytes) / stage_bytes;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return false;
     p->stages = static_cast<int32_t>(stages);
-    p->smem_bytes = 1024 + stages * stage_bytes + sizeof(SmemCtl);
+    p->smem_bytes = 1024 + stages * stage_bytes + p->out_stage_bytes + sizeof(SmemCtl);
     int32_t cols = 32;
     while (cols < 2 * p->n_tile) cols *= 2;
     p->tmem_cols = cols;
@@ -818,7 +842,7 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     if (!encode_bf16_2d(&p->tmap_w, w, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
                         static_cast<uint64_t>(ldw), BK, BM))
         return false;
-    p->y_tma = (p->owner_fix && encode_out_2d(&p->tmap_y, out, out_bf16, static_cast<uint64_t>(M),
+    p->y_tma = (want_y_tma && encode_out_2d(&p->tmap_y, out, out_bf16, static_cast<uint64_t>(M),
                                               static_cast<uint64_t>(rows), static_cast<uint64_t>(ldo)))
                    ? 1
                    : 0;
@@ -906,6 +930,7 @@ cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
     a.cluster_k = p.cluster_k;
     a.owner_fix = p.owner_fix;
     a.y_tma = p.y_tma;
+    a.out_stage_bytes = p.out_stage_bytes;
     a.partials = p.partials;
     a.counters = p.counters;
     a.status = p.status;

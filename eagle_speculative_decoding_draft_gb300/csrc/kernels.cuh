@@ -84,7 +84,8 @@ struct LinearPlan {
     int32_t defer;     // rows > kLinearMaxFixupRows: a second launch sums the split tiles
     int32_t cluster_k; // > 1: split-K over clusters of this many CTAs per tile, summed on chip
     int32_t owner_fix; // > 16 rows, at most two CTAs per tile: summed in the launch by its owner
-    int32_t y_tma;     // the owner writes Y with TMA stores
+    int32_t y_tma;     // outputs and partials leave by bulk stores (16-row groups)
+    int32_t out_stage_bytes;  // their shared-memory staging
     float *partials;   // [grid][2][n_tile][128]
     int32_t *counters; // [num_tiles], zero before and after
     int32_t *status;
