@@ -806,7 +806,9 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     p->num_tiles = (M + BM - 1) / BM;
     const int64_t total = static_cast<int64_t>(p->num_kb) * p->num_tiles;
     p->grid = static_cast<int32_t>(total < num_sms ? total : num_sms);
-    p->cluster_k = linear_cluster_k(p->num_tiles, p->num_kb, num_sms);
+    // Cluster-K above 16 rows only: up to 16 rows stream-K on every SM is faster (the split-K
+    // sums are small), above it the partials and their sum would cost more than the idle SMs.
+    p->cluster_k = rows > kLinearMaxFixupRows ? linear_cluster_k(p->num_tiles, p->num_kb, num_sms) : 1;
     if (p->cluster_k > 1) p->grid = p->num_tiles * p->cluster_k;
     const size_t stage_bytes = kABytes + static_cast<size_t>(p->n_tile) * 128;
     // above 16 rows (stream-K), outputs and partials leave in 16-row groups by bulk stores
@@ -855,7 +857,7 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
 // Split-K over thread-block clusters when the weight tiles are at most half the SMs: C CTAs per
 // tile (a power of two, at most 8, at least 2 k-blocks each), used only when every cluster of the
 // launch can be resident at once with the largest shared-memory request (checked once per C and
-// device; the choice does not depend on the row count, so neither do the results).
+// device).  Results are bit-identical among launches of 1-16 rows and among launches of 17-256.
 int32_t linear_cluster_k(int32_t num_tiles, int32_t num_kb, int32_t num_sms) {
     int32_t c = 1;
     while (c < 8 && num_tiles * (2 * c) <= num_sms && num_kb >= 2 * (2 * c)) c *= 2;

@@ -72,21 +72,24 @@ def test_linear_within_fp32_bound_of_oracle(dev, M, K, rows, out_bf16):
 
 @pytest.mark.parametrize("M,K", [(4096, 8192), (32000, 4096), (300, 640)])
 def test_linear_split_sums_do_not_depend_on_the_row_count(dev, M, K):
-    """Up to 16 rows the last CTA of a split tile sums the partials; above, a second launch does.
-    Both add the same partials in the same CTA order, so shared rows agree bit for bit, whatever
-    the row count of the launch."""
+    """A row's result depends on the split of the k-blocks only, which is the same for every
+    launch of 1-16 rows (stream-K, the last CTA of a split tile sums the partials) and for every
+    launch of 17-256 rows (cluster-K for few weight tiles, else stream-K with the sum by the
+    tile's owner or a second launch, all adding the same partials in the same CTA order)."""
     from eagle_speculative_decoding_draft_gb300.engine import linear_bf16
     rng = np.random.default_rng(M + K)
     W = bf16_tensor(rng, (M, K), 1 / np.sqrt(K)).to(dev)
     X = bf16_tensor(rng, (256, K), 1.0).to(dev)
     bias = bf16_tensor(rng, (M,), 0.1).to(dev)
     for out_bf16 in (False, True):
+        one = linear_bf16(W, X[:1].contiguous(), bias, out_bf16=out_bf16)
         few = linear_bf16(W, X[:16].contiguous(), bias, out_bf16=out_bf16)
-        more = linear_bf16(W, X[:48].contiguous(), bias, out_bf16=out_bf16)
+        more = linear_bf16(W, X[:17].contiguous(), bias, out_bf16=out_bf16)
         wide = linear_bf16(W, X[:64].contiguous(), bias, out_bf16=out_bf16)
         widest = linear_bf16(W, X, bias, out_bf16=out_bf16)
         torch.cuda.synchronize()
-        assert torch.equal(few, more[:16])
+        assert torch.equal(one, few[:1])
+        assert torch.equal(more, wide[:17])
         assert torch.equal(wide, widest[:64])
 
 
