@@ -39,9 +39,14 @@ def bf16_tensor(rng, shape, std):
 
 
 # Ragged M and K, 1..256 rows (padded to the MMA's N in steps of 16), M below one 128-row tile.
+# Above 16 rows every way of summing split tiles: cluster-K for few tiles ((4096, 8192), (777, 1000):
+# clusters of 8, (70, 4104): one tile, ragged K slices), the owner's fix-up with bulk stores when
+# every CTA covers a whole tile ((20000, 512), (20000, 520) with a ragged last k-block), and the
+# second launch otherwise ((12000, 2048): 94 tiles of 32 k-blocks over 152 CTAs).
 LINEAR_CASES = [(128, 64, 1), (200, 200, 17), (1000, 512, 256), (300, 64, 33), (128, 128, 16),
                 (4096, 8192, 10), (32000, 4096, 10), (777, 1000, 100), (130, 72, 255),
-                (4096, 8192, 256), (300, 64, 64), (513, 1000, 49), (70, 4104, 80), (2000, 2048, 128)]
+                (4096, 8192, 256), (300, 64, 64), (513, 1000, 49), (70, 4104, 80), (2000, 2048, 128),
+                (20000, 512, 40), (20000, 520, 200), (12000, 2048, 24)]
 
 
 @pytest.mark.parametrize("M,K,rows", LINEAR_CASES)
