@@ -8,15 +8,17 @@
 // reads it from memory once, into registers:
 //   pass 1  every thread takes the max of its elements.  The slice max and the slice threshold
 //           (the largest, over warps, of the warp's k-th largest thread max: that warp alone has
-//           k elements >= it) go to the CTA's shared memory; after a cluster barrier every CTA
-//           takes the row max M and the row threshold tau as the max over the cluster.  Every
-//           element of the row's top k is >= tau.
+//           k elements >= it) are pushed into every cluster CTA's shared memory; after a cluster
+//           barrier every CTA takes the row max M and the row threshold tau as the max over the
+//           cluster from its own copy (no remote loads).  Every element of the row's top k is
+//           >= tau.
 //   pass 2  from the registers: sum of exp2((x - M) log2 e) for the logsumexp, and every
-//           element >= tau is appended to a shared candidate list; one warp sorts it with
-//           bitonic networks and keeps the slice's best k.
-//   merge   every CTA stores its sorted list and its sum into rank 0's shared memory; after a
-//           second cluster barrier rank 0 merges the C lists (a tree of pairwise bitonic merges
-//           whose levels run in lockstep) and writes the row's top k and logsumexp.
+//           element >= tau is appended to a shared candidate list; each candidate's rank in
+//           the slice is the number of candidates that rank before it (one thread a candidate,
+//           no sort), and the first k land in rank order.
+//   merge   every CTA pushes its best k and its sum into rank 0's shared memory; after a second
+//           cluster barrier rank 0 ranks the C x k entries the same way and writes the row's
+//           top k and logsumexp.
 // C shrinks when there are many rows, so that the grid fits in about one wave.
 // A slice with more than kCand elements >= tau (massive ties) falls back to k exact block-wide
 // arg-max passes over that slice.
@@ -69,29 +71,6 @@ __device__ __forceinline__ void visit(const T *z, const uint4 (&cache)[kCacheVec
     for (int32_t i = s.sbeg + tid; i < s.send; i += kThreads) f(to_f32(z[i]), i);
 }
 
-// One level of a tree merge of sorted lists held across the warp (lane j = entry j): lists
-// p and p + STEP (p a multiple of 2 STEP, both < C) merge into list p, keeping the best 32.  The
-// merges of a level are independent and run in lockstep.
-template <int STEP>
-__device__ __forceinline__ void merge_level(float (&lv)[kMaxCluster], int32_t (&li)[kMaxCluster], int lane,
-                                            uint32_t C) {
-#pragma unroll
-    for (int p = 0; p + STEP < kMaxCluster; p += 2 * STEP) {
-        if (p + STEP < static_cast<int>(C)) {
-            const float rv = __shfl_sync(kFullMask, lv[p + STEP], 31 - lane);
-            const int32_t ri = __shfl_sync(kFullMask, li[p + STEP], 31 - lane);
-            const bool take = before_nb(rv, ri, lv[p], li[p]);
-            lv[p] = take ? rv : lv[p];
-            li[p] = take ? ri : li[p];
-        }
-    }
-#pragma unroll
-    for (int j = 16; j > 0; j >>= 1)
-#pragma unroll
-        for (int p = 0; p + STEP < kMaxCluster; p += 2 * STEP)
-            if (p + STEP < static_cast<int>(C)) bitonic_step(lv[p], li[p], j, (lane & j) == 0);
-}
-
 // Two CTAs per SM (64 registers a thread), so the CTAs of the next launch fit beside a GEMM CTA.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -105,8 +84,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ float r_v[kWarps];
     __shared__ int32_t r_i[kWarps];
     __shared__ float s_row[2];  // row max and threshold over the cluster
-    // read by the cluster's other CTAs
-    __shared__ float x_stat[2];  // this slice's max and threshold
+    __shared__ float p_stat[kMaxCluster][2];  // every slice's max and threshold, pushed by its CTA
     __shared__ float x_sum;      // this slice's sum of exp relative to the row max
     __shared__ float x_v[16];    // this slice's best k, sorted
     __shared__ int32_t x_i[16];
@@ -151,21 +129,23 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (tid == 0) s_count = 0;
     __syncthreads();
-    if (tid == 0) {
+    if (warp == 0) {
         float m = -INFINITY, t = -INFINITY;
         for (int w = 0; w < kWarps; ++w) {
             m = fmaxf(m, s_max[w]);
             t = fmaxf(t, s_kth[w]);
         }
-        x_stat[0] = m;
-        x_stat[1] = t;
+        if (lane < static_cast<int>(C)) {  // push this slice's stats into CTA `lane`'s copy
+            st_peer_f32(peer_addr(&p_stat[rank][0], lane), m);
+            st_peer_f32(peer_addr(&p_stat[rank][1], lane), t);
+        }
     }
-    cluster_sync();
+    cluster_sync();  // every CTA's stats are in every CTA's p_stat
     if (warp == 0) {
         float m = -INFINITY, t = -INFINITY;
         if (lane < static_cast<int>(C)) {
-            m = ld_peer_f32(peer_addr(&x_stat[0], lane));
-            t = ld_peer_f32(peer_addr(&x_stat[1], lane));
+            m = p_stat[lane][0];
+            t = p_stat[lane][1];
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -206,23 +186,21 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // ---- this slice's best k ----
     if (count <= kCand) {
-        if (warp == 0) {
-            float v = -INFINITY;
-            int32_t i = INT_MAX;
-            for (int32_t b0 = 0; b0 < count; b0 += 32) {
-                float bv = (b0 + lane < count) ? c_v[b0 + lane] : -INFINITY;
-                int32_t bi = (b0 + lane < count) ? c_i[b0 + lane] : INT_MAX;
-                warp_sort(bv, bi, lane);
-                if (b0 == 0) {
-                    v = bv;
-                    i = bi;
-                } else {
-                    warp_merge_sorted(v, i, bv, bi, lane);
-                }
-            }
-            if (lane < 16) {
-                x_v[lane] = v;
-                x_i[lane] = i;
+        // rank of each candidate among the slice's candidates (a strict total order); the first
+        // k go to their rank's slot, unfilled slots keep the (-inf, INT_MAX) sentinel
+        if (tid < 16) {
+            x_v[tid] = -INFINITY;
+            x_i[tid] = INT_MAX;
+        }
+        __syncthreads();
+        if (tid < count) {
+            const float v = c_v[tid];
+            const int32_t i = c_i[tid];
+            int32_t r = 0;
+            for (int32_t j = 0; j < count; ++j) r += before_nb(c_v[j], c_i[j], v, i) ? 1 : 0;
+            if (r < k) {
+                x_v[r] = v;
+                x_i[r] = i;
             }
         }
     } else {
@@ -273,28 +251,30 @@ __global__ void __launch_bounds__(kThreads, 2)
     // After this barrier no CTA touches a peer's shared memory again: rank 0 merges from its own.
     cluster_sync();
 
-    // ---- rank 0 merges the slices' lists: a tree of pairwise merges, levels in lockstep ----
-    if (rank == 0 && warp == 0) {
-        float lv[kMaxCluster];
-        int32_t li[kMaxCluster];
+    // ---- rank 0 ranks the C x k entries of the slices' lists and writes the row's best k ----
+    if (rank == 0) {
+        if (warp == 0) {
+            float tot = (lane < static_cast<int>(C)) ? m_sum[lane] : 0.0f;
 #pragma unroll
-        for (int p = 0; p < kMaxCluster; ++p) {
-            const bool ok = p < static_cast<int>(C) && lane < k;
-            lv[p] = ok ? m_v[p][lane] : -INFINITY;
-            li[p] = ok ? m_i[p][lane] : INT_MAX;
+            for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(kFullMask, tot, off);
+            if (lane == 0) s_sum[0] = want_lse ? M + logf(tot) : 0.0f;
         }
-        float tot = (lane < static_cast<int>(C)) ? m_sum[lane] : 0.0f;
-        merge_level<1>(lv, li, lane, C);
-        merge_level<2>(lv, li, lane, C);
-        merge_level<4>(lv, li, lane, C);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(kFullMask, tot, off);
-        const float lse = want_lse ? M + logf(tot) : 0.0f;
-        if (lane < k) {
-            ids[static_cast<int64_t>(row) * k + lane] = li[0];
-            if (vals) vals[static_cast<int64_t>(row) * k + lane] = want_lse ? lv[0] - lse : lv[0];
+        __syncthreads();
+        const float lse = s_sum[0];
+        const int32_t n = static_cast<int32_t>(C) * k;
+        if (tid < n) {
+            const int32_t p = tid / k, e = tid - p * k;
+            const float v = m_v[p][e];
+            const int32_t i = m_i[p][e];
+            int32_t r = 0;
+            for (int32_t q = 0; q < static_cast<int32_t>(C); ++q)
+                for (int32_t f = 0; f < k; ++f) r += before_nb(m_v[q][f], m_i[q][f], v, i) ? 1 : 0;
+            if (r < k) {  // sentinels rank after the >= k real entries of the row
+                ids[static_cast<int64_t>(row) * k + r] = i;
+                if (vals) vals[static_cast<int64_t>(row) * k + r] = want_lse ? v - lse : v;
+            }
         }
-        if (want_lse && lane == 0) lse_out[row] = lse;
+        if (want_lse && tid == 0) lse_out[row] = lse;
     }
 }
 
