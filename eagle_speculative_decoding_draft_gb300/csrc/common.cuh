@@ -129,12 +129,13 @@ __device__ __forceinline__ float ld_peer_f32(uint32_t a) {
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
     return v;
 }
+// No "memory" clobber: callers order these loads by barriers, and consecutive loads stay free
+// to be in flight together.
 __device__ __forceinline__ float4 ld_peer_v4(uint32_t a) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(a)
-                 : "memory");
+                 : "r"(a));
     return v;
 }
 // Atomic add on a 32-bit word in a cluster CTA's shared memory; returns the old value.

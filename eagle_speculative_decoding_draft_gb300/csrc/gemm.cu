@@ -576,27 +576,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp >= 2 && !*abort_flag) {
             const int32_t et = static_cast<int32_t>(threadIdx.x) - 64;
             const int32_t rank = g % CK, tile = g / CK;
-            const int32_t per = (BM / 4) / CK;  // 4-wide groups of this CTA's share, per row
+            const int32_t share = BM / CK;      // columns of this CTA's share of the tile
+            const int32_t per = share / 4;      // 4-wide groups of it, per row
             const int32_t groups = per * a.rows;
             const float *stage_acc = reinterpret_cast<const float *>(base);
-            constexpr int kUnroll = 4;
+            // with y_tma the sums are assembled behind the staged accumulator ([row][share], Y's
+            // type) and leave by one TMA store
+            uint8_t *out_stage = base + ((static_cast<size_t>(a.n_tile) * BM * 4 + 1023) & ~static_cast<size_t>(1023));
+            constexpr int kUnroll = 8;
             for (int32_t e0 = et; e0 < groups; e0 += 128 * kUnroll) {
+                // peer by peer (rank order), the loads of all kUnroll groups in flight together
                 float4 sum[kUnroll];
+                for (int32_t c = 0; c < CK; ++c) {
+                    float4 v[kUnroll];
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int32_t e = e0 + u * 128;
-                    const int32_t n = e / per, m4 = (rank * per + e % per) * 4;
-#pragma unroll 1
-                    for (int32_t c = 0; c < CK; ++c) {
-                        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                        if (e < groups) v = ld_peer_v4(peer_addr(stage_acc + static_cast<size_t>(n) * BM + m4, c));
+                    for (int u = 0; u < kUnroll; ++u) {
+                        const int32_t e = e0 + u * 128;
+                        const int32_t n = e / per, m4 = rank * share + (e % per) * 4;
+                        v[u] = (e < groups) ? ld_peer_v4(peer_addr(stage_acc + static_cast<size_t>(n) * BM + m4, c))
+                                            : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kUnroll; ++u) {
                         if (c == 0) {
-                            sum[u] = v;
+                            sum[u] = v[u];
                         } else {
-                            sum[u].x += v.x;
-                            sum[u].y += v.y;
-                            sum[u].z += v.z;
-                            sum[u].w += v.w;
+                            sum[u].x += v[u].x;
+                            sum[u].y += v[u].y;
+                            sum[u].z += v[u].z;
+                            sum[u].w += v[u].w;
                         }
                     }
                 }
@@ -604,13 +612,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int u = 0; u < kUnroll; ++u) {
                     const int32_t e = e0 + u * 128;
                     if (e >= groups) continue;
-                    const int32_t n = e / per, m4 = (rank * per + e % per) * 4;
-                    const float v[4] = {sum[u].x, sum[u].y, sum[u].z, sum[u].w};
+                    const int32_t n = e / per, q4 = (e % per) * 4, m4 = rank * share + q4;
+                    float v[4] = {sum[u].x, sum[u].y, sum[u].z, sum[u].w};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int32_t o = tile * BM + m4 + q;
-                        if (o < a.M) store_y(a, n, o, v[q] + (a.bias != nullptr ? __bfloat162float(a.bias[o]) : 0.0f));
+                        v[q] += (a.bias != nullptr && o < a.M) ? __bfloat162float(a.bias[o]) : 0.0f;
                     }
+                    if (a.y_tma) {
+                        const size_t at = static_cast<size_t>(n) * share + q4;
+                        if (a.out_bf16) {
+                            __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(
+                                reinterpret_cast<__nv_bfloat16 *>(out_stage) + at);
+                            ob[0] = __floats2bfloat162_rn(v[0], v[1]);
+                            ob[1] = __floats2bfloat162_rn(v[2], v[3]);
+                        } else {
+                            *reinterpret_cast<float4 *>(reinterpret_cast<float *>(out_stage) + at) =
+                                make_float4(v[0], v[1], v[2], v[3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (tile * BM + m4 + q < a.M) store_y(a, n, tile * BM + m4 + q, v[q]);
+                    }
+                }
+            }
+            if (a.y_tma) {
+                fence_proxy_async_smem();  // the writes above, before the TMA store reads them
+                named_barrier_sync(1, 128);
+                if (et == 0) {  // rows >= rows and columns >= M fall outside the tensor map
+                    tma_store_2d(&tmap_y, out_stage, tile * BM + rank * share, 0);
+                    bulk_commit();
+                    bulk_wait_all();
                 }
             }
         }
@@ -762,9 +795,9 @@ bool encode_bf16_2d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Y [rows][ldo] (fp32 or bf16) for TMA stores of {128 columns, 16 rows}, no swizzle.
+// Y [rows][ldo] (fp32 or bf16) for TMA stores of {box_cols columns, box_rows rows}, no swizzle.
 bool encode_out_2d(CUtensorMap *map, const void *ptr, int32_t out_bf16, uint64_t inner, uint64_t outer,
-                   uint64_t row_stride_elems) {
+                   uint64_t row_stride_elems, uint32_t box_cols, uint32_t box_rows) {
     EncodeTiledFn fn = encoder();
     if (!fn) return false;
     const uint64_t es = out_bf16 ? 2 : 4;
@@ -772,12 +805,22 @@ bool encode_out_2d(CUtensorMap *map, const void *ptr, int32_t out_bf16, uint64_t
     if ((row_stride_elems * es) % 16 != 0) return false;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {row_stride_elems * es};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(BM), 16};
+    if ((box_cols * es) % 16 != 0 || box_cols > 256 || box_rows > 256 || box_rows < 1) return false;
+    cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
               const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The output map of a plan: {128, 16} boxes for the stream-K epilogue's 16-row groups, or one box
+// of {128 / C columns, n_tile rows} for a cluster-K CTA's share of its tile.
+bool encode_plan_out(LinearPlan *p, const void *out) {
+    const bool ck = p->cluster_k > 1;
+    return encode_out_2d(&p->tmap_y, out, p->out_bf16, static_cast<uint64_t>(p->M), static_cast<uint64_t>(p->rows),
+                         static_cast<uint64_t>(p->ldo), ck ? static_cast<uint32_t>(BM / p->cluster_k) : BM,
+                         ck ? static_cast<uint32_t>(p->n_tile) : 16u);
 }
 
 }  // namespace
@@ -844,10 +887,13 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     if (!encode_bf16_2d(&p->tmap_w, w, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
                         static_cast<uint64_t>(ldw), BK, BM))
         return false;
-    p->y_tma = (want_y_tma && encode_out_2d(&p->tmap_y, out, out_bf16, static_cast<uint64_t>(M),
-                                              static_cast<uint64_t>(rows), static_cast<uint64_t>(ldo)))
-                   ? 1
-                   : 0;
+    // cluster-K writes each CTA's share of its tile with one TMA store from the idle ring, behind
+    // the staged accumulator (n_tile rows x 128 fp32) when both fit
+    const size_t ck_out = static_cast<size_t>(p->n_tile) * (BM / p->cluster_k) * (out_bf16 ? 2 : 4);
+    const bool ck_tma = p->cluster_k > 1 &&
+                        ((static_cast<size_t>(p->n_tile) * BM * 4 + 1023) & ~static_cast<size_t>(1023)) + ck_out <=
+                            stages * stage_bytes;
+    p->y_tma = ((want_y_tma || ck_tma) && encode_plan_out(p, out)) ? 1 : 0;
     if (!encode_bf16_2d(&p->tmap_x, x, static_cast<uint64_t>(K), static_cast<uint64_t>(rows),
                         static_cast<uint64_t>(ldx), BK, static_cast<uint32_t>(p->n_tile)))
         return false;
@@ -907,11 +953,7 @@ cudaError_t prepare_kernels() {
 
 void linear_retarget_out(LinearPlan *p, void *out) {
     p->out = out;
-    if (p->y_tma)
-        p->y_tma = encode_out_2d(&p->tmap_y, out, p->out_bf16, static_cast<uint64_t>(p->M),
-                                 static_cast<uint64_t>(p->rows), static_cast<uint64_t>(p->ldo))
-                       ? 1
-                       : 0;
+    if (p->y_tma) p->y_tma = encode_plan_out(p, out) ? 1 : 0;
 }
 
 cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
