@@ -20,6 +20,8 @@
 //           cluster barrier rank 0 ranks the C x k entries the same way and writes the row's
 //           top k and logsumexp.
 // C shrinks when there are many rows, so that the grid fits in about one wave.
+// k = 1 without the logsumexp (greedy verification's arg-max) takes a short path: the slices' best
+// entries go to rank 0 and one cluster barrier separates them from the result.
 // A slice with more than kCand elements >= tau (massive ties) falls back to k exact block-wide
 // arg-max passes over that slice.
 #include <cfloat>
@@ -115,6 +117,45 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int u = 0; u < kCacheVec; ++u) {
         const int32_t c = sl.vbeg + tid + u * kThreads;
         cache[u] = (c < sl.vend) ? __ldg(reinterpret_cast<const uint4 *>(z) + c) : make_uint4(0, 0, 0, 0);
+    }
+
+    if (k == 1 && !want_lse) {
+        // Arg-max only (greedy verification): the slice's best (value desc, id asc) by thread, warp
+        // and block, pushed into rank 0, which takes the best of the C after one cluster barrier.
+        float bv = -INFINITY;
+        int32_t bi = INT_MAX;
+        visit(z, cache, sl, tid, [&](float x, int32_t id) {
+            if (before_nb(x, id, bv, bi)) {
+                bv = x;
+                bi = id;
+            }
+        });
+        warp_best(bv, bi);
+        if (lane == 0) {
+            r_v[warp] = bv;
+            r_i[warp] = bi;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            float v = (lane < kWarps) ? r_v[lane] : -INFINITY;
+            int32_t i = (lane < kWarps) ? r_i[lane] : INT_MAX;
+            warp_best(v, i);
+            if (lane == 0) {
+                st_peer_f32(peer_addr(&m_v[rank][0], 0), v);
+                st_peer_s32(peer_addr(&m_i[rank][0], 0), i);
+            }
+        }
+        cluster_sync();
+        if (rank == 0 && warp == 0) {
+            float v = (lane < static_cast<int>(C)) ? m_v[lane][0] : -INFINITY;
+            int32_t i = (lane < static_cast<int>(C)) ? m_i[lane][0] : INT_MAX;
+            warp_best(v, i);
+            if (lane == 0) {
+                ids[row] = i;
+                if (vals) vals[row] = v;
+            }
+        }
+        return;
     }
 
     // ---- pass 1: thread max; slice max and threshold; row max and threshold ----
