@@ -90,14 +90,27 @@ __global__ void __launch_bounds__(kExpandThreads) expand_kernel(const ExpandArgs
     const uint8_t *fh = reinterpret_cast<const uint8_t *>(a.fhat);
     const uint8_t *em = reinterpret_cast<const uint8_t *>(a.emb);
     uint8_t *xo = reinterpret_cast<uint8_t *>(a.x_next);
-    for (int32_t i = blockIdx.y * kExpandThreads + t; i < k * vpr; i += gridDim.y * kExpandThreads) {
-        const int32_t sp = i / vpr, off = i - (i / vpr) * vpr;
-        const int32_t src = slot[sp];
-        const uint4 *from = (off < vh)
-            ? reinterpret_cast<const uint4 *>(fh + static_cast<int64_t>(sRow[src]) * a.h * eb) + off
-            : reinterpret_cast<const uint4 *>(em + static_cast<int64_t>(sTok[src]) * a.h * eb) + (off - vh);
-        uint4 *to = reinterpret_cast<uint4 *>(xo + static_cast<int64_t>(b * k + sp) * 2 * a.h * eb) + off;
-        *to = __ldg(from);
+    // two vectors a thread and step, both loads issued before either store
+    const int32_t nv = k * vpr, stride = gridDim.y * kExpandThreads;
+    for (int32_t i0 = blockIdx.y * kExpandThreads + t; i0 < nv; i0 += 2 * stride) {
+        uint4 v[2];
+        uint4 *to[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int32_t i = i0 + u * stride;
+            to[u] = nullptr;
+            if (i >= nv) continue;
+            const int32_t sp = i / vpr, off = i - sp * vpr;
+            const int32_t src = slot[sp];
+            const uint4 *from = (off < vh)
+                ? reinterpret_cast<const uint4 *>(fh + static_cast<int64_t>(sRow[src]) * a.h * eb) + off
+                : reinterpret_cast<const uint4 *>(em + static_cast<int64_t>(sTok[src]) * a.h * eb) + (off - vh);
+            to[u] = reinterpret_cast<uint4 *>(xo + static_cast<int64_t>(b * k + sp) * 2 * a.h * eb) + off;
+            v[u] = __ldg(from);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+            if (to[u]) *to[u] = v[u];
     }
 }
 
