@@ -64,7 +64,20 @@ __device__ __forceinline__ void visit(const T *z, const uint4 (&cache)[kCacheVec
             for (int j = 0; j < EPV; ++j) f(to_f32(e[j]), c * EPV + j);
         }
     }
-    for (int32_t c = s.vbeg + kCacheVec * kThreads + tid; c < s.vend; c += kThreads) {
+    // long rows: four vectors a thread and step, all loaded before any is used (same order of f)
+    int32_t c = s.vbeg + kCacheVec * kThreads + tid;
+    for (; c + 3 * kThreads < s.vend; c += 4 * kThreads) {
+        uint4 raw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) raw[u] = __ldg(reinterpret_cast<const uint4 *>(z) + c + u * kThreads);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const T *e = reinterpret_cast<const T *>(&raw[u]);
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) f(to_f32(e[j]), (c + u * kThreads) * EPV + j);
+        }
+    }
+    for (; c < s.vend; c += kThreads) {
         const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(z) + c);
         const T *e = reinterpret_cast<const T *>(&raw);
 #pragma unroll
