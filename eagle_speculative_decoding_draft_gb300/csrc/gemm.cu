@@ -14,14 +14,21 @@
 //               and write Y[r][o] coalesced along o (+ bias, rounding to bf16 for the FC);
 //   stream-K    all k-blocks of all tiles are one sequence split evenly over one CTA per SM, so
 //               every SM streams the same number of weight bytes whatever the tile count; a tile
-//               cut between CTAs is summed by the last CTA to arrive (atomic ticket, no waiting),
-//               which adds the partials in ascending CTA order so results are deterministic;
-//   cluster-K   when the weight tiles are few (at most half the SMs: the FC, M = h), the grid is
-//               tiles x C CTAs in thread-block clusters of C; CTA r of a cluster takes the r-th
-//               slice of the tile's k-blocks, stages its fp32 accumulator in its own (then idle)
-//               ring, and after a cluster barrier sums a 1/C share of the tile's outputs over the
-//               C CTAs in rank order through distributed shared memory: no partials in global
-//               memory, no tickets, no second launch.
+//               cut between CTAs is summed in ascending CTA order, so results are deterministic:
+//               up to 16 rows by the last CTA to arrive (atomic ticket, no waiting); above, when
+//               every CTA covers a whole tile, by the CTA that reaches the tile at the end of its
+//               range and finds its partner's ticket in (the partner's partial bulk-copied into
+//               its idle ring, its own values straight from TMEM), else by a second launch;
+//   bulk stores above 16 rows every 16-row group of outputs or partials is assembled in shared
+//               memory and leaves by one bulk store (TMA tensor store into Y, 1-D bulk store of
+//               partials) instead of per-thread stores to rows far apart;
+//   cluster-K   above 16 rows, when the weight tiles are few (at most half the SMs: the FC,
+//               M = h), the grid is tiles x C CTAs in thread-block clusters of C; CTA r of a
+//               cluster takes the r-th slice of the tile's k-blocks, stages its fp32 accumulator
+//               in its own (then idle) ring, and after a cluster barrier sums a 1/C share of the
+//               tile's outputs over the C CTAs in rank order through distributed shared memory,
+//               written by one TMA store: no partials in global memory, no tickets, no second
+//               launch.
 #include <cstdio>
 #include <mutex>
 

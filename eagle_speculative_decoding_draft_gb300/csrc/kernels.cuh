@@ -63,8 +63,10 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
 //   Y[r][o] = sum_i W[o][i] * X[r][i] (+ bias[o]),  r < rows, o < M
 // The weight matrix is cut into 128-row tiles and 64-wide k-blocks; the k-blocks of all tiles
 // form one stream that is split evenly over a persistent grid (one CTA per SM).  A tile whose
-// k-blocks land in more than one CTA is finished by the last CTA to arrive, which adds the
-// partial sums in ascending CTA order (deterministic).
+// k-blocks land in more than one CTA is summed in ascending CTA order (deterministic) by the last
+// CTA to arrive, by the CTA that finds its partner done, or by a second launch; few-tile GEMMs
+// above 16 rows split each tile's k-blocks over a thread-block cluster and sum on chip instead.
+// A row's result is bit-identical among launches of 1-16 rows and among launches of 17-256.
 // ---------------------------------------------------------------------------------------------
 constexpr int kLinearTileM = 128;
 constexpr int kLinearTileK = 64;
