@@ -493,7 +493,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int32_t oq = tile * BM + m4 + q;
                         b4[q] = (a.bias != nullptr && oq < a.M) ? __bfloat162float(a.bias[oq]) : 0.0f;
                     }
-                    constexpr int kRowsPerBatch = 2, kCtasPerBatch = 8;  // per thread
+                    // 4 rows x 6 CTAs a thread and batch: up to 16 rows all in one batch, so a
+                    // tile shared by up to 6 CTAs costs one round trip of loads
+                    constexpr int kRowsPerBatch = 4, kCtasPerBatch = 6;  // per thread
                     for (int32_t n0 = rsub; n0 < a.rows; n0 += 4 * kRowsPerBatch) {
                         float4 sum[kRowsPerBatch];
                         for (int32_t g0 = gf; g0 <= gl; g0 += kCtasPerBatch) {
