@@ -55,33 +55,35 @@ __device__ __forceinline__ void online(float &m, float &s, float x) {
     }
 }
 
-// Cluster-wide reductions.  Each exchange goes through slot `ph` of the CTA's `xch` array and
-// flips `ph`, so a slot is written again only after every peer has passed the barrier of the
-// exchange that follows its last read.
+// Cluster-wide reductions.  Each CTA pushes its values into slot `ph` of every cluster CTA's
+// inbox before the barrier, and after it reads all of them from its own shared memory (no remote
+// loads); `ph` flips, so a slot is written again only after every CTA has passed the barrier of
+// the exchange that follows its last read of it.
 struct Cluster {
     uint32_t C, rank;
     int ph;
-    float *red;           // kWarps floats (block partials)
-    float (*xch)[4];      // [2][4]: values this CTA publishes
-    float *bc;            // 4 floats: broadcast of the cluster result inside the CTA
+    float *red;                      // kWarps floats (block partials)
+    float (*inbox)[kMaxCluster][4];  // [2][C][4]: the values of every cluster CTA, by rank
+    float *bc;                       // 4 floats: broadcast of the cluster result inside the CTA
 
     // Publishes up to 4 block-level values, then every thread returns the cluster result:
     // kind 0: sum of v[0]; kind 1: lse merge of (v[0], v[1]) and of (v[2], v[3]);
     // kind 2: (sum v0 in rank order, exclusive prefix of v0 before this rank, min v1, max v2).
+    // v must hold the same values in every thread of the CTA.
     __device__ void exchange(const float (&v)[4], int kind, float (&out)[4]) {
         const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-        if (tid == 0) {
+        if (tid < static_cast<int>(C)) {  // thread p pushes this CTA's values into CTA p's inbox
 #pragma unroll
-            for (int i = 0; i < 4; ++i) xch[ph][i] = v[i];
+            for (int i = 0; i < 4; ++i) st_peer_f32(peer_addr(&inbox[ph][rank][i], tid), v[i]);
         }
         cluster_sync();
         if (warp == 0) {
             float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
             if (lane < static_cast<int>(C)) {
-                a0 = ld_peer_f32(peer_addr(&xch[ph][0], lane));
-                a1 = ld_peer_f32(peer_addr(&xch[ph][1], lane));
-                a2 = ld_peer_f32(peer_addr(&xch[ph][2], lane));
-                a3 = ld_peer_f32(peer_addr(&xch[ph][3], lane));
+                a0 = inbox[ph][lane][0];
+                a1 = inbox[ph][lane][1];
+                a2 = inbox[ph][lane][2];
+                a3 = inbox[ph][lane][3];
             }
             // combination over ranks 0..C-1 in a fixed order, identical on every CTA
             float o0 = 0.0f, o1 = 0.0f, o2 = 0.0f, o3 = 0.0f;
@@ -138,13 +140,13 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 __global__ void __launch_bounds__(kThreads) verify_sample_kernel(const SampleArgs a) {
     __shared__ float red[kWarps], redm[kWarps], reds[kWarps];
     __shared__ int32_t redi[kWarps];
-    __shared__ float xch[2][4];
+    __shared__ float inbox[2][kMaxCluster][4];
     __shared__ float bc[4];
     __shared__ int32_t kids[kMaxCandidates + 1];
     __shared__ int32_t s_nk;
     pdl_launch_dependents();  // dependents still wait for this grid to finish
     pdl_wait();
-    Cluster cl{cluster_size(), cluster_rank(), 0, red, xch, bc};
+    Cluster cl{cluster_size(), cluster_rank(), 0, red, inbox, bc};
     const int32_t b = blockIdx.x / cl.C, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t n = a.n, V = a.V;
     // this CTA's slice of the vocabulary
