@@ -166,7 +166,10 @@ def small_tree(dtype="bf16", B=3, d=4, k=3, m=12, h=32, V=300, seed=5):
 
 
 @pytest.mark.parametrize("B,d,k,m", [(3, 4, 3, 12), (2, 6, 10, 60), (5, 5, 4, 7), (4, 3, 1, 3),
-                                     (2, 5, 16, 100), (1, 1, 4, 4)])
+                                     (2, 5, 16, 100), (1, 1, 4, 4),
+                                     # the largest pools: 3856 candidates kept whole (3857 nodes,
+                                     # 121 mask words), the deepest tree, a 32-level chain
+                                     (2, 16, 16, 3856), (2, 32, 11, 3762), (2, 32, 11, 500), (1, 32, 1, 32)])
 def test_expand_and_build_are_bit_exact_on_oracle_inputs(dev, B, d, k, m):
     from eagle_speculative_decoding_draft_gb300.engine import build_tree, expand
     w, inp, ref = small_tree(B=B, d=d, k=k, m=m, V=max(300, k + 1), seed=B + d + k)

@@ -139,6 +139,9 @@ EDGE = [
     dict(h=32, V=300, B=3, d=4, k=3, m=12, dtype="f32"),
     dict(h=256, V=1024, B=5, d=3, k=16, m=40, dtype="f32"),
     dict(h=64, V=257, B=1, d=2, k=16, m=272, dtype="bf16"),    # k = 16, m = n_cand
+    dict(h=64, V=300, B=2, d=16, k=16, m=3856, dtype="f32"),   # largest pool kept whole: 3857 nodes
+    dict(h=64, V=400, B=2, d=32, k=11, m=1000, dtype="f32"),   # maximum depth
+    dict(h=64, V=300, B=2, d=32, k=1, m=32, dtype="bf16"),     # 32-level chain
 ]
 
 

@@ -107,7 +107,8 @@ def random_forest(rng, B, n, k_max, V):
 @pytest.mark.parametrize("B,n,V,temp,mode", [(8, 12, 100, 1.0, 0), (6, 40, 1000, 0.7, 0),
                                              (4, 61, 32000, 1.0, 0), (3, 30, 5000, 2.0, 1),
                                              (16, 5, 17, 1.0, 0), (2, 65, 128256, 1.0, 0),
-                                             (5, 9, 2049, 1.3, 1)])
+                                             (5, 9, 2049, 1.3, 1),
+                                             (1, 4097, 64, 1.0, 0)])  # the largest tree the call takes
 def test_random_trees_match_the_oracle(dev, B, n, V, temp, mode):
     rng = np.random.default_rng(B * 1000 + n * 10 + V)
     tok, par, depth = random_forest(rng, B, n, 4, V)

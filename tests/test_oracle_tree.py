@@ -143,6 +143,8 @@ PROP_CASES = [
     dict(h=32, V=2000, B=2, d=6, k=10, m=60, dtype="bf16"),
     dict(h=48, V=700, B=2, d=5, k=8, m=64, dtype="f32"),
     dict(h=16, V=100, B=4, d=3, k=2, m=6, dtype="f32"),
+    dict(h=16, V=300, B=1, d=16, k=16, m=600, dtype="bf16"),  # 3856 candidates, near the 4096 cap
+    dict(h=16, V=100, B=1, d=32, k=11, m=300, dtype="f32"),   # the deepest tree the API takes
 ]
 
 
