@@ -103,6 +103,8 @@ CASES = [
     (1, 1, 0, 128, 2, 2, 128, 256, 0),      # a lone root, no cache, MHA, D = 128
     (3, 40, 70, 192, 3, 1, 32, 320, 6),     # two mask words, MQA, ragged everywhere
     (4, 80, 5, 256, 4, 4, 64, 384, 6),      # 320 rows: two GEMM row chunks, deferred split-K sums
+    (40, 4, 300, 128, 8, 8, 128, 256, 3),   # 16 query rows a CTA, D = 128, 5 key tiles each (no key split)
+    (2, 8, 700, 128, 2, 2, 128, 256, 4),    # the same rows split over the keys: runs of 2 tiles
 ]
 
 
