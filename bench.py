@@ -61,6 +61,49 @@ def dist_env():
     return world, rank, local
 
 
+class Ranks:
+    """The ranks of one run, from torchrun's environment (a single rank without it): a barrier,
+    the max and the sum over ranks of a host number, and whole-job throughput.  Requests are
+    independent, so every rank runs its own replica on its own inputs and nothing on the data
+    path is exchanged; these reductions only combine the timings and counts."""
+
+    def __init__(self, backend: str, device):
+        self.world, self.rank, self.local = dist_env()
+        self.device = device
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def _reduce(self, x: float, op_name: str) -> float:
+        if self.dist is None:
+            return float(x)
+        import torch
+        t = torch.tensor([float(x)], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=getattr(self.dist.ReduceOp, op_name))
+        return float(t.item())
+
+    def max(self, x: float) -> float:
+        return self._reduce(x, "MAX")
+
+    def sum(self, x: float) -> float:
+        return self._reduce(x, "SUM")
+
+    def throughput(self, units: float, seconds: float) -> float:
+        """The units all ranks processed over the slowest rank's time."""
+        return self.sum(units) / self.max(seconds)
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+            self.dist = None
+
+
 def kernel_hash() -> str:
     """Hash of the GEMM's source code with comments and blank lines left out, so that the ncu
     counters recorded for it stay attached until the code itself changes."""
@@ -380,30 +423,10 @@ def run_eagle(args, w):
     from eagle_speculative_decoding_draft_gb300.engine import EagleTree
 
     world, rank, local = dist_env()
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
-    def max_over_ranks(x: float) -> float:
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    def sum_over_ranks(x: float) -> float:
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t)
-        return float(t.item())
+    ranks = Ranks("nccl", dev)
+    barrier = ranks.barrier
 
     inp = synth.make_inputs(w)
     g = lambda t: t.to(dev).contiguous()
@@ -470,8 +493,8 @@ def run_eagle(args, w):
     gemm_bytes = sum(e["bytes"] for e in plist)
     eng.profile(0)
     eng.status()
-    ms_max = max_over_ranks(ms)
-    value = world * K / (ms_max / 1e3)
+    ms_max = ranks.max(ms)
+    value = ranks.throughput(K, ms / 1e3)
 
     accept = []
     for i in range(N_INPUT_SETS):
@@ -497,7 +520,7 @@ def run_eagle(args, w):
     for i in range(E):
         f, t, T = hsets[i % N_INPUT_SETS]
         eng.step_host(f, t, T, staging, hout)
-    e2e_s = max_over_ranks(time.perf_counter() - t0)
+    e2e_value = ranks.throughput(E, time.perf_counter() - t0)
     barrier()
     f, t, T = hsets[0]
     h2d = f.numel() * f.element_size() + t.numel() * 4 + T.numel() * T.element_size()
@@ -625,11 +648,11 @@ def run_eagle(args, w):
                      "tensor_peak": tpeak,
                      "tensor_peak_source": f"{tpeak_kind} bf16_tflops_sustained"},
         "clocks": clocks.summary(),
-        "e2e": {"value": world * E / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "how": "eagle_tree_step_host per step: pinned host inputs and target logits "
                        "copied in, tree and verify results copied out, stream synchronised"},
-        "gpu_launches": int(sum_over_ranks(launches)),
+        "gpu_launches": int(ranks.sum(launches)),
         "round_with_extend": {"value": 1e3 / round_ms, "unit": "rounds/s", "ms_per_round": round_ms,
                               "rounds": ROUNDS,
                               "how": "eagle_draft_extend from the previous verify (FC over every "
@@ -651,8 +674,7 @@ def run_eagle(args, w):
     if rank == 0:
         print(json.dumps(line), flush=True)
     eng.close()
-    if dist is not None:
-        dist.destroy_process_group()
+    ranks.close()
 
 
 def main():
