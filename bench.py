@@ -556,6 +556,23 @@ def run_eagle(args, w):
     sample_us = s0.elapsed_time(s1) * 1e3 / S_CALLS
     sample_accept = float(torch.stack(sacc).float().mean().item())
 
+    # ---------------- greedy verification alone ----------------
+    # The arg-max over every tree node's target logits and the walk, on the tree of input set 0,
+    # cycling over the input sets' target logits (at the Llama-3-8B vocabulary they are 1.07 GB
+    # each, far beyond L2; the smaller shapes' 4 sets stay in L2).  CUDA events, G_CALLS calls.
+    G_CALLS = 50
+    for i in range(3):
+        eng.verify_greedy(tree_out["tokens"], tree_out["parents"], sets[i % N_INPUT_SETS][2], None, ver_out)
+    torch.cuda.synchronize()
+    s0.record()
+    for i in range(G_CALLS):
+        eng.verify_greedy(tree_out["tokens"], tree_out["parents"], sets[i % N_INPUT_SETS][2], None, ver_out)
+    s1.record()
+    torch.cuda.synchronize()
+    greedy_us = s0.elapsed_time(s1) * 1e3 / G_CALLS
+    greedy_bytes = float(T0.numel() * T0.element_size())
+    in_l2 = N_INPUT_SETS * greedy_bytes <= 96e6
+
     # ---------------- the multi-round loop with draft extend ----------------
     # Steady state of decoding: each round starts from the previous verify through
     # eagle_draft_extend (the FC over every verified position, then level 0 of the next tree),
@@ -668,6 +685,14 @@ def run_eagle(args, w):
                                    "every node, p = the synthetic target; CUDA events, "
                                    f"{S_CALLS} calls"},
         "draft_decoder_layer": dec_fig,
+        "greedy_verify": {"us_per_call": greedy_us, "target_logit_bytes": greedy_bytes,
+                          "achieved_gbs": greedy_bytes / (greedy_us * 1e-6) / 1e9,
+                          "frac_of_hbm": greedy_bytes / (greedy_us * 1e-6) / 1e9 / peak,
+                          "target_logits_in_l2": in_l2,
+                          "how": "eagle_verify_greedy (arg-max over the B x (m+1) x V target logits, "
+                                 "then the walk) on the step's tree, alone; CUDA events, "
+                                 f"{G_CALLS} calls over {N_INPUT_SETS} target sets; bytes = the "
+                                 "target logits read"},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
