@@ -164,6 +164,33 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Key tile t of (request b, kv head hk) into `stage`: rows of K and V, cached positions first,
+// then the tree nodes' rotated keys and values from the qkv rows; zero rows past the last key.
+template <int D>
+__device__ __forceinline__ void attn_load_tile(const AttnArgs &a, __nv_bfloat16 *sKV, int32_t t, int32_t stage,
+                                               int32_t b, int32_t hk, int32_t total) {
+    constexpr int kRow = AttnShape<D>::kRow, kChunks = AttnShape<D>::kChunks;
+    __nv_bfloat16 *sK = sKV + (2 * stage) * kAttnKeys * kRow, *sV = sK + kAttnKeys * kRow;
+    for (int32_t c = threadIdx.x; c < kAttnKeys * kChunks; c += blockDim.x) {
+        const int32_t j = c / kChunks, ch = c - j * kChunks, key = t * kAttnKeys + j;
+        const __nv_bfloat16 *kp = a.qkv, *vp = a.qkv;
+        bool ok = true;
+        if (key < a.P) {
+            const int64_t off = ((static_cast<int64_t>(b) * a.P + key) * a.Hk + hk) * D + ch * 8;
+            kp = a.k_cache + off;
+            vp = a.v_cache + off;
+        } else if (key < total) {
+            const int64_t row = static_cast<int64_t>(b) * a.n + (key - a.P);
+            kp = a.qkv + row * a.nqkv + (a.H + hk) * D + ch * 8;
+            vp = a.qkv + row * a.nqkv + (a.H + a.Hk + hk) * D + ch * 8;
+        } else {
+            ok = false;  // past the last key: zero rows (finite values for the P V product)
+        }
+        cp_async16(sK + j * kRow + ch * 8, kp, ok);
+        cp_async16(sV + j * kRow + ch * 8, vp, ok);
+    }
+}
+
 template <int D, int KW>
 __global__ void __launch_bounds__(kAttnMaxWarps * 32, 2) tree_attention_kernel(const AttnArgs a) {
     using S = AttnShape<D>;
@@ -191,27 +218,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 2) tree_attention_kernel(c
         const __nv_bfloat16 *src = a.qkv + static_cast<int64_t>(b * a.n + i) * a.nqkv + (hk * a.group + g) * D + ch * 8;
         cp_async16(sQ + r * kRow + ch * 8, src, ok);
     }
-    auto load_tile = [&](int32_t t, int32_t stage) {
-        __nv_bfloat16 *sK = sKV + (2 * stage) * kAttnKeys * kRow, *sV = sK + kAttnKeys * kRow;
-        for (int32_t c = threadIdx.x; c < kAttnKeys * kChunks; c += nthreads) {
-            const int32_t j = c / kChunks, ch = c - j * kChunks, key = t * kAttnKeys + j;
-            const __nv_bfloat16 *kp = a.qkv, *vp = a.qkv;
-            bool ok = true;
-            if (key < a.P) {
-                const int64_t off = ((static_cast<int64_t>(b) * a.P + key) * a.Hk + hk) * D + ch * 8;
-                kp = a.k_cache + off;
-                vp = a.v_cache + off;
-            } else if (key < total) {
-                const int64_t row = static_cast<int64_t>(b) * a.n + (key - a.P);
-                kp = a.qkv + row * a.nqkv + (a.H + hk) * D + ch * 8;
-                vp = a.qkv + row * a.nqkv + (a.H + a.Hk + hk) * D + ch * 8;
-            } else {
-                ok = false;  // past the last key: zero rows (finite values for the P V product)
-            }
-            cp_async16(sK + j * kRow + ch * 8, kp, ok);
-            cp_async16(sV + j * kRow + ch * 8, vp, ok);
-        }
-    };
+    auto load_tile = [&](int32_t t, int32_t stage) { attn_load_tile<D>(a, sKV, t, stage, b, hk, total); };
     load_tile(t_begin, 0);
     cp_async_commit();
 
@@ -413,6 +420,228 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 2) tree_attention_kernel(c
     }
 }
 
+// Few-query tree attention: at most 8 query rows per (request, kv head), e.g. one node per tree
+// level and one query head per kv head.  The scores are formed transposed, S^T = K Q^T, with the 16
+// keys of a warp's slice of the tile on the MMA's M side and the query rows on N = 8, and the
+// output as O^T = V^T P^T with the head dims on M: no MMA row is padding, half the MMAs of the
+// 16-row form.  A warp's probabilities move from the accumulator layout (key rows) to the
+// B-operand layout (query columns) through a small shared-memory tile.  Tiles, stages, masking,
+// the online softmax, the hi/lo split of P and the outputs are those of tree_attention_kernel.
+constexpr int kFewWarps = 4;      // key slices of 16 keys per 64-key tile
+constexpr int kFewPStride = 20;   // floats per row of the probability transpose: no bank conflicts
+
+template <int D>
+__global__ void __launch_bounds__(kFewWarps * 32, 3) tree_attention_few_kernel(const AttnArgs a) {
+    using S = AttnShape<D>;
+    constexpr int kRow = S::kRow, kChunks = S::kChunks, kKS = D / 16, kMT = D / 16;
+    extern __shared__ __align__(16) uint8_t attn_smem[];
+    __shared__ __align__(16) float sP[kFewWarps][8][kFewPStride];
+    __nv_bfloat16 *sQ = reinterpret_cast<__nv_bfloat16 *>(attn_smem);  // 16 rows, the first Mq live
+    __nv_bfloat16 *sKV = sQ + 16 * kRow;
+    pdl_launch_dependents();  // dependents still wait for this grid to finish
+    pdl_wait();
+    const int32_t ks = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t pair = blockIdx.x;  // one query tile
+    const int32_t b = pair / a.Hk, hk = pair - b * a.Hk;
+    const int32_t total = a.P + a.n, num_tiles = (total + kAttnKeys - 1) / kAttnKeys;
+    const int32_t t_begin = blockIdx.y * a.tiles_per_split;
+    const int32_t t_end = min(num_tiles, t_begin + a.tiles_per_split);
+
+    for (int32_t c = threadIdx.x; c < 16 * kChunks; c += blockDim.x) {
+        const int32_t r = c / kChunks, ch = c - r * kChunks;
+        const bool ok = r < a.Mq;
+        const int32_t i = ok ? r / a.group : 0, g = ok ? r - i * a.group : 0;
+        const __nv_bfloat16 *src = a.qkv + static_cast<int64_t>(b * a.n + i) * a.nqkv + (hk * a.group + g) * D + ch * 8;
+        cp_async16(sQ + r * kRow + ch * 8, src, ok);
+    }
+    attn_load_tile<D>(a, sKV, t_begin, 0, b, hk, total);
+    cp_async_commit();
+
+    // this thread's accumulator entries: keys (or head dims) gq and gq + 8, query columns 2 qd, 2 qd + 1
+    const int32_t gq = lane >> 2, qd = lane & 3;
+    int32_t node[2];
+    const uint32_t *mrow[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int32_t q = 2 * qd + c;
+        node[c] = q < a.Mq ? q / a.group : -1;
+        mrow[c] = a.mask + static_cast<int64_t>(b * a.n + (node[c] < 0 ? 0 : node[c])) * a.W;
+    }
+    const float scale = 1.0f / sqrtf(static_cast<float>(D));
+    uint32_t qb[kKS][2];
+    float o[kMT][4];
+#pragma unroll
+    for (int j = 0; j < kMT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.0f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+    float (*pw)[kFewPStride] = sP[ks];
+
+    for (int32_t t = t_begin; t < t_end; ++t) {
+        const int32_t stage = (t - t_begin) & 1;
+        if (t + 1 < t_end) attn_load_tile<D>(a, sKV, t + 1, stage ^ 1, b, hk, total);
+        cp_async_commit();
+        cp_async_wait1();
+        __syncthreads();
+        const __nv_bfloat16 *sK = sKV + (2 * stage) * kAttnKeys * kRow + ks * 16 * kRow;
+        const __nv_bfloat16 *sV = sKV + (2 * stage + 1) * kAttnKeys * kRow + ks * 16 * kRow;
+        if (t == t_begin) {  // Q^T as the B operand, two k-steps per load
+#pragma unroll
+            for (int k = 0; k < kKS; k += 2) {
+                uint32_t r[4];
+                ldsm_x4(r, sQ + (lane & 7) * kRow + (k + (lane >> 4)) * 16 + ((lane >> 3) & 1) * 8);
+                qb[k][0] = r[0];
+                qb[k][1] = r[1];
+                qb[k + 1][0] = r[2];
+                qb[k + 1][1] = r[3];
+            }
+        }
+        // S^T over this warp's 16 keys; two accumulators over alternate k-steps
+        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int k = 0; k < kKS; ++k) {
+            uint32_t ka[4];
+            ldsm_x4(ka, sK + (lane & 15) * kRow + k * 16 + (lane >> 4) * 8);
+            if (k & 1)
+                mma_bf16(s2, ka, qb[k][0], qb[k][1]);
+            else
+                mma_bf16(s, ka, qb[k][0], qb[k][1]);
+        }
+        // scale, mask, column max over the warp's 16 keys
+        const int32_t key0 = t * kAttnKeys + ks * 16;
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = e & 1;
+            const int32_t key = key0 + gq + 8 * (e >> 1);
+            bool vis = node[c] >= 0 && key < total;
+            if (vis && key >= a.P) {
+                const int32_t tn = key - a.P;
+                vis = (mrow[c][tn >> 5] >> (tn & 31)) & 1u;
+            }
+            const float v = vis ? (s[e] + s2[e]) * scale : -INFINITY;
+            s[e] = v;
+            mx[c] = fmaxf(mx[c], v);
+        }
+        float corr[2];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) mx[c] = fmaxf(mx[c], __shfl_xor_sync(kFullMask, mx[c], off));
+            const float nm = fmaxf(m_run[c], mx[c]);
+            corr[c] = (m_run[c] == -INFINITY) ? 0.0f : expf(m_run[c] - nm);
+            m_run[c] = nm;
+            l_run[c] *= corr[c];
+        }
+#pragma unroll
+        for (int j = 0; j < kMT; ++j) {
+            o[j][0] *= corr[0];
+            o[j][1] *= corr[1];
+            o[j][2] *= corr[0];
+            o[j][3] *= corr[1];
+        }
+        // probabilities, then P (query rows) into the warp's transpose tile
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = e & 1;
+            const float p = (s[e] == -INFINITY) ? 0.0f : expf(s[e] - m_run[c]);
+            l_run[c] += p;
+            pw[2 * qd + c][gq + 8 * (e >> 1)] = p;
+        }
+        __syncwarp();
+        const float2 p_lo = *reinterpret_cast<const float2 *>(&pw[gq][2 * qd]);      // keys 2qd, 2qd+1
+        const float2 p_hi = *reinterpret_cast<const float2 *>(&pw[gq][2 * qd + 8]);  // keys 2qd+8, 2qd+9
+        const float src[4] = {p_lo.x, p_lo.y, p_hi.x, p_hi.y};
+        float hi_f[4], lo_f[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            hi_f[u] = __bfloat162float(__float2bfloat16_rn(src[u]));
+            lo_f[u] = src[u] - hi_f[u];
+        }
+        const uint32_t bh0 = pack_bf16(hi_f[0], hi_f[1]), bh1 = pack_bf16(hi_f[2], hi_f[3]);
+        const uint32_t bl0 = pack_bf16(lo_f[0], lo_f[1]), bl1 = pack_bf16(lo_f[2], lo_f[3]);
+        // O^T += V^T P^T, head dims on M
+#pragma unroll
+        for (int j = 0; j < kMT; ++j) {
+            uint32_t va[4];
+            ldsm_x4_t(va, sV + ((lane & 7) + (lane >> 4) * 8) * kRow + j * 16 + ((lane >> 3) & 1) * 8);
+            mma_bf16(o[j], va, bh0, bh1);
+            mma_bf16(o[j], va, bl0, bl1);
+        }
+        __syncthreads();  // the next iteration's loads overwrite this stage (and the transpose tile)
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) l_run[c] += __shfl_xor_sync(kFullMask, l_run[c], off);
+
+    // the four key slices merge through shared memory (the stages are free now)
+    float *mo = reinterpret_cast<float *>(sKV);                       // [kFewWarps][8][D]
+    float2 *mml = reinterpret_cast<float2 *>(mo + kFewWarps * 8 * D);  // [kFewWarps][8]
+#pragma unroll
+    for (int j = 0; j < kMT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            mo[(ks * 8 + 2 * qd + (e & 1)) * D + j * 16 + gq + 8 * (e >> 1)] = o[j][e];
+    if (gq == 0) {
+        mml[ks * 8 + 2 * qd] = make_float2(m_run[0], l_run[0]);
+        mml[ks * 8 + 2 * qd + 1] = make_float2(m_run[1], l_run[1]);
+    }
+    __syncthreads();
+    if (ks != 0) return;
+    float wk[2][kFewWarps];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int32_t q = 2 * qd + c;
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kFewWarps; ++k) M = fmaxf(M, mml[k * 8 + q].x);
+        float L = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kFewWarps; ++k) {
+            const float2 ml = mml[k * 8 + q];
+            wk[c][k] = (ml.x == -INFINITY) ? 0.0f : expf(ml.x - M);
+            L += wk[c][k] * ml.y;
+        }
+        m_run[c] = M;
+        l_run[c] = L;
+    }
+#pragma unroll
+    for (int j = 0; j < kMT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = e & 1;
+            const int32_t q = 2 * qd + c, d = j * 16 + gq + 8 * (e >> 1);
+            float v = 0.0f;
+#pragma unroll
+            for (int k = 0; k < kFewWarps; ++k) v = fmaf(wk[c][k], mo[(k * 8 + q) * D + d], v);
+            o[j][e] = v;
+        }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int32_t q = 2 * qd + c;
+        if (q >= a.Mq) continue;
+        if (a.splits == 1) {
+            const int32_t i = node[c], g = q - i * a.group, hq = hk * a.group + g;
+            __nv_bfloat16 *orow = a.o + static_cast<int64_t>(b * a.n + i) * a.H * D + hq * D;
+            const float inv = l_run[c] > 0.0f ? 1.0f / l_run[c] : 0.0f;
+#pragma unroll
+            for (int j = 0; j < kMT; ++j) {
+                orow[j * 16 + gq] = __float2bfloat16_rn(o[j][c] * inv);
+                orow[j * 16 + gq + 8] = __float2bfloat16_rn(o[j][c + 2] * inv);
+            }
+        } else {
+            const int64_t prow = static_cast<int64_t>(blockIdx.y) * a.B * a.Hk * a.Mq +
+                                 static_cast<int64_t>(pair) * a.Mq + q;
+            float *po = a.part_o + prow * D;
+#pragma unroll
+            for (int j = 0; j < kMT; ++j) {
+                po[j * 16 + gq] = o[j][c];
+                po[j * 16 + gq + 8] = o[j][c + 2];
+            }
+            if (gq == 0) a.part_ml[prow] = make_float2(m_run[c], l_run[c]);
+        }
+    }
+}
+
 // Merges the key splits of each query row: o = sum_s w_s O_s / sum_s w_s l_s with
 // w_s = exp(m_s - max_s m_s) (0 for a split that saw no visible key).  A warp per query row: lane
 // s reads split s's (max, sum) (at most 32 splits), then each lane sums 4 output columns.
@@ -567,6 +796,7 @@ constexpr int32_t kAttnMaxSplits = 32;
 // split count (enough CTAs for two per SM when (request, kv head, query tile) alone are fewer).
 struct AttnPlan {
     int32_t group, Mq, qw, kw, warps, rows_cta, q_tiles, splits_max;
+    bool few;  // at most 8 query rows per (request, kv head): tree_attention_few_kernel
 };
 
 AttnPlan attn_plan(const eagle_decoder_layer_weights *w, int32_t batch, int32_t nodes, int32_t sms) {
@@ -578,6 +808,7 @@ AttnPlan attn_plan(const eagle_decoder_layer_weights *w, int32_t batch, int32_t 
     p.warps = p.qw * p.kw;
     p.rows_cta = p.qw * 16;
     p.q_tiles = (p.Mq + p.rows_cta - 1) / p.rows_cta;
+    p.few = p.Mq <= 8;  // one warp's 16-row tile would be half padding: the transposed kernel
     const int64_t ctas = static_cast<int64_t>(batch) * w->kv_heads * p.q_tiles;
     p.splits_max = ctas >= 2 * sms ? 1 : static_cast<int32_t>(std::min<int64_t>(kAttnMaxSplits, (2 * sms + ctas - 1) / ctas));
     return p;
@@ -663,6 +894,9 @@ cudaError_t set_attention_smem() {
         e = cudaFuncSetAttribute(tree_attention_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(tree_attention_kernel<D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tree_attention_few_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int32_t>(AttnShape<D>::smem_bytes(16)));
     return e;
 }
 
@@ -670,6 +904,7 @@ template <int D>
 cudaError_t launch_attention(const AttnPlan &ap, dim3 grid, const AttnArgs &aa, cudaStream_t st) {
     const dim3 block(ap.warps * 32);
     const size_t smem = AttnShape<D>::smem_bytes(ap.rows_cta);
+    if (ap.few) return launch_pdl(tree_attention_few_kernel<D>, grid, block, smem, st, aa);
     if (ap.kw == 4) return launch_pdl(tree_attention_kernel<D, 4>, grid, block, smem, st, aa);
     if (ap.kw == 2) return launch_pdl(tree_attention_kernel<D, 2>, grid, block, smem, st, aa);
     return launch_pdl(tree_attention_kernel<D, 1>, grid, block, smem, st, aa);

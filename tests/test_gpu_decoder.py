@@ -105,6 +105,8 @@ CASES = [
     (4, 80, 5, 256, 4, 4, 64, 384, 6),      # 320 rows: two GEMM row chunks, deferred split-K sums
     (40, 4, 300, 128, 8, 8, 128, 256, 3),   # 16 query rows a CTA, D = 128, 5 key tiles each (no key split)
     (2, 8, 700, 128, 2, 2, 128, 256, 4),    # the same rows split over the keys: runs of 2 tiles
+    (3, 3, 150, 128, 4, 2, 64, 256, 2),     # 6 query rows of 2-head groups, D = 64, key splits
+    (2, 4, 90, 64, 2, 1, 32, 128, 3),       # exactly 8 query rows (MQA pairs), D = 32
 ]
 
 
