@@ -618,7 +618,7 @@ eagle_status eagle_draft_level(eagle_tree *t, int32_t level, const void *d_root_
     const eagle_tree_config &c = t->cfg;
     if (level < 0 || level >= c.depth) return EAGLE_ERR_INVALID_ARG;
     if (level != 0 && level != t->next_level) return EAGLE_ERR_STATE;
-    const int32_t B = c.batch, h = c.hidden, V = c.vocab, k = c.topk, d = c.depth;
+    const int32_t B = c.batch, h = c.hidden, V = c.vocab;
     if (B == 0) {
         t->tree_built = false;
         t->next_level = level + 1;
