@@ -107,6 +107,7 @@ CASES = [
     (2, 8, 700, 128, 2, 2, 128, 256, 4),    # the same rows split over the keys: runs of 2 tiles
     (3, 3, 150, 128, 4, 2, 64, 256, 2),     # 6 query rows of 2-head groups, D = 64, key splits
     (2, 4, 90, 64, 2, 1, 32, 128, 3),       # exactly 8 query rows (MQA pairs), D = 32
+    (2, 1, 130, 128, 8, 1, 64, 256, 0),     # a lone root under 8-head groups: 8 query rows of one node
 ]
 
 
