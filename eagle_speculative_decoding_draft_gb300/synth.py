@@ -108,6 +108,16 @@ def make_inputs(w: Workload, seed: int | None = None) -> Inputs:
     return Inputs(w, w_fc, b_fc, w_lm, emb, root_feat, root_tok, rng)
 
 
+def extra_roots(w: Workload, count: int, seed: int):
+    """`count` more root inputs (features [count][h] ~ N(0, 1), tokens ~ U{0..V-1}) for the same
+    weights, from their own seeded stream; returns CPU tensors (features in the workload's dtype,
+    tokens int32)."""
+    rng = np.random.default_rng(seed)
+    feat = _normal(rng, (count, w.hidden), 1.0, w.dtype)
+    tok = torch.from_numpy(rng.integers(0, w.vocab, size=count, dtype=np.int64).astype(np.int32))
+    return feat, tok
+
+
 def target_noise(inp: Inputs, shape=None) -> np.ndarray:
     """N(0, sigma) noise, float32, of shape [B][m+1][V] by default, drawn next in the stream."""
     w = inp.workload

@@ -1,25 +1,40 @@
 """End-to-end parity of one draft-tree step on the GPU against the oracle, on the same seeded inputs.
 
-For the tiny fp32 workload, the Vicuna-7B-shaped workload and a set of ragged / edge shapes the
-oracle runs the whole batch; for the three large workloads (SGLang default, LLaMA2-70B shape,
-Llama-3-8B vocabulary) the GPU runs the full batch in the benchmark's launch configuration and
-the oracle recomputes sampled requests (requests are independent).
+The GPU always runs the whole batch in the benchmark's launch configuration.  For the tiny fp32
+workload, the LLaMA2-70B shape and the ragged / edge shapes the oracle checks every request; the
+Vicuna-7B shape (one request a step) is checked on eight seeded roots with the same weights; for
+the SGLang default and the Llama-3-8B vocabulary the oracle recomputes 16 and 4 requests spread
+over the batch (requests are independent).
 
-Per request, level by level while both sides expand the same nodes: every draft row's logits
-within tolerance, and a decision (children of a row, the frontier, the rerank cut) allowed to
-differ only when its margin is at most max(1e-3, twice the GPU-oracle deviation measured at that
-level).  When all decisions agree: tree arrays, mask, positions, node logits and the verify
-result bit-exact / within tolerance.  Always: the GPU tree is valid (parents first, child score
-<= parent score, mask = ancestor closure, positions = depth) and greedy verify of the oracle's
-own tree is bit-exact.
+Two comparisons per checked request:
+
+* free-running: the oracle drafts the request from its root on its own, and the two are walked
+  level by level while they expand the same nodes.  Every draft row's logits within tolerance; a
+  decision (children of a row, the frontier, the rerank cut) may differ only when its margin is at
+  most max(1e-3, twice the GPU-oracle deviation measured at that level), because one-ulp
+  differences in the bf16 rounding of f^ grow from level to level (see parity.py).  When all
+  decisions agree: tree arrays, mask, positions, node logits and the verify result bit-exact /
+  within tolerance.  Whole trees rarely agree at bf16 (see the floors below), so this comparison is
+  recorded rather than floored, except for the fp32 workload and the SGLang shape.
+* teacher-forced: each level is checked against the oracle fed the GPU's own inputs to that level,
+  so there is no drift and the benchmark spec's rule holds as written: every decision identical wherever
+  its margin exceeds 1e-3, frontier, rerank, tree and verify bit-exact (parity.teacher_forced_check).
+  Nearly every checked request must come out whole (no decision differing at all).
+
+Always: the GPU tree is valid (parents first, child score <= parent score, mask = ancestor closure,
+positions = depth) and greedy verify of the oracle's own tree is bit-exact.  The counts of both
+comparisons go into the session's parity record (conftest.parity_record).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from eagle_speculative_decoding_draft_gb300 import synth
-from parity import assert_close_logits, assert_valid_tree, close_logits, lockstep_compare, to_np
+from parity import (MARGIN, assert_close_logits, assert_valid_tree, close_logits, lockstep_compare,
+                    new_tf_record, teacher_forced_check, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -38,11 +53,21 @@ def sub(t, idx):
     return t[idx].contiguous()
 
 
-def run_case(dev, w, inp, sample=None, report=None):
+def new_free_record():
+    return {"requests": 0, "exact": 0, "decisions": 0, "within_1e3": 0, "widened_only": 0,
+            "diverged": [], "diverged_beyond_1e3": 0}
+
+
+def run_case(dev, w, inp, sample=None, free=None, tf=None, eng=None):
+    """One GPU step over the whole batch of `inp`, checked against the oracle on the requests in
+    `sample` (all by default).  Adds to the free-running and teacher-forced records; returns
+    (exact, diverged) of the free-running comparison."""
     from eagle_speculative_decoding_draft_gb300.engine import EagleTree
     B, d, k, m, V, n = w.batch, w.depth, w.topk, w.num_keep, w.vocab, w.num_nodes
     idx = list(range(B)) if sample is None else list(sample)
-    # ---- oracle on the sampled requests ----
+    free = new_free_record() if free is None else free
+    tf = new_tf_record() if tf is None else tf
+    # ---- oracle, free-running, on the sampled requests ----
     ref = oracle.draft_tree(inp.w_fc, inp.b_fc, inp.w_lm, inp.emb, sub(inp.root_feat, idx),
                             sub(inp.root_tok, idx), d, k, m, w.is_bf16,
                             pos_base=np.array([7 * b + 1 for b in idx], np.int32),
@@ -54,19 +79,24 @@ def run_case(dev, w, inp, sample=None, report=None):
 
     # ---- GPU, whole batch ----
     g = lambda t: t.to(dev).contiguous()
-    eng = EagleTree(g(inp.w_fc), g(inp.b_fc) if w.bias else None, g(inp.w_lm), g(inp.emb), B, d,
-                    k, m)
+    own = eng is None
+    if own:
+        eng = EagleTree(g(inp.w_fc), g(inp.b_fc) if w.bias else None, g(inp.w_lm), g(inp.emb), B, d,
+                        k, m)
     R = B * k
     logits_out = torch.empty(d, max(R, 1), V, dtype=torch.float32, device=dev)
     pos_base = torch.tensor([7 * b + 1 for b in range(B)], dtype=torch.int32, device=dev)
     root_feat, root_tok = g(inp.root_feat), g(inp.root_tok)
     tree = eng.draft(root_feat, root_tok, pos_base, logits_out=logits_out)
     views = eng.views()
-    gpu = {key: to_np(views[key]) for key in ("pool_tok", "pool_S", "pool_parent")}
+    gpu = {key: to_np(views[key]) for key in ("pool_tok", "pool_S", "pool_parent", "pool_row")}
+    gpu["fhat"] = to_np(views["fhat"].float())
     gpu["logits"] = logits_out
     node_z = eng.node_logits(root_feat)
     Td = torch.from_numpy(T).to(dev)
     ver = eng.verify_greedy(tree["tokens"], tree["parents"], Td)
+    GV = {key: to_np(v) for key, v in ver.items()}
+    G = {key: to_np(v) for key, v in tree.items()}
     # verify of the oracle's own trees (bit-exact always)
     tok_mix, par_mix = tree["tokens"].clone(), tree["parents"].clone()
     tok_mix[idx] = torch.from_numpy(ref["tree_tok"]).to(dev)
@@ -77,13 +107,12 @@ def run_case(dev, w, inp, sample=None, report=None):
     eng.status()
     torch.cuda.synchronize()
 
-    G = {key: to_np(v) for key, v in tree.items()}
     G2 = {key: to_np(v) for key, v in tree2.items()}
     for key in ("tokens", "parents", "positions", "mask", "logscore"):
         assert np.array_equal(G[key], G2[key]), f"{key} not deterministic"
-    GV = {key: to_np(v) for key, v in ver.items()}
     GVR = {key: to_np(v) for key, v in ver_ref_tree.items()}
-    exact, diverged, dz = 0, [], []
+    gpu.update({key: G[key] for key in ("tokens", "parents", "positions", "mask", "logscore")})
+    exact, diverged = 0, []
     for j, b in enumerate(idx):
         # validity of the GPU tree, always
         assert_valid_tree(G["tokens"][b], G["parents"][b], G["positions"][b], G["mask"][b],
@@ -93,11 +122,22 @@ def run_case(dev, w, inp, sample=None, report=None):
         assert GVR["accept_len"][b] == ref_ver["accept_len"][j]
         assert np.array_equal(GVR["accept_nodes"][b], ref_ver["accept_nodes"][j])
         assert np.array_equal(GVR["accept_tokens"][b], ref_ver["accept_tok"][j])
+        # teacher-forced: every level against the oracle on the GPU's own inputs
+        teacher_forced_check(inp, w, gpu, b, lambda l, r: to_np(logits_out[l, r]), T[b],
+                             (GV["accept_len"][b], GV["accept_nodes"][b], GV["accept_tokens"][b]),
+                             7 * b + 1, tf)
+        # free-running
         info = lockstep_compare(ref, j, gpu, b, k, d, m, w.is_bf16)
-        dz.append(info["dz"])
+        free["requests"] += 1
+        for key in ("decisions", "within_1e3", "widened_only"):
+            free[key] += info[key]
         if not info["exact"]:
             diverged.append((b, info["diverged_at"], round(info["margin"], 6),
                              round(info["threshold"], 6)))
+            free["diverged"].append({"request": b, "level": info["diverged_at"],
+                                     "margin": info["margin"], "threshold": info["threshold"]})
+            if info["margin"] > MARGIN:
+                free["diverged_beyond_1e3"] += 1
             continue
         exact += 1
         for key, rk in (("tokens", "tree_tok"), ("parents", "tree_parent"),
@@ -109,21 +149,67 @@ def run_case(dev, w, inp, sample=None, report=None):
         assert GV["accept_len"][b] == ref_ver["accept_len"][j]
         assert np.array_equal(GV["accept_nodes"][b], ref_ver["accept_nodes"][j])
         assert np.array_equal(GV["accept_tokens"][b], ref_ver["accept_tok"][j])
-    if report is not None:
-        report.update(exact=exact, diverged=diverged, accept=GV["accept_len"][idx].tolist(),
-                      dz=[[round(x, 5) for x in row] for row in dz])
-    eng.close()
+    free["exact"] += exact
+    if own:
+        eng.close()
     return exact, diverged
 
 
-@pytest.mark.parametrize("num", [1, 2])
-def test_full_oracle_workloads(dev, num):
-    w = synth.WORKLOADS[num]
+def summary(free, tf):
+    return (f"free-running: {free['exact']} of {free['requests']} trees identical, "
+            f"{free['decisions']} decisions ({free['within_1e3']} with margin <= 1e-3, "
+            f"{free['widened_only']} within the widened window only), diverged {free['diverged']}; "
+            f"teacher-forced: {tf['exact_trees']} of {tf['requests']} requests identical, {tf['rows']} rows, {tf['rows_diverged']} "
+            f"top-k decisions differ (all at margin <= 1e-3; {tf['rows_within_1e3']} rows have such a "
+            f"margin), f^ one-ulp flips {tf['fhat_flips']} of {tf['fhat_elems']}, max |dz| {tf['max_dz']:.3g}")
+
+
+# Floors.  Teacher-forced: requests whose every decision (each row's top-k children, the frontiers,
+# the rerank and the tree, the verify) equals the oracle's on the same inputs; a top-k decision may
+# differ only at a margin of at most 1e-3, so nearly all must be whole.  Free-running: whole trees
+# identical to the oracle's own from the root.  At bf16 that is rare by construction: one-ulp
+# differences in the bf16 rounding of f^ (any two fp32 summation orders give some) move the next
+# level's logits by ~1e-3, and a request has 17-51 rows of k close top-k gaps.  Only the fp32
+# workload and the SGLang shape (17 rows of k = 4 a request, 16 requests checked) get a floor.
+def tf_floor(requests):
+    return max(1, requests - requests // 8)
+
+
+FREE_FLOOR = {1: 1, 3: 1}
+
+
+def test_tiny_fp32_workload(dev, parity_record):
+    w = synth.WORKLOADS[1]
     inp = synth.make_inputs(w)
-    rep = {}
-    exact, diverged = run_case(dev, w, inp, report=rep)
-    print(f"workload {num}: trees identical {exact}, diverged at a near-tie {diverged}, "
-          f"accept_len {rep['accept']}, max|dz| per level {rep['dz']}")
+    free, tf = new_free_record(), new_tf_record()
+    run_case(dev, w, inp, free=free, tf=tf)
+    parity_record[w.name] = {"free_running": free, "teacher_forced": tf}
+    print(summary(free, tf))
+    assert free["exact"] >= FREE_FLOOR[1], summary(free, tf)
+    assert tf["exact_trees"] >= tf_floor(tf["requests"]), summary(free, tf)
+
+
+VICUNA_ROOTS = 8
+
+
+def test_vicuna7b_shape_over_seeded_roots(dev, parity_record):
+    """Batch 1 (the benchmark's launch configuration), one handle, eight roots: the workload's own
+    and seven more from a seeded stream, each drafted, built and verified in full."""
+    from eagle_speculative_decoding_draft_gb300.engine import EagleTree
+    w = synth.WORKLOADS[2]
+    inp = synth.make_inputs(w)
+    g = lambda t: t.to(dev).contiguous()
+    eng = EagleTree(g(inp.w_fc), g(inp.b_fc), g(inp.w_lm), g(inp.emb), 1, w.depth, w.topk, w.num_keep)
+    feats, toks = synth.extra_roots(w, VICUNA_ROOTS - 1, seed=2024)
+    free, tf = new_free_record(), new_tf_record()
+    for r in range(VICUNA_ROOTS):
+        one = inp if r == 0 else dataclasses.replace(
+            inp, root_feat=feats[r - 1:r].contiguous(), root_tok=toks[r - 1:r].contiguous())
+        run_case(dev, w, one, free=free, tf=tf, eng=eng)
+    eng.close()
+    parity_record[w.name + f" ({VICUNA_ROOTS} roots)"] = {"free_running": free, "teacher_forced": tf}
+    print(summary(free, tf))
+    assert tf["requests"] == VICUNA_ROOTS and tf["exact_trees"] >= tf_floor(VICUNA_ROOTS), summary(free, tf)
 
 
 EDGE = [
@@ -155,14 +241,19 @@ def test_edge_shapes(dev, case):
 
 
 @pytest.mark.parametrize("num", [3, 4, 5])
-def test_large_workloads_sampled(dev, num):
+def test_large_workloads_sampled(dev, num, parity_record):
     w = synth.WORKLOADS[num]
     inp = synth.make_inputs(w)
-    sample = sorted({0, w.batch // 2, w.batch - 1})
-    rep = {}
-    exact, diverged = run_case(dev, w, inp, sample=sample, report=rep)
-    print(f"workload {num}: sampled {sample}, trees identical {exact}, diverged at a near-tie "
-          f"{diverged}, accept_len {rep['accept']}, max|dz| per level {rep['dz']}")
+    # every request of the LLaMA2-70B shape; 16 of the SGLang default's 64 (so that its free-running
+    # floor means something); 4 of the Llama-3-8B vocabulary's 32 (its oracle rows are the costliest)
+    count = {3: 16, 4: w.batch, 5: 4}[num]
+    sample = sorted({round(i * (w.batch - 1) / max(count - 1, 1)) for i in range(count)})
+    free, tf = new_free_record(), new_tf_record()
+    run_case(dev, w, inp, sample=sample, free=free, tf=tf)
+    parity_record[w.name + f" (requests {sample})"] = {"free_running": free, "teacher_forced": tf}
+    print(summary(free, tf))
+    assert tf["requests"] == len(sample) and tf["exact_trees"] >= tf_floor(len(sample)), summary(free, tf)
+    assert free["exact"] >= FREE_FLOOR.get(num, 0), summary(free, tf)
 
 
 def test_empty_batch_is_a_no_op(dev):

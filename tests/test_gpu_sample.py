@@ -109,7 +109,7 @@ def random_forest(rng, B, n, k_max, V):
                                              (16, 5, 17, 1.0, 0), (2, 65, 128256, 1.0, 0),
                                              (5, 9, 2049, 1.3, 1),
                                              (1, 4097, 64, 1.0, 0)])  # the largest tree the call takes
-def test_random_trees_match_the_oracle(dev, B, n, V, temp, mode):
+def test_random_trees_match_the_oracle(dev, B, n, V, temp, mode, parity_record):
     rng = np.random.default_rng(B * 1000 + n * 10 + V)
     tok, par, depth = random_forest(rng, B, n, 4, V)
     # target close to the draft so that children are often accepted and walks go deep
@@ -124,10 +124,18 @@ def test_random_trees_match_the_oracle(dev, B, n, V, temp, mode):
     ua = rng.random((B, n), dtype=np.float32)
     ub = rng.random(B, dtype=np.float32)
     thr = 0.05 if mode == 1 else 0.0
+    compared, excused = 0, 0
     for d in sorted({depth, max(depth - 1, 0), 1}):
         got = gpu_sample(dev, tok, par, T, Z, d, temp, ua, ub, mode=mode, threshold=thr)
         near = compare(tok, par, T, Z, d, temp, ua, ub, got, mode=mode, threshold=thr)
+        compared += B
+        excused += near
         assert near <= max(1, B // 8)
+    # the observed count, not only the cap: requests whose result the oracle reproduces only with
+    # that request's uniforms moved by 1e-4 (fp32 kernel against the double-precision oracle)
+    parity_record[f"sampling verify B{B} n{n} V{V} t{temp} mode{mode}"] = {
+        "requests_compared": compared, "excused_by_uniform_shift": excused}
+    print(f"sampling verify B{B} n{n} V{V}: {excused} of {compared} requests excused by a 1e-4 uniform shift")
 
 
 def test_edge_cases(dev):

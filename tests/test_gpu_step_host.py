@@ -17,8 +17,8 @@ def dev():
     return torch.device("cuda", 0)
 
 
-@pytest.mark.parametrize("wl", [1, 2])
-def test_host_step_matches_the_device_step(dev, wl):
+@pytest.mark.parametrize("wl,tdt", [(1, "f32"), (2, "f32"), (2, "bf16")])
+def test_host_step_matches_the_device_step(dev, wl, tdt):
     from eagle_speculative_decoding_draft_gb300.engine import EagleTree
     w = synth.WORKLOADS[wl]
     inp = synth.make_inputs(w)
@@ -41,6 +41,8 @@ def test_host_step_matches_the_device_step(dev, wl):
         tree = eng.draft(fd, td, None if pos is None else g(pos))
         nz = eng.node_logits(fd)
         T = (nz + torch.randn(nz.shape, device=dev, generator=torch.Generator(device=dev).manual_seed(it))).contiguous()
+        if tdt == "bf16":  # the target logits a bf16 target model emits
+            T = T.to(torch.bfloat16)
         ver = eng.verify_greedy(tree["tokens"], tree["parents"], T)
         torch.cuda.synchronize()
         if staging is None:
