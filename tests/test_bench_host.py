@@ -86,14 +86,39 @@ def test_kernel_hash_ignores_comments_and_follows_code(tmp_path, monkeypatch):
 
 
 def test_recorded_traffic_needs_the_current_hash(tmp_path, monkeypatch):
+    import json
     src = tmp_path / "k.cu"
     src.write_text("int f() { return 1; }\n")
     monkeypatch.setattr(bench, "ROOT", tmp_path)
     monkeypatch.setattr(bench, "KERNEL_SOURCES", ["k.cu"])
-    prof = tmp_path / "p.md"
+    prof = tmp_path / "t.json"
     monkeypatch.setattr(bench, "TRAFFIC_FILE", prof)
-    assert bench.recorded_traffic() is None                        # no summary
-    prof.write_text(f"kernel_source_hash: {bench.kernel_hash()}\ntraffic_bytes_per_launch: 167.2e6\n")
-    assert bench.recorded_traffic() == pytest.approx(167.2e6)
-    src.write_text("int f() { return 2; }\n")                       # the kernel changed since
-    assert bench.recorded_traffic() is None
+    assert bench.recorded_traffic("w") is None                     # no record
+    prof.write_text(json.dumps({"kernel_source_hash": bench.kernel_hash(),
+                                "workloads": {"w": {"traffic_bytes_per_launch": 167.2e6}}}))
+    assert bench.recorded_traffic("w") == pytest.approx(167.2e6)
+    assert bench.recorded_traffic("other") is None                 # not captured for that one
+    src.write_text("int f() { return 2; }\n")                     # the kernel changed since
+    assert bench.recorded_traffic("w") is None
+
+
+def test_step_floor_matches_the_survey_table():
+    from eagle_speculative_decoding_draft_gb300 import synth
+    # Vicuna-7B shape: 6 levels of 329.25 MB of weights, HBM-bound, about 291 us at 6779.4 GB/s
+    f = bench.step_floor(synth.WORKLOADS[2], 6779.4, 1679.0)
+    assert f["bytes"] == pytest.approx(1.976e9, rel=2e-3)
+    assert f["us"] == pytest.approx(291.4, rel=3e-3)
+    # Llama-3-8B vocabulary: 5 levels of 1117.8 MB; the 256-row levels sit near the ridge
+    f5 = bench.step_floor(synth.WORKLOADS[5], 6779.4, 1679.0)
+    assert f5["bytes"] == pytest.approx(5.589e9, rel=5e-3)
+    assert 824.0 <= f5["us"] <= 900.0
+    assert f5["verify_scan_bytes"] == 32 * 65 * 128256 * 2
+
+
+def test_gemm_roofline_fractions():
+    plist = [{"ms": 0.05, "bytes": 250e6, "flops": 1e9}, {"ms": 0.1, "bytes": 250e6, "flops": 150e12 * 1e-4}]
+    r = bench.gemm_roofline(plist, hbm=5000.0, tflops=1000.0)
+    assert r["achieved"] == pytest.approx(500e6 / 0.15e-3 / 1e9)
+    # floors: 0.05 ms (bytes) and max(0.05, 0.015) ms: 0.1 ms of 0.15 ms measured
+    assert r["frac_of_roofline_time"] == pytest.approx(0.1 / 0.15)
+    assert bench.gemm_roofline([], 5000.0, 1000.0) is None
