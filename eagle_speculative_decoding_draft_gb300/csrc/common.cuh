@@ -289,6 +289,62 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ---- the same for a CTA pair (tcgen05 with .cta_group::2): the MMA of M = 256 reads A's two
+// 128-row halves and B's two column halves from the shared memory of both CTAs of the pair (same
+// offsets) and accumulates each CTA's 128 rows into that CTA's tensor memory.  Every tcgen05
+// instruction of a kernel that uses them carries .cta_group::2.
+// Whole-warp, one warp in each CTA of the pair together.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Issued by one thread of the pair's even CTA.
+__device__ __forceinline__ void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrives once on the mbarrier at this shared-memory offset in every CTA of `cta_mask` when the
+// pair's tcgen05 operations issued so far by this thread complete.
+__device__ __forceinline__ void mma_commit_pair_mc(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+// 2-D tiled load into this CTA's shared memory whose completion is counted on an mbarrier that
+// may sit in the peer CTA of the pair (`bar_cluster`: a shared::cluster address from mapa).
+__device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const void *map, uint32_t bar_cluster, int32_t x,
+                                                 int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+// Arrive (release at cluster scope) on an mbarrier in a cluster CTA's shared memory.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+// arrive.expect_tx on an mbarrier given by its shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar_cluster, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar_cluster),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA with 128-byte
 // swizzling: rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), tile base
 // 1024-byte aligned.  Fields: start address >> 4 in bits 0-13, leading byte offset >> 4 in

@@ -28,8 +28,17 @@
 //               in its own (then idle) ring, and after a cluster barrier sums a 1/C share of the
 //               tile's outputs over the C CTAs in rank order through distributed shared memory,
 //               written by one TMA store: no partials in global memory, no tickets, no second
-//               launch.
+//               launch;
+//   CTA pairs   above 16 rows, with an even number of weight tiles and stream-K, the CTAs run as
+//               pairs (clusters of 2) on tcgen05 with .cta_group::2: one MMA of M = 256 covers
+//               the pair's two adjacent weight tiles, each CTA streams its own tile's weights and
+//               half of the activation rows, and the MMA reads both halves from the two CTAs'
+//               shared memory.  An activation byte brought into an SM then feeds 256 weight rows
+//               instead of 128: per k-block an SM takes in 16 KB of weights and n/2 x 128 B of
+//               activations (32 KB at 256 rows, against 48 KB).  The stream-K split is over pairs
+//               (k-blocks of pair tiles), and each CTA sums and writes its own tile as before.
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -69,6 +78,8 @@ struct LinearArgs {
     int32_t defer;  // split tiles: write partials only; linear_reduce_kernel sums them
     int32_t cluster_k;  // > 1: split-K over a cluster of this many CTAs per tile (no stream-K)
     int32_t owner_fix;  // split tiles summed in the launch by the CTA that finds its partner done
+    int32_t pair;       // 1: CTA pairs (.cta_group::2), the stream-K split over pairs of tiles
+    int32_t num_wtiles; // units of the stream-K split: tiles, or pairs of tiles when pair
     int32_t y_tma;      // 16-row groups of Y and of partials go out by bulk stores (tmap_y valid)
     int32_t out_stage_bytes;  // shared-memory staging of those groups (after the ring)
     float *partials;
@@ -84,9 +95,15 @@ __device__ __forceinline__ int64_t div_nonneg(int64_t a, int64_t b) {
     return a / b;
 }
 
-// CTA whose k-block range [total*g/G, total*(g+1)/G) contains k-block p.
+// Worker (CTA, or CTA pair) whose k-block range [total*g/G, total*(g+1)/G) contains k-block p.
 __device__ __forceinline__ int32_t cta_of(int64_t p, int64_t total, int32_t G) {
     return static_cast<int32_t>(div_nonneg((p + 1) * G + total - 1, total)) - 1;
+}
+
+// A worker's partial sums of one of its (at most two) split tiles: slot 0 for the tile its range
+// starts in, 1 for the one it ends in; with CTA pairs each CTA of the pair (rank) has its own.
+__device__ __forceinline__ float *part_slot(const LinearArgs &a, int32_t worker, int32_t slot, int32_t rank) {
+    return a.partials + static_cast<size_t>((((worker * 2 + slot) << a.pair) + rank)) * a.n_tile * BM;
 }
 
 __device__ __forceinline__ void store_y(const LinearArgs &a, int32_t r, int32_t o, float v) {
@@ -138,8 +155,8 @@ __device__ __forceinline__ void group_store(const LinearArgs &a, const CUtensorM
 __device__ __forceinline__ bool staged_fixup(const LinearArgs &a, const CUtensorMap *tmap_y, SmemCtl *ctl,
                                              uint8_t *ring, uint32_t ring_bytes, uint8_t *out_stage, int32_t &gi,
                                              int32_t tile, int32_t gf, int32_t gl, int32_t self, bool gf_second,
-                                             uint32_t t_row, int32_t et, int32_t m_local, int32_t o, bool o_ok,
-                                             float bias_o, volatile int32_t *abort_flag) {
+                                             int32_t rank, uint32_t t_row, int32_t et, int32_t m_local, int32_t o,
+                                             bool o_ok, float bias_o, volatile int32_t *abort_flag) {
     const int32_t np = gl - gf;  // partials read from global memory
     const uint32_t row_bytes = BM * 4u;
     int32_t cr = static_cast<int32_t>(ring_bytes / (static_cast<uint32_t>(np) * row_bytes)) & ~15;
@@ -157,8 +174,8 @@ __device__ __forceinline__ bool staged_fixup(const LinearArgs &a, const CUtensor
             for (int32_t gg = gf; gg <= gl; ++gg) {
                 if (gg == self) continue;
                 const int32_t slot = (gg == gf && gf_second) ? 1 : 0;
-                const uint8_t *src = reinterpret_cast<const uint8_t *>(
-                    a.partials + static_cast<size_t>(gg * 2 + slot) * a.n_tile * BM + static_cast<size_t>(r0) * BM);
+                const uint8_t *src = reinterpret_cast<const uint8_t *>(part_slot(a, gg, slot, rank) +
+                                                                       static_cast<size_t>(r0) * BM);
                 uint8_t *dst = ring + static_cast<size_t>(pi) * cr * row_bytes;
                 const uint32_t bytes = static_cast<uint32_t>(rc) * row_bytes;
                 for (uint32_t off = 0; off < bytes; off += 32768u)
@@ -215,6 +232,8 @@ __device__ __forceinline__ bool staged_fixup(const LinearArgs &a, const CUtensor
     return true;
 }
 
+// kPair: CTA pairs on tcgen05 .cta_group::2 (launched in clusters of 2; a.pair == 1).
+template <int kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                           const __grid_constant__ CUtensorMap tmap_x,
@@ -223,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const int32_t stages = a.stages;
-    const uint32_t b_bytes = static_cast<uint32_t>(a.n_tile) * 128u;
+    // with pairs each CTA holds half of the activation rows of a stage
+    const uint32_t b_bytes = static_cast<uint32_t>(a.n_tile >> kPair) * 128u;
     uint8_t *a_tiles = base;
     uint8_t *b_tiles = base + static_cast<size_t>(stages) * kABytes;
     uint8_t *out_stage = b_tiles + static_cast<size_t>(stages) * b_bytes;  // bulk-store staging
@@ -232,9 +252,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int32_t *abort_flag = &ctl->abort;
 
     const int32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int32_t G = gridDim.x, g = blockIdx.x;
+    // workers: CTAs, or CTA pairs (the pair's even CTA issues the MMAs for both); the k-block
+    // stream runs over the workers' units: tiles, or pairs of adjacent tiles
+    const int32_t G = gridDim.x >> kPair, g = blockIdx.x >> kPair;
+    const int32_t rank = kPair ? static_cast<int32_t>(blockIdx.x & 1u) : 0;
     const int64_t nkb = a.num_kb;
-    const int64_t total = static_cast<int64_t>(a.num_tiles) * nkb;
+    const int64_t total = static_cast<int64_t>(a.num_wtiles) * nkb;
     int64_t kb_begin = div_nonneg(total * g, G), kb_end = div_nonneg(total * (g + 1), G);
     const int32_t CK = a.cluster_k;
     if (CK > 1) {  // tile g / CK, k-slice g % CK (the CTA's rank in its cluster)
@@ -252,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctl->acc_full[i], 1);
-            mbar_init(&ctl->acc_empty[i], 4);
+            mbar_init(&ctl->acc_empty[i], kPair ? 8 : 4);  // pairs: both CTAs' epilogue warps
         }
         mbar_init(&ctl->fix, 1);
         mbar_init(&ctl->drain, 1);
@@ -264,11 +287,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tmap_x);
     }
     if (warp == 1) {
-        tmem_alloc(&ctl->tmem_base, static_cast<uint32_t>(a.tmem_cols));
-        tmem_relinquish();
+        if (kPair) {
+            tmem_alloc_pair(&ctl->tmem_base, static_cast<uint32_t>(a.tmem_cols));
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&ctl->tmem_base, static_cast<uint32_t>(a.tmem_cols));
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (kPair) cluster_sync();  // both CTAs' barriers are initialised before either signals the other
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
 
@@ -279,41 +308,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------- TMA producer ----------------
             const uint64_t pol_w = policy_evict_first();  // weights: streamed once
             const uint64_t pol_x = policy_evict_last();   // activation rows: read by every CTA
+            // A stage holds one k-block: this CTA's weight tile and its activation rows (all of
+            // them, or with pairs this CTA's half).  With pairs both CTAs' loads count on the even
+            // CTA's barrier, which expects the bytes of both.
+            auto expect = [&](int s) {
+                if (!kPair)
+                    mbar_arrive_expect_tx(&ctl->full[s], kABytes + b_bytes);
+                else if (rank == 0)
+                    mbar_arrive_expect_tx(&ctl->full[s], 2u * (kABytes + b_bytes));
+            };
+            auto load_w = [&](int s, int32_t kx, int32_t unit) {
+                uint8_t *dst = a_tiles + static_cast<size_t>(s) * kABytes;
+                if (kPair)
+                    tma_load_2d_pair(dst, &tmap_w, peer_addr(&ctl->full[s], 0), kx, (2 * unit + rank) * BM, pol_w);
+                else
+                    tma_load_2d(dst, &tmap_w, &ctl->full[s], kx, unit * BM, pol_w);
+            };
+            auto load_x = [&](int s, int32_t kx) {
+                uint8_t *dst = b_tiles + static_cast<size_t>(s) * b_bytes;
+                if (kPair)
+                    tma_load_2d_pair(dst, &tmap_x, peer_addr(&ctl->full[s], 0), kx, rank * (a.n_tile >> 1), pol_x);
+                else
+                    tma_load_2d(dst, &tmap_x, &ctl->full[s], kx, 0, pol_x);
+            };
             // The weights do not depend on the previous kernel: fill the whole ring with weight
             // tiles first, then wait for the previous kernel and add the activation slices.
             const int64_t n_pre = min(static_cast<int64_t>(stages), kb_end - kb_begin);
             for (int64_t i = 0; i < n_pre; ++i) {
                 const int64_t kb = kb_begin + i;
-                const int32_t tile = static_cast<int32_t>(div_nonneg(kb, nkb));
-                const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(tile) * nkb) * BK;
-                mbar_arrive_expect_tx(&ctl->full[i], kABytes + b_bytes);
-                tma_load_2d(a_tiles + static_cast<size_t>(i) * kABytes, &tmap_w, &ctl->full[i], kx,
-                            tile * BM, pol_w);
+                const int32_t unit = static_cast<int32_t>(div_nonneg(kb, nkb));
+                const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(unit) * nkb) * BK;
+                expect(static_cast<int>(i));
+                load_w(static_cast<int>(i), kx, unit);
                 issued |= 1u << i;
             }
             pdl_wait();
             for (int64_t i = 0; i < n_pre; ++i) {
                 const int64_t kb = kb_begin + i;
-                const int32_t tile = static_cast<int32_t>(div_nonneg(kb, nkb));
-                const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(tile) * nkb) * BK;
-                tma_load_2d(b_tiles + static_cast<size_t>(i) * b_bytes, &tmap_x, &ctl->full[i], kx, 0,
-                            pol_x);
+                const int32_t unit = static_cast<int32_t>(div_nonneg(kb, nkb));
+                const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(unit) * nkb) * BK;
+                load_x(static_cast<int>(i), kx);
             }
             uint32_t stage = static_cast<uint32_t>(n_pre % stages);
             uint32_t phase = (n_pre == stages) ? 1u : 0u;
             for (int64_t kb = kb_begin + n_pre; kb < kb_end; ++kb) {
-                const int32_t tile = static_cast<int32_t>(div_nonneg(kb, nkb));
-                const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(tile) * nkb) * BK;
+                const int32_t unit = static_cast<int32_t>(div_nonneg(kb, nkb));
+                const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(unit) * nkb) * BK;
                 if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
                     *abort_flag = 1;
                     latch(a.status, kDevTimeout);
                     break;
                 }
-                mbar_arrive_expect_tx(&ctl->full[stage], kABytes + b_bytes);
-                tma_load_2d(a_tiles + static_cast<size_t>(stage) * kABytes, &tmap_w,
-                            &ctl->full[stage], kx, tile * BM, pol_w);
-                tma_load_2d(b_tiles + static_cast<size_t>(stage) * b_bytes, &tmap_x,
-                            &ctl->full[stage], kx, 0, pol_x);
+                expect(static_cast<int>(stage));
+                load_w(static_cast<int>(stage), kx, unit);
+                load_x(static_cast<int>(stage), kx);
                 issued |= 1u << stage;
                 issued_parity = phase ? (issued_parity | (1u << stage))
                                       : (issued_parity & ~(1u << stage));
@@ -325,9 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer (single thread) ----------------
-            const uint32_t idesc = idesc_bf16_f32(BM, static_cast<uint32_t>(a.n_tile));
+        if (lane == 0 && rank == 0) {
+            // ---------------- MMA issuer (single thread; with pairs, the even CTA's) ----------------
+            const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * BM : BM, static_cast<uint32_t>(a.n_tile));
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int64_t kb = kb_begin; kb < kb_end && ok;) {
@@ -348,18 +396,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a0 = smem_u32(a_tiles + static_cast<size_t>(stage) * kABytes);
                     const uint32_t b0 = smem_u32(b_tiles + static_cast<size_t>(stage) * b_bytes);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_bf16_ss(d_tmem, sw128_kmajor_desc(a0 + kk * 32),
-                                    sw128_kmajor_desc(b0 + kk * 32), idesc,
-                                    (k > kb || kk > 0) ? 1u : 0u);
-                    mma_commit(&ctl->empty[stage]);
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        if (kPair)
+                            mma_bf16_ss_pair(d_tmem, sw128_kmajor_desc(a0 + kk * 32),
+                                             sw128_kmajor_desc(b0 + kk * 32), idesc,
+                                             (k > kb || kk > 0) ? 1u : 0u);
+                        else
+                            mma_bf16_ss(d_tmem, sw128_kmajor_desc(a0 + kk * 32),
+                                        sw128_kmajor_desc(b0 + kk * 32), idesc,
+                                        (k > kb || kk > 0) ? 1u : 0u);
+                    }
+                    if (kPair)
+                        mma_commit_pair_mc(&ctl->empty[stage], 3);  // the stage is free in both CTAs
+                    else
+                        mma_commit(&ctl->empty[stage]);
                     if (++stage == static_cast<uint32_t>(stages)) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                mma_commit(&ctl->acc_full[acc]);
+                if (kPair)
+                    mma_commit_pair_mc(&ctl->acc_full[acc], 3);  // each CTA drains its own 128 rows
+                else
+                    mma_commit(&ctl->acc_full[acc]);
                 acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
                 kb = k1;
@@ -379,8 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool first = true;
         int32_t gi = 0;  // 16-row groups sent by bulk stores
         for (int64_t kb = kb_begin; kb < kb_end;) {
-            const int32_t tile = static_cast<int32_t>(div_nonneg(kb, nkb));
-            const int64_t t0 = static_cast<int64_t>(tile) * nkb;
+            const int32_t unit = static_cast<int32_t>(div_nonneg(kb, nkb));
+            const int32_t tile = kPair ? 2 * unit + rank : unit;  // this CTA's 128-row tile
+            const int64_t t0 = static_cast<int64_t>(unit) * nkb;
             const int64_t k1 = min(kb_end, t0 + nkb);
             const bool full = (kb == t0) && (k1 == t0 + nkb);
             const bool got = mbar_wait(&ctl->acc_full[acc], acc_phase, abort_flag);
@@ -418,14 +479,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        acc * static_cast<uint32_t>(a.n_tile);
-                staged_fixup(a, &tmap_y, ctl, base, ring_bytes, out_stage, gi, tile, gf, gl, g, gf_second, t_row,
-                             threadIdx.x - 64, m_local, o, o_ok, bias_o, abort_flag);
+                staged_fixup(a, &tmap_y, ctl, base, ring_bytes, out_stage, gi, tile, gf, gl, g, gf_second, rank,
+                             t_row, threadIdx.x - 64, m_local, o, o_ok, bias_o, abort_flag);
             } else if (got) {
                 tc_fence_after();
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        acc * static_cast<uint32_t>(a.n_tile);
-                float *part = a.partials + static_cast<size_t>(g * 2 + (first ? 0 : 1)) *
-                                               a.n_tile * BM;
+                float *part = part_slot(a, g, first ? 0 : 1, rank);
                 // cluster-K: the accumulator goes to this CTA's ring (every stage is consumed)
                 float *stage_acc = reinterpret_cast<float *>(base);
                 for (int32_t n0 = 0; n0 < a.rows; n0 += 16) {
@@ -458,7 +518,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0 && got) mbar_arrive(&ctl->acc_empty[acc]);
+            if (lane == 0 && got) {
+                if (kPair)
+                    mbar_arrive_cluster(peer_addr(&ctl->acc_empty[acc], 0));  // the issuing CTA's
+                else
+                    mbar_arrive(&ctl->acc_empty[acc]);
+            }
             if (split && owner) {
                 if (threadIdx.x == 64) a.counters[tile] = 0;  // ready for the next launch
                 named_barrier_sync(1, 128);                  // ctl->is_last is reused
@@ -504,8 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int c = 0; c < kCtasPerBatch; ++c) {
                                 const int32_t gg = g0 + c;
                                 const int32_t slot = (gg == gf && gf_second) ? 1 : 0;
-                                const float *src =
-                                    a.partials + static_cast<size_t>(gg * 2 + slot) * a.n_tile * BM + m4;
+                                const float *src = part_slot(a, gg, slot, rank) + m4;
 #pragma unroll
                                 for (int j = 0; j < kRowsPerBatch; ++j) {
                                     const int32_t n = n0 + 4 * j;
@@ -560,13 +624,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Unwind after a timeout: let every copy and MMA this CTA started land before the CTA
         // exits and its shared and tensor memory are handed to another CTA.
         if (warp == 0 && lane == 0) {
-            for (int s = 0; s < stages; ++s)
-                if ((issued >> s) & 1u) mbar_wait(&ctl->full[s], (issued_parity >> s) & 1u, nullptr);
+            if (kPair && rank == 1) {
+                // this CTA's loads count on the other CTA's barriers, which it cannot wait on:
+                // give them a bounded time to land (a load takes microseconds)
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 200000ull) {
+                }
+            } else {
+                for (int s = 0; s < stages; ++s)
+                    if ((issued >> s) & 1u) mbar_wait(&ctl->full[s], (issued_parity >> s) & 1u, nullptr);
+            }
             if (ctl->fix_chunks > 0)
                 mbar_wait(&ctl->fix, static_cast<uint32_t>(ctl->fix_chunks - 1) & 1u, nullptr);
         }
-        if (warp == 1 && lane == 0) {
-            mma_commit(&ctl->drain);
+        if (warp == 1 && lane == 0 && rank == 0) {
+            if (kPair)
+                mma_commit_pair_mc(&ctl->drain, 1);
+            else
+                mma_commit(&ctl->drain);
             mbar_wait(&ctl->drain, 0, nullptr);
         }
         __syncwarp();
@@ -659,9 +734,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         cluster_sync();  // no CTA leaves while another still reads its shared memory
     }
+    if (kPair) {
+        // the issuing CTA's MMAs read this CTA's shared memory and write its tensor memory, and
+        // this CTA's epilogue arrives on the issuing CTA's barriers: neither leaves before the
+        // other is done
+        __syncwarp();
+        cluster_sync();
+    }
     if (warp == 1) {
         __syncwarp();
-        tmem_dealloc(tmem_base, static_cast<uint32_t>(a.tmem_cols));
+        if (kPair)
+            tmem_dealloc_pair(tmem_base, static_cast<uint32_t>(a.tmem_cols));
+        else
+            tmem_dealloc(tmem_base, static_cast<uint32_t>(a.tmem_cols));
     }
 }
 
@@ -677,9 +762,10 @@ __global__ void __launch_bounds__(256) linear_reduce_kernel(const LinearArgs a, 
     pdl_launch_dependents();  // dependents still wait for this grid to finish
     pdl_wait();
     const int32_t tile = blockIdx.x;
+    const int32_t unit = tile >> a.pair, rank = tile & a.pair;  // G counts workers (CTAs or pairs)
     const int64_t nkb = a.num_kb;
-    const int64_t total = static_cast<int64_t>(a.num_tiles) * nkb;
-    const int64_t t0 = static_cast<int64_t>(tile) * nkb;
+    const int64_t total = static_cast<int64_t>(a.num_wtiles) * nkb;
+    const int64_t t0 = static_cast<int64_t>(unit) * nkb;
     const int32_t gf = cta_of(t0, total, G), gl = cta_of(t0 + nkb - 1, total, G);
     if (gf == gl) return;  // one CTA computed the whole tile and wrote it
     const bool gf_second = div_nonneg(total * gf, G) < t0;
@@ -692,7 +778,7 @@ __global__ void __launch_bounds__(256) linear_reduce_kernel(const LinearArgs a, 
         for (int c = 0; c < kCtasPerBatch; ++c) {
             const int32_t gg = g0 + c;
             const int32_t slot = (gg == gf && gf_second) ? 1 : 0;
-            const float *src = a.partials + static_cast<size_t>(gg * 2 + slot) * a.n_tile * BM + m4;
+            const float *src = part_slot(a, gg, slot, rank) + m4;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int32_t n = blockIdx.y * kReduceRows + rsub + 8 * j;
@@ -862,7 +948,20 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     // sums are small), above it the partials and their sum would cost more than the idle SMs.
     p->cluster_k = rows > kLinearMaxFixupRows ? linear_cluster_k(p->num_tiles, p->num_kb, num_sms) : 1;
     if (p->cluster_k > 1) p->grid = p->num_tiles * p->cluster_k;
-    const size_t stage_bytes = kABytes + static_cast<size_t>(p->n_tile) * 128;
+    // CTA pairs (.cta_group::2) for stream-K above 16 rows when the tiles pair up: the split runs
+    // over pairs of adjacent tiles and the grid is twice the pairs
+    p->pair = 0;
+    p->num_wtiles = p->num_tiles;
+    if (rows > kLinearMaxFixupRows && p->cluster_k == 1 && p->num_tiles % 2 == 0) {
+        const int32_t pairs = linear_pair_workers(num_sms);
+        if (pairs > 0) {
+            p->pair = 1;
+            p->num_wtiles = p->num_tiles / 2;
+            const int64_t total_w = static_cast<int64_t>(p->num_kb) * p->num_wtiles;
+            p->grid = 2 * static_cast<int32_t>(total_w < pairs ? total_w : pairs);
+        }
+    }
+    const size_t stage_bytes = kABytes + static_cast<size_t>(p->n_tile >> p->pair) * 128;
     // above 16 rows (stream-K), outputs and partials leave in 16-row groups by bulk stores
     const bool want_y_tma = rows > kLinearMaxFixupRows && p->cluster_k == 1;
     p->out_stage_bytes = want_y_tma ? static_cast<int32_t>(kOutStageBytes) : 0;
@@ -884,7 +983,7 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     // whole tile's k-blocks (then a tile is shared by at most two CTAs, and the one that reaches
     // it at the end of its range finds the other's partial in and owns the sum), else by a
     // second launch.
-    const int64_t per_cta = total / p->grid;  // fewest k-blocks of any CTA
+    const int64_t per_cta = static_cast<int64_t>(p->num_kb) * p->num_wtiles / (p->grid >> p->pair);  // fewest of any worker
     p->owner_fix = (rows > kLinearMaxFixupRows && p->cluster_k == 1 && per_cta >= p->num_kb) ? 1 : 0;
     p->defer = (rows > kLinearMaxFixupRows && p->cluster_k == 1 && !p->owner_fix) ? 1 : 0;
     // cluster-K stages the accumulator (rows x 128 fp32) in the ring
@@ -904,7 +1003,7 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
                             stages * stage_bytes;
     p->y_tma = ((want_y_tma || ck_tma) && encode_plan_out(p, out)) ? 1 : 0;
     if (!encode_bf16_2d(&p->tmap_x, x, static_cast<uint64_t>(K), static_cast<uint64_t>(rows),
-                        static_cast<uint64_t>(ldx), BK, static_cast<uint32_t>(p->n_tile)))
+                        static_cast<uint64_t>(ldx), BK, static_cast<uint32_t>(p->n_tile >> p->pair)))
         return false;
     return true;
 }
@@ -940,7 +1039,7 @@ int32_t linear_cluster_k(int32_t num_tiles, int32_t num_kb, int32_t num_sms) {
                 cfg.attrs = attr;
                 cfg.numAttrs = 1;
                 int n = 0;
-                if (cudaOccupancyMaxActiveClusters(&n, linear_bf16_tc_kernel, &cfg) != cudaSuccess) {
+                if (cudaOccupancyMaxActiveClusters(&n, linear_bf16_tc_kernel<0>, &cfg) != cudaSuccess) {
                     cudaGetLastError();
                     n = 0;
                 }
@@ -953,11 +1052,50 @@ int32_t linear_cluster_k(int32_t num_tiles, int32_t num_kb, int32_t num_sms) {
     return 1;
 }
 
+// CTA pairs that can be resident at once (clusters of 2 with the largest shared-memory request),
+// at most half the SMs; 0 disables pairs (also when EAGLE_LINEAR_PAIR=0 is set in the
+// environment, to compare the two ways).  Checked once per device.
+int32_t linear_pair_workers(int32_t num_sms) {
+    static std::mutex mu;
+    static int cached[64] = {};  // 0 unknown, else max active pair clusters + 1
+    static const bool disabled = [] {
+        const char *e = std::getenv("EAGLE_LINEAR_PAIR");
+        return e != nullptr && e[0] == '0';
+    }();
+    if (disabled) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (prepare_kernels() != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kMaxDynSmem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, linear_bf16_tc_kernel<1>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        cached[dev] = n + 1;
+    }
+    const int32_t n = cached[dev] - 1;
+    return n < num_sms / 2 ? n : num_sms / 2;
+}
+
 cudaError_t prepare_kernels() {
-    cudaError_t e = cudaFuncSetAttribute(linear_bf16_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(linear_bf16_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kMaxDynSmem));
-    return e;
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(linear_bf16_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kMaxDynSmem));
 }
 
 void linear_retarget_out(LinearPlan *p, void *out) {
@@ -982,20 +1120,26 @@ cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
     a.defer = p.defer;
     a.cluster_k = p.cluster_k;
     a.owner_fix = p.owner_fix;
+    a.pair = p.pair;
+    a.num_wtiles = p.num_wtiles;
     a.y_tma = p.y_tma;
     a.out_stage_bytes = p.out_stage_bytes;
     a.partials = p.partials;
     a.counters = p.counters;
     a.status = p.status;
-    cudaError_t e = p.cluster_k > 1
-                        ? launch_pdl_cluster(linear_bf16_tc_kernel, dim3(p.grid), dim3(kThreads),
-                                             static_cast<unsigned>(p.cluster_k), p.smem_bytes, st, p.tmap_w,
-                                             p.tmap_x, p.tmap_y, a)
-                        : launch_pdl(linear_bf16_tc_kernel, dim3(p.grid), dim3(kThreads), p.smem_bytes, st,
-                                     p.tmap_w, p.tmap_x, p.tmap_y, a);
+    cudaError_t e;
+    if (p.pair)
+        e = launch_pdl_cluster(linear_bf16_tc_kernel<1>, dim3(p.grid), dim3(kThreads), 2u, p.smem_bytes, st,
+                               p.tmap_w, p.tmap_x, p.tmap_y, a);
+    else if (p.cluster_k > 1)
+        e = launch_pdl_cluster(linear_bf16_tc_kernel<0>, dim3(p.grid), dim3(kThreads),
+                               static_cast<unsigned>(p.cluster_k), p.smem_bytes, st, p.tmap_w, p.tmap_x, p.tmap_y, a);
+    else
+        e = launch_pdl(linear_bf16_tc_kernel<0>, dim3(p.grid), dim3(kThreads), p.smem_bytes, st, p.tmap_w,
+                       p.tmap_x, p.tmap_y, a);
     if (e != cudaSuccess || !p.defer) return e;
     return launch_pdl(linear_reduce_kernel, dim3(p.num_tiles, (p.rows + kReduceRows - 1) / kReduceRows),
-                      dim3(256), 0, st, a, p.grid);
+                      dim3(256), 0, st, a, p.grid >> p.pair);
 }
 
 cudaError_t launch_linear_f32(const float *w, int64_t ldw, const float *x, int64_t ldx,

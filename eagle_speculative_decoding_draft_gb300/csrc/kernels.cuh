@@ -86,6 +86,8 @@ struct LinearPlan {
     int32_t defer;     // rows > kLinearMaxFixupRows: a second launch sums the split tiles
     int32_t cluster_k; // > 1: split-K over clusters of this many CTAs per tile, summed on chip
     int32_t owner_fix; // > 16 rows, at most two CTAs per tile: summed in the launch by its owner
+    int32_t pair;      // CTA pairs on .cta_group::2 (clusters of 2; grid = 2 x pairs)
+    int32_t num_wtiles;  // units of the stream-K split: tiles, or pairs of tiles
     int32_t y_tma;     // outputs and partials leave by bulk stores (16-row groups)
     int32_t out_stage_bytes;  // their shared-memory staging
     float *partials;   // [grid][2][n_tile][128]
@@ -99,6 +101,8 @@ size_t linear_counters_bytes(int32_t M);
 int32_t linear_n_tile(int32_t rows);
 // CTAs per tile of the cluster split-K (1: stream-K over one CTA per SM).
 int32_t linear_cluster_k(int32_t num_tiles, int32_t num_kb, int32_t num_sms);
+// CTA pairs of the .cta_group::2 mode that fit on the device at once (0: the mode is off).
+int32_t linear_pair_workers(int32_t num_sms);
 
 // Fills `plan` (tensor maps included).  Returns false on an unusable argument (alignment,
 // strides, sizes) or when the driver's tensor-map encoder is unavailable.

@@ -41,12 +41,17 @@ def bf16_tensor(rng, shape, std):
 # Ragged M and K, 1..256 rows (padded to the MMA's N in steps of 16), M below one 128-row tile.
 # Above 16 rows every way of summing split tiles: cluster-K for few tiles ((4096, 8192), (777, 1000):
 # clusters of 8, (70, 4104): one tile, ragged K slices), the owner's fix-up with bulk stores when
-# every CTA covers a whole tile ((20000, 512), (20000, 520) with a ragged last k-block), and the
-# second launch otherwise ((12000, 2048): 94 tiles of 32 k-blocks over 152 CTAs).
+# every CTA covers a whole tile ((20000, 512), (20000, 520) with a ragged last k-block: 157 tiles,
+# one CTA each), and the second launch otherwise.  With an even tile count stream-K runs on CTA
+# pairs (.cta_group::2, M = 256): (32000, 4096) at 17, 64 and 256 rows (the LM head: the owner's
+# fix-up), (12000, 2048, 24) (47 pairs of tiles over 76 pairs: the second launch), (130, 72, 255)
+# (one pair of tiles split over two pairs with 255 rows, the largest ragged N) and (20480, 520, 40)
+# (160 tiles, ragged last k-block).
 LINEAR_CASES = [(128, 64, 1), (200, 200, 17), (1000, 512, 256), (300, 64, 33), (128, 128, 16),
                 (4096, 8192, 10), (32000, 4096, 10), (777, 1000, 100), (130, 72, 255),
                 (4096, 8192, 256), (300, 64, 64), (513, 1000, 49), (70, 4104, 80), (2000, 2048, 128),
-                (20000, 512, 40), (20000, 520, 200), (12000, 2048, 24)]
+                (20000, 512, 40), (20000, 520, 200), (12000, 2048, 24), (32000, 4096, 256),
+                (32000, 4096, 17), (32000, 4096, 64), (20480, 520, 40)]
 
 
 @pytest.mark.parametrize("M,K,rows", LINEAR_CASES)
@@ -242,3 +247,36 @@ def test_verify_walk_and_greedy_are_bit_exact(dev):
     assert np.array_equal(to_np(out["accept_nodes"]), ref["accept_nodes"])
     assert np.array_equal(to_np(out["accept_tokens"]), ref["accept_tok"])
     assert ref["accept_len"].max() >= 3  # the planted agreements make long paths
+
+
+@pytest.mark.parametrize("V", [6, 32000])
+def test_verify_greedy_with_bf16_target_logits_is_bit_exact(dev, V):
+    """eagle_verify_greedy on bf16 target logits (the dtype a bf16 target model emits): the
+    arg-max over bf16 values, ties to the lowest id (rounding to bf16 makes ties common), against
+    the oracle's walk over the same values widened to fp32."""
+    from eagle_speculative_decoding_draft_gb300.engine import EagleTree
+    rng = np.random.default_rng(V)
+    B, d, k, m = 16, 4, 3, 9
+    n = m + 1
+    w = synth.custom(32, V, B, d, k, m, dtype="bf16")
+    inp = synth.make_inputs(w, seed=V + 1)
+    g = lambda t: t.to(dev).contiguous()
+    eng = EagleTree(g(inp.w_fc), g(inp.b_fc), g(inp.w_lm), g(inp.emb), B, d, k, m)
+    tree = eng.draft(g(inp.root_feat), g(inp.root_tok))
+    tok, par = to_np(tree["tokens"]), to_np(tree["parents"])
+    T = (rng.standard_normal((B, n, V)) * 0.05).astype(np.float32)  # coarse bf16 grid: many ties
+    for b in range(B):
+        for i in range(n):
+            kids = np.nonzero(par[b] == i)[0]
+            if kids.size and rng.random() < 0.8:
+                T[b, i, tok[b, rng.choice(kids)]] = 0.25  # ties with any other 0.25 in the row
+                T[b, i, rng.integers(0, V)] = 0.25
+    Tb = torch.from_numpy(T).to(torch.bfloat16)
+    ver = eng.verify_greedy(tree["tokens"], tree["parents"], g(Tb))
+    torch.cuda.synchronize()
+    ref = oracle.verify_greedy(tok, par, Tb.float().numpy(), d)
+    assert np.array_equal(to_np(ver["accept_len"]), ref["accept_len"])
+    assert np.array_equal(to_np(ver["accept_nodes"]), ref["accept_nodes"])
+    assert np.array_equal(to_np(ver["accept_tokens"]), ref["accept_tok"])
+    eng.status()
+    eng.close()
