@@ -278,16 +278,16 @@ def gamma32(n):
     return n * u / (1 - n * u)
 
 
-_ABS_W = {}
+_ABS_W = {"w": None, "abs": None}
 
 
 def fc_absdot(inp, x):
-    """sum_i |W_fc[o][i]| |x_i| for every output o (float64), |W_fc| kept per input set."""
-    key = id(inp.w_fc)
-    if key not in _ABS_W:
-        _ABS_W.clear()
-        _ABS_W[key] = np.abs(inp.w_fc.float().numpy()).astype(np.float32)
-    return (_ABS_W[key] @ np.abs(x).astype(np.float32)).astype(np.float64) * (1 + 1e-6)
+    """sum_i |W_fc[o][i]| |x_i| for every output o (float64), |W_fc| kept for the last weight
+    tensor seen (held by reference, so a new tensor at a reused address is not mistaken for it)."""
+    if _ABS_W["w"] is not inp.w_fc:
+        _ABS_W["w"] = inp.w_fc
+        _ABS_W["abs"] = np.abs(inp.w_fc.float().numpy()).astype(np.float32)
+    return (_ABS_W["abs"] @ np.abs(x).astype(np.float32)).astype(np.float64) * (1 + 1e-6)
 
 
 def emb_row(inp, tok):

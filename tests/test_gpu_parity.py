@@ -228,14 +228,22 @@ EDGE = [
     dict(h=64, V=300, B=2, d=16, k=16, m=3856, dtype="f32"),   # largest pool kept whole: 3857 nodes
     dict(h=64, V=400, B=2, d=32, k=11, m=1000, dtype="f32"),   # maximum depth
     dict(h=64, V=300, B=2, d=32, k=1, m=32, dtype="bf16"),     # 32-level chain
+    # every LM-head row the same: every logit of a row ties, so the top-k from the LM head's
+    # per-tile statistics (80 rows) gathers more candidates than it holds and takes its exact
+    # fallback; ties go to the lowest id everywhere
+    dict(h=64, V=3000, B=20, d=3, k=4, m=10, dtype="bf16", tie=True),
+    dict(h=64, V=1000, B=20, d=3, k=16, m=40, dtype="bf16", tie=True),
 ]
 
 
-@pytest.mark.parametrize("case", EDGE, ids=lambda c: "h{h}V{V}B{B}d{d}k{k}m{m}{dtype}".format(**c))
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: "h{h}V{V}B{B}d{d}k{k}m{m}{dtype}".format(**c)
+                         + ("ties" if c.get("tie") else ""))
 def test_edge_shapes(dev, case):
     w = synth.custom(case["h"], case["V"], case["B"], case["d"], case["k"], case["m"],
                      dtype=case["dtype"])
     inp = synth.make_inputs(w, seed=case["h"] + case["V"] + case["B"])
+    if case.get("tie"):
+        inp.w_lm[:] = inp.w_lm[0].clone()
     exact, diverged = run_case(dev, w, inp)
     assert exact >= 1 or w.batch <= 1, f"no request checked exactly: {diverged}"
 
