@@ -546,7 +546,7 @@ static eagle_status level_tail(eagle_tree *t, int32_t level, float *d_logits_out
     }
     // log-softmax + top-k children of every row
     EAGLE_CUDA(launch_row_topk(lg, 0, R, V, V, L.kk, t->at<int32_t>(L.row_ids), t->at<float>(L.row_logp),
-                               t->at<float>(L.row_lse), st));
+                               t->at<float>(L.row_lse), st, t->status));
     ++t->launches;
     if (t->is_static) {
         // the nodes of depth level+1 take their ranked tokens; those with children get their rows
@@ -807,7 +807,7 @@ eagle_status eagle_verify_greedy(eagle_tree *t, const int32_t *d_tokens, const i
     if (d_target_logits) {
         int32_t *gw = t->at<int32_t>(t->L.g);
         EAGLE_CUDA(launch_row_topk(d_target_logits, target_dtype == EAGLE_BF16, c.batch * n, c.vocab, c.vocab, 1,
-                                   gw, nullptr, nullptr, st));
+                                   gw, nullptr, nullptr, st, t->status));
         ++t->launches;
         g = gw;
     }

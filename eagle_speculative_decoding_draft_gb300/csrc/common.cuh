@@ -378,6 +378,15 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // Wait until the kernels this one depends on have completed and flushed their memory.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// 2^x by the special-function unit's approximation (ex2.approx.ftz: relative error near 2^-22,
+// results below 2^-126 flushed to zero): one instruction, for sums of exponentials where the
+// terms' own rounding is far below the sum's.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // (value, index) ranks before (value2, index2): value descending, index ascending.
 __device__ __forceinline__ bool ranks_before(float a, int32_t ia, float b, int32_t ib) {
     return a > b || (a == b && ia < ib);

@@ -123,11 +123,14 @@ cudaError_t launch_linear_f32(const float *w, int64_t ldw, const float *x, int64
                               int32_t rows, cudaStream_t st);
 
 // ---------------------------------------------------------------------------------------------
-// Per-row log-softmax + top-k (k <= 16), or argmax (k = 1, lse == null); one CTA per row.
+// Per-row log-softmax + top-k (k <= 16), or argmax (k = 1, lse == null): a thread-block cluster
+// per row holding the row in registers, or, for at least as many rows as SMs with rows of at
+// least 32 KB, one CTA per row streaming it once through shared memory.  `status` (may be null)
+// receives kDevTimeout if a streamed copy does not land in time.
 // ---------------------------------------------------------------------------------------------
 cudaError_t launch_row_topk(const void *logits, int32_t is_bf16, int32_t rows, int32_t V,
                             int64_t ld, int32_t k, int32_t *ids, float *vals, float *lse,
-                            cudaStream_t st);
+                            cudaStream_t st, int32_t *status = nullptr);
 
 // ---------------------------------------------------------------------------------------------
 // Tree kernels

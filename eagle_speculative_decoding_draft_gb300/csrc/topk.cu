@@ -362,11 +362,318 @@ cudaError_t launch_typed(const T *logits, int32_t rows, int32_t V, int64_t ld, i
                               st, logits, V, ld, k, ids, vals, lse);
 }
 
+// ---------------------------------------------------------------------------------------------
+// Streaming row top-k for many long rows (rows at least the SM count, rows of at least 32 KB):
+// one CTA a row reads it once, through a ring of 16 KB bulk copies (cp.async.bulk) into shared
+// memory.  Warp 0 is the producer: it refills a stage as soon as the 16 consumer warps have
+// released it (an mbarrier each way, no block-wide barrier in the loop), so the copies run ahead
+// of the consumers by the whole ring.  Each consumer warp, with no barrier but its own:
+//   lse     every thread sums exp(x - c) over its elements against its own offset c (its first
+//           element, raised by rescaling only when an element exceeds it by more than 2^4); the
+//           threads' (c, sum) pairs are merged by warps, then over the warps in a fixed order;
+//   top k   the warp appends every element at or above its threshold to its own buffer (a
+//           ballot a round, no atomics); when the buffer could overflow it keeps only its k best
+//           (each entry ranked by counting, value descending, column ascending) and raises its
+//           threshold to the k-th.  A row's top-k element is within its warp's k best,
+//           so the warps' final k best, ranked the same way, give the row's top k exactly,
+//           whatever the ties.
+// k = 1 without the logsumexp (greedy verification's arg-max) keeps one best element a thread.
+// ---------------------------------------------------------------------------------------------
+constexpr int kStreamConsumers = 512;
+constexpr int kStreamWarps = kStreamConsumers / 32;
+constexpr int kStreamThreads = kStreamConsumers + 32;  // + the producer warp
+constexpr uint32_t kChunkBytes = 16384;
+constexpr int kStreamStages = 6;
+constexpr int kWarpCap = 64;  // a warp's candidate buffer
+
+struct StreamSmem {
+    uint64_t full[kStreamStages];
+    uint64_t empty[kStreamStages];
+    float w_m[kStreamWarps], w_s[kStreamWarps], w_t[kStreamWarps];
+    int32_t w_i[kStreamWarps];
+    int32_t abort;
+    float b_v[kStreamWarps][kWarpCap];  // the warps' candidates
+    int32_t b_i[kStreamWarps][kWarpCap];
+};
+
+// Keeps the k best of the warp's n <= 64 buffered entries (value descending, column ascending),
+// in rank order at the front of the buffer; returns how many remain (min(n, k)) and sets thr to
+// the k-th kept value when k are kept (-inf otherwise).  An element equal to it may still rank
+// before it (a lower column appended later in the same round), so the filter is x >= thr and the
+// next compaction settles the tie.
+__device__ __forceinline__ int32_t warp_keep_best(float *bv, int32_t *bi, int32_t n, int32_t k, int32_t lane,
+                                                  float &thr) {
+    const float v0 = lane < n ? bv[lane] : -INFINITY, v1 = lane + 32 < n ? bv[lane + 32] : -INFINITY;
+    const int32_t i0 = lane < n ? bi[lane] : INT_MAX, i1 = lane + 32 < n ? bi[lane + 32] : INT_MAX;
+    int32_t r0 = 0, r1 = 0;
+    for (int32_t j = 0; j < n; ++j) {
+        const float u = bv[j];
+        const int32_t ui = bi[j];
+        r0 += ranks_before(u, ui, v0, i0) ? 1 : 0;
+        r1 += ranks_before(u, ui, v1, i1) ? 1 : 0;
+    }
+    __syncwarp();
+    if (lane < n && r0 < k) {
+        bv[r0] = v0;
+        bi[r0] = i0;
+    }
+    if (lane + 32 < n && r1 < k) {
+        bv[r1] = v1;
+        bi[r1] = i1;
+    }
+    __syncwarp();
+    const int32_t kept = n < k ? n : k;
+    thr = (kept == k) ? bv[k - 1] : -INFINITY;
+    return kept;
+}
+
+template <typename T, bool kBestOnly>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+    row_topk_stream_kernel(const T *__restrict__ logits, int32_t V, int64_t ld, int32_t k, int32_t *__restrict__ ids,
+                           float *__restrict__ vals, float *__restrict__ lse_out, int32_t *status) {
+    constexpr int EPV = 16 / sizeof(T);
+    constexpr float kLog2e = 1.4426950408889634f;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *ring = smem_raw + (((raw_addr + 127u) & ~127u) - raw_addr);
+    StreamSmem *sm = reinterpret_cast<StreamSmem *>(ring + kStreamStages * kChunkBytes);
+    pdl_launch_dependents();  // dependents still wait for this grid to finish
+    const int32_t row = blockIdx.x, lane = threadIdx.x & 31, warp = static_cast<int32_t>(threadIdx.x >> 5) - 1;
+    const T *z = logits + static_cast<int64_t>(row) * ld;
+    const uint32_t row_bytes = static_cast<uint32_t>(V) * sizeof(T);
+    const int32_t nchunk = static_cast<int32_t>((row_bytes + kChunkBytes - 1) / kChunkBytes);
+    const bool want_lse = lse_out != nullptr;
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kStreamStages; ++st) {
+            mbar_init(&sm->full[st], 1);
+            mbar_init(&sm->empty[st], kStreamWarps);
+        }
+        sm->abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_wait();  // the logits come from the previous kernel
+
+    if (warp < 0) {
+        // ---------------- producer: one thread refills each stage once the consumers release it ----
+        if (lane == 0) {
+            for (int32_t c = 0; c < nchunk; ++c) {
+                const int st = c % kStreamStages;
+                if (c >= kStreamStages &&
+                    !mbar_wait(&sm->empty[st], static_cast<uint32_t>(c / kStreamStages - 1) & 1u, &sm->abort)) {
+                    sm->abort = 1;
+                    latch(status, kDevTimeout);
+                    break;
+                }
+                const uint32_t off = static_cast<uint32_t>(c) * kChunkBytes;
+                const uint32_t bytes = min(kChunkBytes, row_bytes - off);
+                if (c >= kStreamStages) fence_proxy_async_smem();  // the consumers' reads, then the copy
+                mbar_arrive_expect_tx(&sm->full[st], bytes);
+                bulk_load(ring + st * kChunkBytes, reinterpret_cast<const uint8_t *>(z) + off, bytes, &sm->full[st]);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- 16 consumer warps ----------------
+        const int32_t tid = static_cast<int32_t>(threadIdx.x) - 32;
+        float *wbv = sm->b_v[warp];
+        int32_t *wbi = sm->b_i[warp];
+        int32_t wn = 0;            // entries in this warp's buffer (the same in every lane)
+        float thr = -INFINITY;     // this warp's threshold: an element below it cannot be in its k best
+        float cof = -INFINITY, ssum = 0.0f;
+        float bv = -INFINITY;  // arg-max only
+        int32_t bi = INT_MAX;
+        for (int32_t c = 0; c < nchunk; ++c) {
+            const int st = c % kStreamStages;
+            // one lane polls the stage's barrier while the others wait at the warp barrier (which
+            // also orders the copy's bytes before their reads)
+            int32_t got = 1;
+            if (lane == 0) got = mbar_wait(&sm->full[st], static_cast<uint32_t>(c / kStreamStages) & 1u, &sm->abort);
+            got = __shfl_sync(kFullMask, got, 0);
+            __syncwarp();
+            if (!got) {
+                sm->abort = 1;
+                latch(status, kDevTimeout);
+            }
+            if (sm->abort) break;
+            const uint32_t bytes = min(kChunkBytes, row_bytes - static_cast<uint32_t>(c) * kChunkBytes);
+            const int32_t nv = static_cast<int32_t>(bytes / 16u);
+            const int32_t col0 = c * static_cast<int32_t>(kChunkBytes / sizeof(T));
+            const uint8_t *stage = ring + st * kChunkBytes;
+            for (int32_t v0 = warp * 32; v0 < nv; v0 += kStreamConsumers) {  // warp-uniform trips
+                const int32_t v = v0 + lane;
+                const bool have = v < nv;
+                float x[EPV];
+                float cmax = -INFINITY;
+                if (have) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(stage + v * 16);
+                    const T *e = reinterpret_cast<const T *>(&raw);
+#pragma unroll
+                    for (int j = 0; j < EPV; ++j) {
+                        x[j] = to_f32(e[j]);
+                        cmax = fmaxf(cmax, x[j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < EPV; ++j) x[j] = -INFINITY;
+                }
+                if (kBestOnly) {
+                    // a thread visits ascending columns: an equal value later ranks after its best
+                    if (cmax > bv) {
+#pragma unroll
+                        for (int j = 0; j < EPV; ++j)
+                            if (x[j] > bv) {
+                                bv = x[j];
+                                bi = col0 + v * EPV + j;
+                            }
+                    }
+                    continue;
+                }
+                if (want_lse && have) {
+                    if (cmax > cof + 16.0f) {  // keep the terms below 2^23: rescale to the new max
+                        ssum = (cof == -INFINITY) ? 0.0f : ssum * ex2_approx((cof - cmax) * kLog2e);
+                        cof = cmax;
+                    }
+                    const float cl = cof * kLog2e;
+#pragma unroll
+                    for (int j = 0; j < EPV; ++j) ssum += ex2_approx(fmaf(x[j], kLog2e, -cl));
+                }
+                if (__any_sync(kFullMask, have && cmax >= thr)) {
+#pragma unroll
+                    for (int j = 0; j < EPV; ++j) {
+                        bool in = have && x[j] >= thr;
+                        uint32_t ball = __ballot_sync(kFullMask, in);
+                        if (ball == 0u) continue;
+                        if (wn + __popc(ball) > kWarpCap) {
+                            // full: keep the warp's k best, raise the threshold, vote again
+                            wn = warp_keep_best(wbv, wbi, wn, k, lane, thr);
+                            in = have && x[j] >= thr;
+                            ball = __ballot_sync(kFullMask, in);
+                            if (ball == 0u) continue;
+                        }
+                        if (in) {
+                            const int32_t pos = wn + __popc(ball & ((1u << lane) - 1u));
+                            wbv[pos] = x[j];
+                            wbi[pos] = col0 + v * EPV + j;
+                        }
+                        wn += __popc(ball);
+                        __syncwarp();
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm->empty[st]);  // this warp is done with the stage
+        }
+        if (!sm->abort) {
+            if (kBestOnly) {
+                warp_best(bv, bi);
+                if (lane == 0) {
+                    sm->w_t[warp] = bv;
+                    sm->w_i[warp] = bi;
+                }
+            } else {
+                wn = warp_keep_best(wbv, wbi, wn, k, lane, thr);
+                if (lane == 0) sm->w_i[warp] = wn;
+                float wm = cof, ws = ssum;
+                warp_lse(wm, ws);
+                if (lane == 0) {
+                    sm->w_m[warp] = wm;
+                    sm->w_s[warp] = ws;
+                }
+            }
+        }
+    }
+    __syncthreads();  // also: every copy landed (the consumers waited on each) unless aborted
+    if (sm->abort) {
+        // let the copies in flight land before the CTA's shared memory is released
+        if (threadIdx.x == 0) {
+            const uint64_t t0 = global_timer_ns();
+            while (global_timer_ns() - t0 < 200000ull) {
+            }
+        }
+        __syncthreads();
+        return;
+    }
+    const int32_t tid = static_cast<int32_t>(threadIdx.x);  // all 544 threads from here
+    if (kBestOnly) {
+        if (tid == 0) {
+            float v = sm->w_t[0];
+            int32_t i = sm->w_i[0];
+            for (int w = 1; w < kStreamWarps; ++w)
+                if (ranks_before(sm->w_t[w], sm->w_i[w], v, i)) {
+                    v = sm->w_t[w];
+                    i = sm->w_i[w];
+                }
+            ids[row] = i;
+            if (vals) vals[row] = v;
+        }
+        return;
+    }
+    float M = -INFINITY, S = 0.0f;
+    for (int w = 0; w < kStreamWarps; ++w) lse_merge(M, S, sm->w_m[w], sm->w_s[w]);
+    const float lse = want_lse ? M + logf(S) : 0.0f;  // without it the values are the logits
+    // the warps' k best (at most 16 x 16 entries): each ranked by counting the others
+    if (tid < kStreamWarps * k) {
+        const int32_t w = tid / k, e = tid - w * k;
+        if (e < sm->w_i[w]) {
+            const float v = sm->b_v[w][e];
+            const int32_t c = sm->b_i[w][e];
+            int32_t rank = 0;
+            for (int32_t w2 = 0; w2 < kStreamWarps; ++w2)
+                for (int32_t e2 = 0; e2 < sm->w_i[w2]; ++e2)
+                    rank += ranks_before(sm->b_v[w2][e2], sm->b_i[w2][e2], v, c) ? 1 : 0;
+            if (rank < k) {
+                ids[static_cast<int64_t>(row) * k + rank] = c;
+                if (vals) vals[static_cast<int64_t>(row) * k + rank] = v - lse;
+            }
+        }
+    }
+    if (tid == 0 && want_lse) lse_out[row] = lse;
+}
+
+constexpr size_t kStreamSmem = 128 + kStreamStages * kChunkBytes + sizeof(StreamSmem);
+
+template <typename T>
+cudaError_t launch_stream(const T *logits, int32_t rows, int32_t V, int64_t ld, int32_t k, int32_t *ids,
+                          float *vals, float *lse, int32_t *status, cudaStream_t st) {
+    static bool attr_set[64][4] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    auto go = [&](auto kernel, int slot) -> cudaError_t {
+        if (dev >= 0 && dev < 64 && !attr_set[dev][slot]) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(kStreamSmem));
+            if (e != cudaSuccess) return e;
+            attr_set[dev][slot] = true;
+        }
+        return launch_pdl(kernel, dim3(rows), dim3(kStreamThreads), kStreamSmem, st, logits, V, ld, k, ids, vals,
+                          lse, status);
+    };
+    if (k == 1 && lse == nullptr) return go(row_topk_stream_kernel<T, true>, 0);
+    return go(row_topk_stream_kernel<T, false>, 1);
+}
+
+// The streaming kernel serves many long rows whose starts and lengths suit 16-byte bulk copies:
+// the arg-max from 32 KB rows on, the top k with the logsumexp from 2^16 elements on (below that
+// the cluster kernel, which holds the row in registers, is faster: each warp's first candidates
+// and the exp of every element cost more than its second read of a short row).
+bool stream_suits(const void *logits, int32_t esize, int32_t rows, int32_t V, int64_t ld, bool best_only) {
+    const int64_t bytes = static_cast<int64_t>(V) * esize;
+    return rows >= sms_of_current_device() && bytes >= 32768 && (best_only || V >= 65536) && bytes % 16 == 0 &&
+           (ld * esize) % 16 == 0 && (reinterpret_cast<uintptr_t>(logits) % 16) == 0;
+}
+
 }  // namespace
 
 cudaError_t launch_row_topk(const void *logits, int32_t is_bf16, int32_t rows, int32_t V, int64_t ld,
-                            int32_t k, int32_t *ids, float *vals, float *lse, cudaStream_t st) {
+                            int32_t k, int32_t *ids, float *vals, float *lse, cudaStream_t st, int32_t *status) {
     if (rows < 1) return cudaSuccess;
+    if (k >= 1 && k <= 16 && stream_suits(logits, is_bf16 ? 2 : 4, rows, V, ld, k == 1 && lse == nullptr)) {
+        if (is_bf16)
+            return launch_stream(reinterpret_cast<const __nv_bfloat16 *>(logits), rows, V, ld, k, ids, vals, lse,
+                                 status, st);
+        return launch_stream(reinterpret_cast<const float *>(logits), rows, V, ld, k, ids, vals, lse, status, st);
+    }
     if (is_bf16)
         return launch_typed(reinterpret_cast<const __nv_bfloat16 *>(logits), rows, V, ld, k, ids, vals, lse, st);
     return launch_typed(reinterpret_cast<const float *>(logits), rows, V, ld, k, ids, vals, lse, st);

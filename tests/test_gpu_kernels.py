@@ -103,9 +103,15 @@ def test_linear_split_sums_do_not_depend_on_the_row_count(dev, M, K):
         assert torch.equal(wide, widest[:64])
 
 
+# At least as many rows as SMs, rows of 2^16 elements or more (and 16-byte aligned rows) take the
+# streaming kernel: (200, 128256, 8), (160, 65536, 16) in bf16, (160, 70000, 1) with the
+# logsumexp; their strided variants (row stride not a multiple of 16 bytes) the cluster one, as do
+# (256, 32000, 4) (shorter rows).  The arg-max without the logsumexp streams from 32 KB rows on
+# (test_verify_*).
 TOPK_CASES = [(10, 32000, 10, "f32"), (3, 1000, 16, "f32"), (4, 128256, 8, "f32"),
               (5, 77, 4, "f32"), (2, 33, 1, "bf16"), (4, 5000, 2, "bf16"), (6, 1024, 2, "f32"),
-              (300, 2048, 4, "f32"), (1, 16, 16, "f32")]
+              (300, 2048, 4, "f32"), (1, 16, 16, "f32"), (256, 32000, 4, "f32"), (200, 128256, 8, "f32"),
+              (160, 65536, 16, "bf16"), (160, 70000, 1, "f32")]
 
 
 @pytest.mark.parametrize("rows,V,k,dt", TOPK_CASES)
@@ -139,13 +145,16 @@ def test_row_topk_matches_oracle(dev, rows, V, k, dt, strided):
 
 
 @pytest.mark.parametrize("V,k,dt", [(32000, 10, "f32"), (1000, 16, "f32"), (128256, 16, "f32"),
-                                    (32000, 1, "bf16"), (4099, 7, "bf16")])
+                                    (32000, 1, "bf16"), (4099, 7, "bf16"), (65536, 8, "bf16")])
 def test_row_topk_massive_ties(dev, V, k, dt):
     """Thousands of entries tie at the top: the candidate lists overflow and every slice falls
-    back to exact passes; ties go to the lower column."""
+    back to exact passes; ties go to the lower column.  With 160 rows of 2^16 elements or more
+    the streaming kernel takes them: its warps' buffers fill with ties and settle them by column
+    at each compaction."""
     from eagle_speculative_decoding_draft_gb300.engine import row_topk
     rng = np.random.default_rng(V + k)
-    z = rng.integers(0, 3, size=(4, V)).astype(np.float32)
+    nrows = 160 if V >= 65536 and V % 8 == 0 else 4
+    z = rng.integers(0, 3, size=(nrows, V)).astype(np.float32)
     z[1] = 0.0  # one constant row
     z[2, ::5] = 3.0
     zt = torch.from_numpy(z)
