@@ -6,6 +6,7 @@ any entry point raises, there is no other implementation to fall back to.
 from __future__ import annotations
 
 import ctypes
+import os
 import threading
 from ctypes import POINTER, c_int, c_int32, c_int64, c_size_t, c_void_p
 from pathlib import Path
@@ -107,11 +108,15 @@ _lib = None
 
 
 def load(path: Path | None = None):
-    """The loaded CUDA library with typed entry points.  Raises if it has not been built."""
+    """The loaded CUDA library with typed entry points.  Raises if it has not been built.
+
+    The environment variable EAGLE_TREE_LIB, when set, names another build of the same library
+    to load instead (the tests use it for the checking build)."""
     global _lib
     with _lock:
         if _lib is None:
-            p = Path(path) if path else LIB_PATH
+            override = os.environ.get("EAGLE_TREE_LIB")
+            p = Path(path) if path else (Path(override) if override else LIB_PATH)
             if not p.exists():
                 raise RuntimeError(
                     f"{p} is missing: build the CUDA library first "

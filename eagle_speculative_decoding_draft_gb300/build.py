@@ -16,6 +16,10 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 OUT_DIR = PKG / "lib"
 LIB = OUT_DIR / "libeagle_tree.so"
+# the same library with the device-side checks of the kernels' own index invariants
+# (-DEAGLE_CHECKS): a separate build, used by the tests
+CHECKS_DIR = OUT_DIR / "checks"
+CHECKS_LIB = CHECKS_DIR / "libeagle_tree.so"
 SOURCES = ["api.cu", "gemm.cu", "topk.cu", "tree.cu", "sample.cu", "noalloc.cu", "decoder.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -26,20 +30,25 @@ def nvcc() -> str:
     return str(p) if p.exists() else "nvcc"
 
 
-def _stale() -> bool:
-    if not LIB.exists():
+def _stale(lib: Path = LIB) -> bool:
+    if not lib.exists():
         return True
-    t = LIB.stat().st_mtime
+    t = lib.stat().st_mtime
     deps = list(CSRC.glob("*.cu")) + list(CSRC.glob("*.cuh")) + [ROOT / "include" / "eagle_tree.h",
                                                                   Path(__file__)]
     return any(d.stat().st_mtime > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> Path:
-    if not force and not _stale():
-        return LIB
-    OUT_DIR.mkdir(exist_ok=True)
-    obj_dir = OUT_DIR / "obj"
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checks: bool = False) -> Path:
+    """Compiles the library (or, with checks, its checking variant) unless it is up to date;
+    returns its path."""
+    out_dir, lib = (CHECKS_DIR, CHECKS_LIB) if checks else (OUT_DIR, LIB)
+    if checks:
+        extra_flags = (*extra_flags, "-DEAGLE_CHECKS")
+    if not force and not _stale(lib):
+        return lib
+    out_dir.mkdir(parents=True, exist_ok=True)
+    obj_dir = out_dir / "obj"
     obj_dir.mkdir(exist_ok=True)
     common = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               f"-I{ROOT / 'include'}", *extra_flags]
@@ -56,14 +65,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> Path:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB.with_suffix(f".so.tmp{os.getpid()}")
+    tmp = lib.with_suffix(f".so.tmp{os.getpid()}")
     cmd = [nvcc(), *ARCH, "-shared", "-o", str(tmp), *map(str, objs)]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
         raise RuntimeError("nvcc link failed")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -838,6 +838,8 @@ eagle_status eagle_tree_node_logits(eagle_tree *t, const void *d_root_feature, f
         const int32_t rows = std::min(L.node_chunk, total - r0);
         GatherArgs g{rows, h, V, L.eb, t->at<int32_t>(L.node_src) + r0, t->at<int32_t>(L.node_tok) + r0,
                      d_root_feature, t->ws + L.fhat, c.embedding, nx, t->status, nullptr};
+        g.src_rows = c.depth * L.r_pad;  // node sources index every level's f^ rows, or a root
+        g.root_rows = c.batch;
         EAGLE_CUDA(launch_gather(g, st));
         ++t->launches;
         float *out = d_node_logits + static_cast<int64_t>(r0) * V;

@@ -40,6 +40,23 @@ __device__ __forceinline__ void latch(int32_t *status, int32_t bits) {
     if (status) atomicOr(status, bits);
 }
 
+// Checks of the library's own index invariants (a candidate's parent, a producing row, a split-K
+// slot, a tile ticket), compiled in by -DEAGLE_CHECKS: a failed check latches kDevBounds and the
+// caller skips or clamps the access.  Without it the checks are constant true and cost nothing;
+// indices that come from the caller are checked in every build.
+#ifdef EAGLE_CHECKS
+constexpr bool kChecks = true;
+#else
+constexpr bool kChecks = false;
+#endif
+__device__ __forceinline__ bool dcheck(bool cond, int32_t *status) {
+    if (kChecks && !cond) {
+        latch(status, kDevBounds);
+        return false;
+    }
+    return true;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

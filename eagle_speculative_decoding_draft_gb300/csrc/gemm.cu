@@ -79,6 +79,7 @@ struct LinearArgs {
     int32_t cluster_k;  // > 1: split-K over a cluster of this many CTAs per tile (no stream-K)
     int32_t owner_fix;  // split tiles summed in the launch by the CTA that finds its partner done
     int32_t pair;       // 1: CTA pairs (.cta_group::2), the stream-K split over pairs of tiles
+    int32_t slots;      // partial-sum slots of the launch: two per CTA of the main kernel
     int32_t num_wtiles; // units of the stream-K split: tiles, or pairs of tiles when pair
     int32_t y_tma;      // 16-row groups of Y and of partials go out by bulk stores (tmap_y valid)
     int32_t out_stage_bytes;  // shared-memory staging of those groups (after the ring)
@@ -103,7 +104,9 @@ __device__ __forceinline__ int32_t cta_of(int64_t p, int64_t total, int32_t G) {
 // A worker's partial sums of one of its (at most two) split tiles: slot 0 for the tile its range
 // starts in, 1 for the one it ends in; with CTA pairs each CTA of the pair (rank) has its own.
 __device__ __forceinline__ float *part_slot(const LinearArgs &a, int32_t worker, int32_t slot, int32_t rank) {
-    return a.partials + static_cast<size_t>((((worker * 2 + slot) << a.pair) + rank)) * a.n_tile * BM;
+    int32_t i = ((worker * 2 + slot) << a.pair) + rank;
+    if (!dcheck(i >= 0 && i < a.slots, a.status)) i = 0;
+    return a.partials + static_cast<size_t>(i) * a.n_tile * BM;
 }
 
 __device__ __forceinline__ void store_y(const LinearArgs &a, int32_t r, int32_t o, float v) {
@@ -449,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *abort_flag = 1;
                 latch(a.status, kDevTimeout);
             }
+            dcheck(tile < a.num_tiles, a.status);  // a phantom tile would overrun the tickets
             const int32_t o = tile * BM + m_local;
             const bool o_ok = o < a.M;
             const float bias_o = (a.bias != nullptr && o_ok) ? __bfloat162float(a.bias[o]) : 0.0f;
@@ -569,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int c = 0; c < kCtasPerBatch; ++c) {
                                 const int32_t gg = g0 + c;
                                 const int32_t slot = (gg == gf && gf_second) ? 1 : 0;
-                                const float *src = part_slot(a, gg, slot, rank) + m4;
+                                const float *src = (gg <= gl) ? part_slot(a, gg, slot, rank) + m4 : a.partials;
 #pragma unroll
                                 for (int j = 0; j < kRowsPerBatch; ++j) {
                                     const int32_t n = n0 + 4 * j;
@@ -778,7 +782,7 @@ __global__ void __launch_bounds__(256) linear_reduce_kernel(const LinearArgs a, 
         for (int c = 0; c < kCtasPerBatch; ++c) {
             const int32_t gg = g0 + c;
             const int32_t slot = (gg == gf && gf_second) ? 1 : 0;
-            const float *src = part_slot(a, gg, slot, rank) + m4;
+            const float *src = (gg <= gl) ? part_slot(a, gg, slot, rank) + m4 : a.partials;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int32_t n = blockIdx.y * kReduceRows + rsub + 8 * j;
@@ -1122,6 +1126,7 @@ cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
     a.owner_fix = p.owner_fix;
     a.pair = p.pair;
     a.num_wtiles = p.num_wtiles;
+    a.slots = 2 * p.grid;
     a.y_tma = p.y_tma;
     a.out_stage_bytes = p.out_stage_bytes;
     a.partials = p.partials;

@@ -194,6 +194,8 @@ struct GatherArgs {
     void *x;
     int32_t *status;
     int32_t *tok_copy;  // [n_rows] receives tok as given, or null
+    int32_t src_rows = 0;   // rows of fhat_all and of root_feat (checking builds), 0: not checked
+    int32_t root_rows = 0;
 };
 cudaError_t launch_gather(const GatherArgs &a, cudaStream_t st);
 

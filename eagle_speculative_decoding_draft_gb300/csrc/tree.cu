@@ -54,7 +54,11 @@ __global__ void __launch_bounds__(kExpandThreads) expand_kernel(const ExpandArgs
             S = a.front_S_in[b * k + s] + a.row_logp[static_cast<int64_t>(row) * k + j];
             par = a.front_cand_in[b * k + s];
             c = k + (a.level - 1) * kk + t;
+            // the frontier holds candidates of the previous level
+            if (!dcheck(par >= (a.level == 1 ? 0 : k + (a.level - 2) * kk) && par < k + (a.level - 1) * kk, a.status))
+                par = 0;
         }
+        if (!dcheck(c < a.n_cand, a.status)) c = 0;
         if (tok < 0 || tok >= a.V) {
             latch(a.status, kDevBounds);
             tok = 0;
@@ -79,6 +83,8 @@ __global__ void __launch_bounds__(kExpandThreads) expand_kernel(const ExpandArgs
         for (int32_t u = 0; u < nl; ++u) rank += ranks_before(sS[u], sC[u], sS[t], sC[t]) ? 1 : 0;
         if (rank < k) slot[rank] = t;
     }
+    __syncthreads();
+    if (t < k && !dcheck(slot[t] >= 0 && slot[t] < nl, a.status)) slot[t] = 0;  // every rank < k is taken
     __syncthreads();
     if (blockIdx.y == 0 && t < k) {
         a.front_cand_out[b * k + t] = sC[slot[t]];
@@ -264,8 +270,11 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(const BuildAr
         a.positions[ob + ti] = dep + pos0;
         if (a.logscore) a.logscore[ob + ti] = sS[c];
         if (a.node_tok) a.node_tok[ob + ti] = tok;
-        if (a.node_src && a.pool_row)
-            a.node_src[ob + ti] = (dep - 1) * a.r_pad + a.pool_row[pb + c];
+        if (a.node_src && a.pool_row) {
+            int32_t prow = a.pool_row[pb + c];
+            if (!dcheck(prow >= 0 && prow < a.r_pad && dep >= 1 && dep <= a.d, a.status)) prow = 0;
+            a.node_src[ob + ti] = (dep - 1) * a.r_pad + prow;
+        }
     }
     __syncthreads();
     // ancestor-only mask, LSB-first bits: walk up the parents (strictly decreasing indices)
@@ -332,7 +341,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
     pdl_launch_dependents();  // dependents still wait for this grid to finish
     pdl_wait();
     const int32_t r = blockIdx.x;
-    const int32_t si = a.src ? a.src[r] : -1 - r;
+    int32_t si = a.src ? a.src[r] : -1 - r;
+    // a source row: f^ row si of the handle's levels, or root feature -1 - si
+    if (a.src_rows > 0 && !dcheck(si < a.src_rows && -1 - si < a.root_rows, a.status)) si = -1;
     int32_t tok = a.tok[r];
     if (a.tok_copy && blockIdx.y == 0 && threadIdx.x == 0) a.tok_copy[r] = tok;
     if (tok < 0 || tok >= a.V) {

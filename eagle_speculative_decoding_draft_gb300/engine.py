@@ -49,10 +49,11 @@ class EagleTree:
     """
 
     def __init__(self, w_fc, b_fc, w_lm, emb, batch: int, depth: int, topk: int, num_keep: int,
-                 static_spec=None):
+                 static_spec=None, workspace=None):
         """static_spec: None for the dynamic EAGLE-2 tree, or an EAGLE-1 static shape as
         [(parent, rank), ...] for drafted nodes 1..N (then depth and num_keep must be its depth
-        and N; topk is not used)."""
+        and N; topk is not used).  workspace: a uint8 CUDA tensor of at least the workspace size
+        (256-byte aligned) to use instead of a fresh one."""
         self.lib = _lib.load()
         dt = w_fc.dtype
         for name, t in (("w_fc", w_fc), ("w_lm", w_lm), ("emb", emb)):
@@ -84,7 +85,12 @@ class EagleTree:
                 nbytes = self.lib.eagle_tree_workspace_bytes_static(ctypes.byref(self.cfg), sp.shape[0], spp)
             if nbytes == 0:
                 raise ValueError("invalid draft-tree configuration")
-            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+            if workspace is None:
+                self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+            else:
+                if workspace.dtype != torch.uint8 or workspace.numel() < nbytes:
+                    raise ValueError(f"workspace must be uint8 with at least {nbytes} bytes")
+                self.workspace = _need(workspace, "workspace")
             h = ctypes.c_void_p()
             if self.static_spec is None:
                 check(self.lib.eagle_tree_init(ctypes.byref(self.cfg),
