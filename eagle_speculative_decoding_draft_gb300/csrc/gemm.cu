@@ -22,14 +22,7 @@
 //   bulk stores above 16 rows every 16-row group of outputs or partials is assembled in shared
 //               memory and leaves by one bulk store (TMA tensor store into Y, 1-D bulk store of
 //               partials) instead of per-thread stores to rows far apart;
-//   cluster-K   above 16 rows, when the weight tiles are few (at most half the SMs: the FC,
-//               M = h), the grid is tiles x C CTAs in thread-block clusters of C; CTA r of a
-//               cluster takes the r-th slice of the tile's k-blocks, stages its fp32 accumulator
-//               in its own (then idle) ring, and after a cluster barrier sums a 1/C share of the
-//               tile's outputs over the C CTAs in rank order through distributed shared memory,
-//               written by one TMA store: no partials in global memory, no tickets, no second
-//               launch;
-//   CTA pairs   above 16 rows, with an even number of weight tiles and stream-K, the CTAs run as
+//   CTA pairs   above 16 rows, with an even number of weight tiles, the CTAs run as
 //               pairs (clusters of 2) on tcgen05 with .cta_group::2: one MMA of M = 256 covers
 //               the pair's two adjacent weight tiles, each CTA streams its own tile's weights and
 //               half of the activation rows, and the MMA reads both halves from the two CTAs'
@@ -76,7 +69,6 @@ struct LinearArgs {
     int64_t ldo;
     int32_t out_bf16;
     int32_t defer;  // split tiles: write partials only; linear_reduce_kernel sums them
-    int32_t cluster_k;  // > 1: split-K over a cluster of this many CTAs per tile (no stream-K)
     int32_t owner_fix;  // split tiles summed in the launch by the CTA that finds its partner done
     int32_t pair;       // 1: CTA pairs (.cta_group::2), the stream-K split over pairs of tiles
     int32_t slots;      // partial-sum slots of the launch: two per CTA of the main kernel
@@ -262,13 +254,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t nkb = a.num_kb;
     const int64_t total = static_cast<int64_t>(a.num_wtiles) * nkb;
     int64_t kb_begin = div_nonneg(total * g, G), kb_end = div_nonneg(total * (g + 1), G);
-    const int32_t CK = a.cluster_k;
-    if (CK > 1) {  // tile g / CK, k-slice g % CK (the CTA's rank in its cluster)
-        const int64_t t0 = static_cast<int64_t>(g / CK) * nkb;
-        const int32_t r = g % CK;
-        kb_begin = t0 + (nkb * r) / CK;
-        kb_end = t0 + (nkb * (r + 1)) / CK;
-    }
 
     pdl_launch_dependents();
     if (threadIdx.x == 0) {
@@ -460,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // at its last segment that finds every other CTA's ticket in (usually: the head of a
             // tile whose tail the next CTA computed first) owns the sum and takes its own values
             // straight from TMEM; the other CTAs leave partials and tickets.
-            const bool split = !full && !a.defer && CK == 1;
+            const bool split = !full && !a.defer;
             int32_t gf = g, gl = g;
             bool owner = false;
             if (split) {
@@ -490,14 +475,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        acc * static_cast<uint32_t>(a.n_tile);
                 float *part = part_slot(a, g, first ? 0 : 1, rank);
-                // cluster-K: the accumulator goes to this CTA's ring (every stage is consumed)
-                float *stage_acc = reinterpret_cast<float *>(base);
                 for (int32_t n0 = 0; n0 < a.rows; n0 += 16) {
                     uint32_t r[16];
                     __syncwarp();
                     tmem_ld_16(t_row + static_cast<uint32_t>(n0), r);
                     tmem_wait_ld();
-                    if (a.y_tma && CK == 1) {  // a whole tile into Y, or this CTA's partial
+                    if (a.y_tma) {  // a whole tile into Y, or this CTA's partial
                         float v[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) + (full ? bias_o : 0.0f);
@@ -509,9 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int32_t n = n0 + j;
                         if (n < a.rows) {
                             const float v = __uint_as_float(r[j]);
-                            if (CK > 1) {
-                                stage_acc[static_cast<size_t>(n) * BM + m_local] = v;
-                            } else if (full) {
+                            if (full) {
                                 if (o_ok) store_y(a, n, o, v + bias_o);
                             } else {
                                 part[static_cast<size_t>(n) * BM + m_local] = v;
@@ -652,91 +633,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-    }
-    if (CK > 1) {
-        // Every CTA of the cluster reaches both barriers, also after a timeout (then the sums
-        // are garbage, and the status word says so).  CTA r adds, for weight rows
-        // 128 r / CK .. 128 (r + 1) / CK - 1 of the tile and every row, the C staged accumulators
-        // in rank order, four outputs per thread and step, reading them through distributed
-        // shared memory.
-        __syncwarp();
-        cluster_sync();
-        if (warp >= 2 && !*abort_flag) {
-            const int32_t et = static_cast<int32_t>(threadIdx.x) - 64;
-            const int32_t rank = g % CK, tile = g / CK;
-            const int32_t share = BM / CK;      // columns of this CTA's share of the tile
-            const int32_t per = share / 4;      // 4-wide groups of it, per row
-            const int32_t groups = per * a.rows;
-            const float *stage_acc = reinterpret_cast<const float *>(base);
-            // with y_tma the sums are assembled behind the staged accumulator ([row][share], Y's
-            // type) and leave by one TMA store
-            uint8_t *out_stage = base + ((static_cast<size_t>(a.n_tile) * BM * 4 + 1023) & ~static_cast<size_t>(1023));
-            constexpr int kUnroll = 8;
-            for (int32_t e0 = et; e0 < groups; e0 += 128 * kUnroll) {
-                // peer by peer (rank order), the loads of all kUnroll groups in flight together
-                float4 sum[kUnroll];
-                for (int32_t c = 0; c < CK; ++c) {
-                    float4 v[kUnroll];
-#pragma unroll
-                    for (int u = 0; u < kUnroll; ++u) {
-                        const int32_t e = e0 + u * 128;
-                        const int32_t n = e / per, m4 = rank * share + (e % per) * 4;
-                        v[u] = (e < groups) ? ld_peer_v4(peer_addr(stage_acc + static_cast<size_t>(n) * BM + m4, c))
-                                            : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                    }
-#pragma unroll
-                    for (int u = 0; u < kUnroll; ++u) {
-                        if (c == 0) {
-                            sum[u] = v[u];
-                        } else {
-                            sum[u].x += v[u].x;
-                            sum[u].y += v[u].y;
-                            sum[u].z += v[u].z;
-                            sum[u].w += v[u].w;
-                        }
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int32_t e = e0 + u * 128;
-                    if (e >= groups) continue;
-                    const int32_t n = e / per, q4 = (e % per) * 4, m4 = rank * share + q4;
-                    float v[4] = {sum[u].x, sum[u].y, sum[u].z, sum[u].w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int32_t o = tile * BM + m4 + q;
-                        v[q] += (a.bias != nullptr && o < a.M) ? __bfloat162float(a.bias[o]) : 0.0f;
-                    }
-                    if (a.y_tma) {
-                        const size_t at = static_cast<size_t>(n) * share + q4;
-                        if (a.out_bf16) {
-                            __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(
-                                reinterpret_cast<__nv_bfloat16 *>(out_stage) + at);
-                            ob[0] = __floats2bfloat162_rn(v[0], v[1]);
-                            ob[1] = __floats2bfloat162_rn(v[2], v[3]);
-                        } else {
-                            *reinterpret_cast<float4 *>(reinterpret_cast<float *>(out_stage) + at) =
-                                make_float4(v[0], v[1], v[2], v[3]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (tile * BM + m4 + q < a.M) store_y(a, n, tile * BM + m4 + q, v[q]);
-                    }
-                }
-            }
-            if (a.y_tma) {
-                fence_proxy_async_smem();  // the writes above, before the TMA store reads them
-                named_barrier_sync(1, 128);
-                if (et == 0) {  // rows >= rows and columns >= M fall outside the tensor map
-                    tma_store_2d(&tmap_y, out_stage, tile * BM + rank * share, 0);
-                    bulk_commit();
-                    bulk_wait_all();
-                }
-            }
-        }
-        __syncwarp();
-        cluster_sync();  // no CTA leaves while another still reads its shared memory
     }
     if (kPair) {
         // the issuing CTA's MMAs read this CTA's shared memory and write its tensor memory, and
@@ -913,13 +809,10 @@ bool encode_out_2d(CUtensorMap *map, const void *ptr, int32_t out_bf16, uint64_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The output map of a plan: {128, 16} boxes for the stream-K epilogue's 16-row groups, or one box
-// of {128 / C columns, n_tile rows} for a cluster-K CTA's share of its tile.
+// The output map of a plan: {128, 16} boxes for the epilogue's 16-row groups.
 bool encode_plan_out(LinearPlan *p, const void *out) {
-    const bool ck = p->cluster_k > 1;
     return encode_out_2d(&p->tmap_y, out, p->out_bf16, static_cast<uint64_t>(p->M), static_cast<uint64_t>(p->rows),
-                         static_cast<uint64_t>(p->ldo), ck ? static_cast<uint32_t>(BM / p->cluster_k) : BM,
-                         ck ? static_cast<uint32_t>(p->n_tile) : 16u);
+                         static_cast<uint64_t>(p->ldo), BM, 16u);
 }
 
 }  // namespace
@@ -948,15 +841,11 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     p->num_tiles = (M + BM - 1) / BM;
     const int64_t total = static_cast<int64_t>(p->num_kb) * p->num_tiles;
     p->grid = static_cast<int32_t>(total < num_sms ? total : num_sms);
-    // Cluster-K above 16 rows only: up to 16 rows stream-K on every SM is faster (the split-K
-    // sums are small), above it the partials and their sum would cost more than the idle SMs.
-    p->cluster_k = rows > kLinearMaxFixupRows ? linear_cluster_k(p->num_tiles, p->num_kb, num_sms) : 1;
-    if (p->cluster_k > 1) p->grid = p->num_tiles * p->cluster_k;
     // CTA pairs (.cta_group::2) for stream-K above 16 rows when the tiles pair up: the split runs
     // over pairs of adjacent tiles and the grid is twice the pairs
     p->pair = 0;
     p->num_wtiles = p->num_tiles;
-    if (rows > kLinearMaxFixupRows && p->cluster_k == 1 && p->num_tiles % 2 == 0) {
+    if (rows > kLinearMaxFixupRows && p->num_tiles % 2 == 0) {
         const int32_t pairs = linear_pair_workers(num_sms);
         if (pairs > 0) {
             p->pair = 1;
@@ -967,7 +856,7 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     }
     const size_t stage_bytes = kABytes + static_cast<size_t>(p->n_tile >> p->pair) * 128;
     // above 16 rows (stream-K), outputs and partials leave in 16-row groups by bulk stores
-    const bool want_y_tma = rows > kLinearMaxFixupRows && p->cluster_k == 1;
+    const bool want_y_tma = rows > kLinearMaxFixupRows;
     p->out_stage_bytes = want_y_tma ? static_cast<int32_t>(kOutStageBytes) : 0;
     size_t stages = (kMaxDynSmem - 1024 - sizeof(SmemCtl) - p->out_stage_bytes) / stage_bytes;
     if (stages > kMaxStages) stages = kMaxStages;
@@ -988,72 +877,19 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     // it at the end of its range finds the other's partial in and owns the sum), else by a
     // second launch.
     const int64_t per_cta = static_cast<int64_t>(p->num_kb) * p->num_wtiles / (p->grid >> p->pair);  // fewest of any worker
-    p->owner_fix = (rows > kLinearMaxFixupRows && p->cluster_k == 1 && per_cta >= p->num_kb) ? 1 : 0;
-    p->defer = (rows > kLinearMaxFixupRows && p->cluster_k == 1 && !p->owner_fix) ? 1 : 0;
-    // cluster-K stages the accumulator (rows x 128 fp32) in the ring
-    if (p->cluster_k > 1 && static_cast<size_t>(p->n_tile) * BM * sizeof(float) > stages * stage_bytes)
-        return false;
+    p->owner_fix = (rows > kLinearMaxFixupRows && per_cta >= p->num_kb) ? 1 : 0;
+    p->defer = (rows > kLinearMaxFixupRows && !p->owner_fix) ? 1 : 0;
     p->partials = partials;
     p->counters = counters;
     p->status = status;
     if (!encode_bf16_2d(&p->tmap_w, w, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
                         static_cast<uint64_t>(ldw), BK, BM))
         return false;
-    // cluster-K writes each CTA's share of its tile with one TMA store from the idle ring, behind
-    // the staged accumulator (n_tile rows x 128 fp32) when both fit
-    const size_t ck_out = static_cast<size_t>(p->n_tile) * (BM / p->cluster_k) * (out_bf16 ? 2 : 4);
-    const bool ck_tma = p->cluster_k > 1 &&
-                        ((static_cast<size_t>(p->n_tile) * BM * 4 + 1023) & ~static_cast<size_t>(1023)) + ck_out <=
-                            stages * stage_bytes;
-    p->y_tma = ((want_y_tma || ck_tma) && encode_plan_out(p, out)) ? 1 : 0;
+    p->y_tma = (want_y_tma && encode_plan_out(p, out)) ? 1 : 0;
     if (!encode_bf16_2d(&p->tmap_x, x, static_cast<uint64_t>(K), static_cast<uint64_t>(rows),
                         static_cast<uint64_t>(ldx), BK, static_cast<uint32_t>(p->n_tile >> p->pair)))
         return false;
     return true;
-}
-
-// Split-K over thread-block clusters when the weight tiles are at most half the SMs: C CTAs per
-// tile (a power of two, at most 8, at least 2 k-blocks each), used only when every cluster of the
-// launch can be resident at once with the largest shared-memory request (checked once per C and
-// device).  Results are bit-identical among launches of 1-16 rows and among launches of 17-256.
-int32_t linear_cluster_k(int32_t num_tiles, int32_t num_kb, int32_t num_sms) {
-    int32_t c = 1;
-    while (c < 8 && num_tiles * (2 * c) <= num_sms && num_kb >= 2 * (2 * c)) c *= 2;
-    if (c == 1) return 1;
-    static std::mutex mu;
-    static int cached[64][4] = {};  // [device][log2 C - 1]: 0 unknown, else max active clusters + 1
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-    if (prepare_kernels() != cudaSuccess) return 1;  // the occupancy query needs the smem attribute
-    for (; c > 1; c /= 2) {
-        const int slot = (c == 2) ? 0 : (c == 4) ? 1 : 2;
-        int active;
-        {
-            std::lock_guard<std::mutex> lock(mu);
-            if (cached[dev][slot] == 0) {
-                cudaLaunchConfig_t cfg = {};
-                cfg.gridDim = dim3(num_tiles * c);
-                cfg.blockDim = dim3(kThreads);
-                cfg.dynamicSmemBytes = kMaxDynSmem;
-                cudaLaunchAttribute attr[1];
-                attr[0].id = cudaLaunchAttributeClusterDimension;
-                attr[0].val.clusterDim.x = c;
-                attr[0].val.clusterDim.y = 1;
-                attr[0].val.clusterDim.z = 1;
-                cfg.attrs = attr;
-                cfg.numAttrs = 1;
-                int n = 0;
-                if (cudaOccupancyMaxActiveClusters(&n, linear_bf16_tc_kernel<0>, &cfg) != cudaSuccess) {
-                    cudaGetLastError();
-                    n = 0;
-                }
-                cached[dev][slot] = n + 1;
-            }
-            active = cached[dev][slot] - 1;
-        }
-        if (active >= num_tiles) return c;
-    }
-    return 1;
 }
 
 // CTA pairs that can be resident at once (clusters of 2 with the largest shared-memory request),
@@ -1122,7 +958,6 @@ cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
     a.ldo = p.ldo;
     a.out_bf16 = p.out_bf16;
     a.defer = p.defer;
-    a.cluster_k = p.cluster_k;
     a.owner_fix = p.owner_fix;
     a.pair = p.pair;
     a.num_wtiles = p.num_wtiles;
@@ -1136,9 +971,6 @@ cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
     if (p.pair)
         e = launch_pdl_cluster(linear_bf16_tc_kernel<1>, dim3(p.grid), dim3(kThreads), 2u, p.smem_bytes, st,
                                p.tmap_w, p.tmap_x, p.tmap_y, a);
-    else if (p.cluster_k > 1)
-        e = launch_pdl_cluster(linear_bf16_tc_kernel<0>, dim3(p.grid), dim3(kThreads),
-                               static_cast<unsigned>(p.cluster_k), p.smem_bytes, st, p.tmap_w, p.tmap_x, p.tmap_y, a);
     else
         e = launch_pdl(linear_bf16_tc_kernel<0>, dim3(p.grid), dim3(kThreads), p.smem_bytes, st, p.tmap_w,
                        p.tmap_x, p.tmap_y, a);

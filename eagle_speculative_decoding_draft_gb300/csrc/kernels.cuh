@@ -64,9 +64,10 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
 // The weight matrix is cut into 128-row tiles and 64-wide k-blocks; the k-blocks of all tiles
 // form one stream that is split evenly over a persistent grid (one CTA per SM).  A tile whose
 // k-blocks land in more than one CTA is summed in ascending CTA order (deterministic) by the last
-// CTA to arrive, by the CTA that finds its partner done, or by a second launch; few-tile GEMMs
-// above 16 rows split each tile's k-blocks over a thread-block cluster and sum on chip instead.
-// A row's result is bit-identical among launches of 1-16 rows and among launches of 17-256.
+// CTA to arrive, by the CTA that finds its partner done, or by a second launch.  Above 16 rows,
+// when the tiles pair up, the CTAs run as pairs sharing one M = 256 MMA (.cta_group::2) and the
+// stream runs over pairs of tiles.  A row's result is bit-identical among launches of 1-16 rows
+// and among launches of 17-256.
 // ---------------------------------------------------------------------------------------------
 constexpr int kLinearTileM = 128;
 constexpr int kLinearTileK = 64;
@@ -84,7 +85,6 @@ struct LinearPlan {
     int64_t ldo;
     int32_t out_bf16;
     int32_t defer;     // rows > kLinearMaxFixupRows: a second launch sums the split tiles
-    int32_t cluster_k; // > 1: split-K over clusters of this many CTAs per tile, summed on chip
     int32_t owner_fix; // > 16 rows, at most two CTAs per tile: summed in the launch by its owner
     int32_t pair;      // CTA pairs on .cta_group::2 (clusters of 2; grid = 2 x pairs)
     int32_t num_wtiles;  // units of the stream-K split: tiles, or pairs of tiles
@@ -99,8 +99,6 @@ struct LinearPlan {
 size_t linear_partials_bytes(int32_t grid, int32_t n_tile);
 size_t linear_counters_bytes(int32_t M);
 int32_t linear_n_tile(int32_t rows);
-// CTAs per tile of the cluster split-K (1: stream-K over one CTA per SM).
-int32_t linear_cluster_k(int32_t num_tiles, int32_t num_kb, int32_t num_sms);
 // CTA pairs of the .cta_group::2 mode that fit on the device at once (0: the mode is off).
 int32_t linear_pair_workers(int32_t num_sms);
 

@@ -510,9 +510,7 @@ EAGLE_API eagle_status eagle_decoder_layer(const eagle_decoder_layer_weights *w,
  *     first call on a device looks its address up (cudaGetSymbolAddress, with that device
  *     current) and sets the kernel's attributes; make that first call before any stream capture.
  *   - Limits: rows <= 32 and out_features <= 131072; larger sizes return EAGLE_ERR_INVALID_ARG.
- *     The stream-K split runs at most 160 CTAs, which bounds the partial sums the array holds;
- *     few-tile shapes split K over thread-block clusters instead (more CTAs, no partials: they
- *     use only the cleared tickets).
+ *     The split runs on at most 160 CTAs, which bounds the partial sums the array holds.
  *   - Results: on a GPU with at most 160 SMs the split is the one eagle_linear_bf16 uses, so
  *     the two entry points agree bit for bit; with more SMs the split differs and they agree
  *     within the GEMM's fp32 rounding bound.

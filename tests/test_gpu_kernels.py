@@ -39,14 +39,14 @@ def bf16_tensor(rng, shape, std):
 
 
 # Ragged M and K, 1..256 rows (padded to the MMA's N in steps of 16), M below one 128-row tile.
-# Above 16 rows every way of summing split tiles: cluster-K for few tiles ((4096, 8192), (777, 1000):
-# clusters of 8, (70, 4104): one tile, ragged K slices), the owner's fix-up with bulk stores when
-# every CTA covers a whole tile ((20000, 512), (20000, 520) with a ragged last k-block: 157 tiles,
-# one CTA each), and the second launch otherwise.  With an even tile count stream-K runs on CTA
-# pairs (.cta_group::2, M = 256): (32000, 4096) at 17, 64 and 256 rows (the LM head: the owner's
-# fix-up), (12000, 2048, 24) (47 pairs of tiles over 76 pairs: the second launch), (130, 72, 255)
-# (one pair of tiles split over two pairs with 255 rows, the largest ragged N) and (20480, 520, 40)
-# (160 tiles, ragged last k-block).
+# Above 16 rows every way of summing split tiles: the owner's fix-up with bulk stores when every
+# worker covers a whole tile ((20000, 512), (20000, 520) with a ragged last k-block: 157 tiles,
+# one CTA each) and the second launch otherwise ((4096, 8192) and (777, 1000): few tiles, long K;
+# (70, 4104): one tile, ragged K).  With an even tile count the CTAs run as pairs (.cta_group::2,
+# M = 256): (32000, 4096) at 17, 64 and 256 rows (the LM head: the owner's fix-up), (4096, 8192)
+# at 256 rows and (2000, 2048, 128) (the FC's shape class: the second launch), (12000, 2048, 24),
+# (130, 72, 255) (one pair of tiles split over two pairs with 255 rows, the largest ragged N) and
+# (20480, 520, 40) (160 tiles, ragged last k-block).
 LINEAR_CASES = [(128, 64, 1), (200, 200, 17), (1000, 512, 256), (300, 64, 33), (128, 128, 16),
                 (4096, 8192, 10), (32000, 4096, 10), (777, 1000, 100), (130, 72, 255),
                 (4096, 8192, 256), (300, 64, 64), (513, 1000, 49), (70, 4104, 80), (2000, 2048, 128),
@@ -84,8 +84,8 @@ def test_linear_within_fp32_bound_of_oracle(dev, M, K, rows, out_bf16):
 def test_linear_split_sums_do_not_depend_on_the_row_count(dev, M, K):
     """A row's result depends on the split of the k-blocks only, which is the same for every
     launch of 1-16 rows (stream-K, the last CTA of a split tile sums the partials) and for every
-    launch of 17-256 rows (cluster-K for few weight tiles, else stream-K with the sum by the
-    tile's owner or a second launch, all adding the same partials in the same CTA order)."""
+    launch of 17-256 rows (stream-K on single CTAs or CTA pairs, with the sum by the tile's
+    owner or a second launch, both adding the same partials in the same CTA order)."""
     from eagle_speculative_decoding_draft_gb300.engine import linear_bf16
     rng = np.random.default_rng(M + K)
     W = bf16_tensor(rng, (M, K), 1 / np.sqrt(K)).to(dev)

@@ -7,11 +7,11 @@ C ABI twice in a row and checks each result against the oracle's fp32 dot produc
 the allocating entry point (eagle_linear_bf16, with a scratch buffer from torch), both within the
 fp32 dot-product bound used by the other GEMM tests; on a GPU with at most 160 SMs the two entry
 points split the work identically, so there they must also agree bit for bit.  The shapes cover
-every way the array is used: stream-K with the in-launch fix-up (10 rows), one row, cluster-K
-(few weight tiles: only the cleared tickets), and 17-32 rows over 250 weight tiles, which fills
-the whole partials region and needs the tickets reset between the two calls.  It also checks that
-oversize requests are refused.  It sits in a file that pytest collects last and passes both alone
-and after the other tests.
+every way the array is used: stream-K with the in-launch fix-up (10 rows), one row, few weight
+tiles with a second launch summing the partials (777 x 1000 at 32 rows), and 17-32 rows over 250
+weight tiles on CTA pairs, which fills the whole partials region and needs the tickets reset
+between the two calls.  It also checks that oversize requests are refused.  It sits in a file
+that pytest collects last and passes both alone and after the other tests.
 """
 import ctypes
 
