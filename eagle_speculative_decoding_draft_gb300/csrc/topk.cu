@@ -394,7 +394,49 @@ struct StreamSmem {
     int32_t abort;
     float b_v[kStreamWarps][kWarpCap];  // the warps' candidates
     int32_t b_i[kStreamWarps][kWarpCap];
+    float seed[kStreamWarps][16];  // each warp's k largest lane maxima of the first chunk
+    float t0;                      // the k-th largest of them all: the warps' first threshold
 };
+
+// Sorts one value a lane across the warp, largest first (bitonic network over the lanes).
+__device__ __forceinline__ float warp_sort_desc(float x, int32_t lane) {
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const float o = __shfl_xor_sync(kFullMask, x, stride);
+            const bool desc = (lane & size) == 0, lower = (lane & stride) == 0;
+            x = (lower == desc) ? fmaxf(x, o) : fminf(x, o);
+        }
+    }
+    return x;
+}
+
+// The consumers' common first threshold, from the first chunk: every lane's maximum over its
+// elements there is one element of the row, so the k-th largest of the 512 lane maxima (taken
+// as the k-th largest of the warps' k largest) is at most the row's k-th largest value and no
+// element of the row's top k falls below it.  Every consumer warp calls this once (two barriers
+// over the 512 consumer threads); a warp whose chunk did not arrive (got false) adds nothing.
+__device__ __forceinline__ float stream_seed_threshold(StreamSmem *sm, float lane_max, int32_t warp, int32_t lane,
+                                                       int32_t k) {
+    const float sorted = warp_sort_desc(lane_max, lane);
+    if (lane < k) sm->seed[warp][lane] = sorted;
+    named_barrier_sync(1, kStreamConsumers);
+    const int32_t tid = warp * 32 + lane;
+    if (tid < kStreamWarps * k) {
+        const float v = sm->seed[tid / k][tid % k];
+        int32_t gt = 0, ge = 0;
+        for (int32_t w = 0; w < kStreamWarps; ++w)
+            for (int32_t e = 0; e < k; ++e) {
+                const float u = sm->seed[w][e];
+                gt += u > v ? 1 : 0;
+                ge += u >= v ? 1 : 0;
+            }
+        if (gt < k && ge >= k) sm->t0 = v;  // every writer holds the same value
+    }
+    named_barrier_sync(1, kStreamConsumers);
+    return sm->t0;
+}
 
 // Keeps the k best of the warp's n <= 64 buffered entries (value descending, column ascending),
 // in rank order at the front of the buffer; returns how many remain (min(n, k)) and sets thr to
@@ -428,7 +470,7 @@ __device__ __forceinline__ int32_t warp_keep_best(float *bv, int32_t *bi, int32_
 }
 
 template <typename T, bool kBestOnly>
-__global__ void __launch_bounds__(kStreamThreads, 1)
+__global__ void __launch_bounds__(kStreamThreads, 2)
     row_topk_stream_kernel(const T *__restrict__ logits, int32_t V, int64_t ld, int32_t k, int32_t *__restrict__ ids,
                            float *__restrict__ vals, float *__restrict__ lse_out, int32_t *status) {
     constexpr int EPV = 16 / sizeof(T);
@@ -449,6 +491,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             mbar_init(&sm->empty[st], kStreamWarps);
         }
         sm->abort = 0;
+        sm->t0 = -INFINITY;
         fence_barrier_init();
     }
     __syncthreads();
@@ -495,11 +538,24 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 sm->abort = 1;
                 latch(status, kDevTimeout);
             }
-            if (sm->abort) break;
             const uint32_t bytes = min(kChunkBytes, row_bytes - static_cast<uint32_t>(c) * kChunkBytes);
             const int32_t nv = static_cast<int32_t>(bytes / 16u);
             const int32_t col0 = c * static_cast<int32_t>(kChunkBytes / sizeof(T));
             const uint8_t *stage = ring + st * kChunkBytes;
+            if (!kBestOnly && c == 0) {
+                // before any element is kept: a threshold from the lane maxima of this chunk, so
+                // that few elements enter the buffers and few compactions follow
+                float lm = -INFINITY;  // fmaxf drops NaN: never NaN
+                if (got)
+                    for (int32_t v = warp * 32 + lane; v < nv; v += kStreamConsumers) {
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(stage + v * 16);
+                        const T *e = reinterpret_cast<const T *>(&raw);
+#pragma unroll
+                        for (int j = 0; j < EPV; ++j) lm = fmaxf(lm, to_f32(e[j]));
+                    }
+                thr = stream_seed_threshold(sm, lm, warp, lane, k);
+            }
+            if (sm->abort) break;
             for (int32_t v0 = warp * 32; v0 < nv; v0 += kStreamConsumers) {  // warp-uniform trips
                 const int32_t v = v0 + lane;
                 const bool have = v < nv;
