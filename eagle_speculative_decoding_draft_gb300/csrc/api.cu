@@ -1246,17 +1246,18 @@ eagle_status eagle_verify_sample(int32_t batch, int32_t num_nodes, int32_t vocab
 }
 
 size_t eagle_linear_workspace_bytes(int32_t out_features, int32_t rows) {
-    if (out_features < 1 || rows < 1 || rows > kLinearMaxRows) return 0;
+    if (out_features < 1 || rows < 1 || rows > kLinearMaxLaunchRows) return 0;
     const int32_t sms = current_num_sms(nullptr);
     if (sms < 1) return 0;
-    return align_up(linear_counters_bytes(out_features)) + linear_partials_bytes(sms, linear_n_tile(rows));
+    return align_up(linear_counters_bytes(out_features, rows)) +
+           linear_partials_bytes(sms, linear_n_tile(std::min(rows, kLinearMaxRows)));
 }
 
 eagle_status eagle_linear_bf16(const void *d_w, int64_t ldw, const void *d_x, int64_t ldx, const void *d_bias,
                                int32_t out_features, int32_t in_features, int32_t rows, void *d_y, int64_t ldy,
                                int32_t out_bf16, void *d_ws, size_t ws_bytes, eagle_stream_t stream) {
     NvtxRange nvtx_range("eagle_linear_bf16");
-    if (out_features < 1 || in_features < 1 || rows < 1 || rows > kLinearMaxRows) return EAGLE_ERR_INVALID_ARG;
+    if (out_features < 1 || in_features < 1 || rows < 1 || rows > kLinearMaxLaunchRows) return EAGLE_ERR_INVALID_ARG;
     if (!d_w || !d_x || !d_y || !d_ws) return EAGLE_ERR_INVALID_ARG;
     if (ldw < in_features || ldx < in_features || ldy < out_features) return EAGLE_ERR_INVALID_ARG;
     if (ldw % 8 != 0 || ldx % 8 != 0 || !aligned16(d_w) || !aligned16(d_x)) return EAGLE_ERR_INVALID_ARG;
@@ -1267,7 +1268,7 @@ eagle_status eagle_linear_bf16(const void *d_w, int64_t ldw, const void *d_x, in
     if (prepare_device() != cudaSuccess) return EAGLE_ERR_CUDA;
     int32_t *counters = reinterpret_cast<int32_t *>(d_ws);
     float *partials = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(d_ws) +
-                                                align_up(linear_counters_bytes(out_features)));
+                                                align_up(linear_counters_bytes(out_features, rows)));
     LinearPlan p;
     if (!plan_linear_bf16(&p, d_w, ldw, out_features, in_features, d_x, ldx, rows, d_bias, d_y, ldy, out_bf16,
                           partials, counters, nullptr, sms))

@@ -845,7 +845,7 @@ DecoderLayout decoder_layout(const eagle_decoder_layer_weights *w, int32_t batch
     };
     const int32_t chunk = static_cast<int32_t>(std::min<int64_t>(rows, kLinearMaxRows));
     const int32_t widest = static_cast<int32_t>(std::max<int64_t>(std::max(nqkv, h), 2 * I));
-    L.counters = take(linear_counters_bytes(widest));
+    L.counters = take(linear_counters_bytes(widest, static_cast<int32_t>(rows)));
     L.partials = take(linear_partials_bytes(sms, linear_n_tile(chunk)));
     L.qkv = take(static_cast<size_t>(rows) * nqkv * 2);
     L.o = take(static_cast<size_t>(rows) * nq * 2);
@@ -869,21 +869,14 @@ int32_t sms_now() {
     return n;
 }
 
-// Y = X W^T over `rows` rows in launches of at most kLinearMaxRows rows.
+// Y = X W^T over all `rows` rows in one launch: every weight byte is read from HBM once for all
+// row chunks (a weight tile's chunks are consecutive units of the split).
 cudaError_t gemm_rows(const void *W, int32_t M, int32_t K, const void *X, int32_t rows, void *Y, int32_t out_bf16,
                       float *partials, int32_t *counters, int32_t sms, cudaStream_t st) {
-    const int32_t ob = out_bf16 ? 2 : 4;
-    for (int32_t r0 = 0; r0 < rows; r0 += kLinearMaxRows) {
-        const int32_t n = std::min(kLinearMaxRows, rows - r0);
-        LinearPlan p;
-        const uint8_t *xb = reinterpret_cast<const uint8_t *>(X) + static_cast<int64_t>(r0) * K * 2;
-        uint8_t *yb = reinterpret_cast<uint8_t *>(Y) + static_cast<int64_t>(r0) * M * ob;
-        if (!plan_linear_bf16(&p, W, K, M, K, xb, K, n, nullptr, yb, M, out_bf16, partials, counters, nullptr, sms))
-            return cudaErrorInvalidValue;
-        const cudaError_t e = launch_linear_bf16(p, st);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    LinearPlan p;
+    if (!plan_linear_bf16(&p, W, K, M, K, X, K, rows, nullptr, Y, M, out_bf16, partials, counters, nullptr, sms))
+        return cudaErrorInvalidValue;
+    return launch_linear_bf16(p, st);
 }
 
 template <int D>

@@ -29,7 +29,12 @@
 //               shared memory.  An activation byte brought into an SM then feeds 256 weight rows
 //               instead of 128: per k-block an SM takes in 16 KB of weights and n/2 x 128 B of
 //               activations (32 KB at 256 rows, against 48 KB).  The stream-K split is over pairs
-//               (k-blocks of pair tiles), and each CTA sums and writes its own tile as before.
+//               (k-blocks of pair tiles), and each CTA sums and writes its own tile as before;
+//   row chunks  more rows than one MMA's N (256) are taken in chunks of 256: a unit of the split
+//               is (weight tile or pair, row chunk), weight-major, so a worker runs the chunks of
+//               one weight tile back to back (its later passes find the tile in L2) and the
+//               whole product is one launch (the draft decoder layer's projections over every
+//               node of a batch of trees).
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
@@ -72,7 +77,8 @@ struct LinearArgs {
     int32_t owner_fix;  // split tiles summed in the launch by the CTA that finds its partner done
     int32_t pair;       // 1: CTA pairs (.cta_group::2), the stream-K split over pairs of tiles
     int32_t slots;      // partial-sum slots of the launch: two per CTA of the main kernel
-    int32_t num_wtiles; // units of the stream-K split: tiles, or pairs of tiles when pair
+    int32_t num_wtiles; // weight units: tiles, or pairs of tiles
+    int32_t num_chunks; // row chunks of n_tile rows; the split's units are (weight unit, chunk)
     int32_t y_tma;      // 16-row groups of Y and of partials go out by bulk stores (tmap_y valid)
     int32_t out_stage_bytes;  // shared-memory staging of those groups (after the ring)
     float *partials;
@@ -115,7 +121,8 @@ __device__ __forceinline__ void store_y(const LinearArgs &a, int32_t r, int32_t 
 // store of the rows into the partial slot `part` (fp32, [row][128]).  All 128 epilogue threads.
 __device__ __forceinline__ void group_store(const LinearArgs &a, const CUtensorMap *tmap_y, uint8_t *out_stage,
                                             int32_t &gi, int32_t et, int32_t m_local, const float (&v)[16],
-                                            bool to_y, float *part, int32_t tile, int32_t n0) {
+                                            bool to_y, float *part, int32_t tile, int32_t n0, int32_t row0,
+                                            int32_t rows_c) {
     uint8_t *buf = out_stage + static_cast<size_t>(gi & 1) * kGroupBytes;
     if (et == 0 && gi >= 2) bulk_wait_read<1>();  // the store of group gi - 2 has read buf
     named_barrier_sync(1, 128);
@@ -132,10 +139,10 @@ __device__ __forceinline__ void group_store(const LinearArgs &a, const CUtensorM
     named_barrier_sync(1, 128);
     if (et == 0) {
         if (to_y)
-            tma_store_2d(tmap_y, buf, tile * BM, n0);
+            tma_store_2d(tmap_y, buf, tile * BM, row0 + n0);
         else
             bulk_store(part + static_cast<size_t>(n0) * BM, buf,
-                       static_cast<uint32_t>(min(16, a.rows - n0)) * BM * 4u);
+                       static_cast<uint32_t>(min(16, rows_c - n0)) * BM * 4u);
         bulk_commit();
     }
     ++gi;
@@ -151,16 +158,17 @@ __device__ __forceinline__ bool staged_fixup(const LinearArgs &a, const CUtensor
                                              uint8_t *ring, uint32_t ring_bytes, uint8_t *out_stage, int32_t &gi,
                                              int32_t tile, int32_t gf, int32_t gl, int32_t self, bool gf_second,
                                              int32_t rank, uint32_t t_row, int32_t et, int32_t m_local, int32_t o,
-                                             bool o_ok, float bias_o, volatile int32_t *abort_flag) {
+                                             bool o_ok, float bias_o, int32_t row0, int32_t rows_c,
+                                             volatile int32_t *abort_flag) {
     const int32_t np = gl - gf;  // partials read from global memory
     const uint32_t row_bytes = BM * 4u;
     int32_t cr = static_cast<int32_t>(ring_bytes / (static_cast<uint32_t>(np) * row_bytes)) & ~15;
     cr = min(cr, a.n_tile);
-    const int32_t nch = (a.rows + cr - 1) / cr;
-    cr = (((a.rows + nch - 1) / nch) + 15) & ~15;
+    const int32_t nch = (rows_c + cr - 1) / cr;
+    cr = (((rows_c + nch - 1) / nch) + 15) & ~15;
     const float *staged = reinterpret_cast<const float *>(ring);
     for (int32_t c = 0; c < nch; ++c) {
-        const int32_t r0 = c * cr, rc = min(cr, a.rows - r0);
+        const int32_t r0 = c * cr, rc = min(cr, rows_c - r0);
         if (et == 0) {
             fence_proxy_async();  // earlier accesses of the ring before the new copies
             ctl->fix_chunks = c + 1;  // at most one staged sum per launch: phase c
@@ -215,11 +223,11 @@ __device__ __forceinline__ bool staged_fixup(const LinearArgs &a, const CUtensor
             if (a.y_tma) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) sum[j] += bias_o;
-                group_store(a, tmap_y, out_stage, gi, et, m_local, sum, true, nullptr, tile, n0);
+                group_store(a, tmap_y, out_stage, gi, et, m_local, sum, true, nullptr, tile, n0, row0, rows_c);
             } else if (o_ok) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    if (n0 + j < r0 + rc) store_y(a, n0 + j, o, sum[j] + bias_o);
+                    if (n0 + j < r0 + rc) store_y(a, row0 + n0 + j, o, sum[j] + bias_o);
             }
         }
         named_barrier_sync(1, 128);  // every thread is done with the chunk
@@ -252,7 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t G = gridDim.x >> kPair, g = blockIdx.x >> kPair;
     const int32_t rank = kPair ? static_cast<int32_t>(blockIdx.x & 1u) : 0;
     const int64_t nkb = a.num_kb;
-    const int64_t total = static_cast<int64_t>(a.num_wtiles) * nkb;
+    const int32_t nch = a.num_chunks;
+    const int64_t total = static_cast<int64_t>(a.num_wtiles) * nch * nkb;
     int64_t kb_begin = div_nonneg(total * g, G), kb_end = div_nonneg(total * (g + 1), G);
 
     pdl_launch_dependents();
@@ -312,22 +321,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     tma_load_2d(dst, &tmap_w, &ctl->full[s], kx, unit * BM, pol_w);
             };
-            auto load_x = [&](int s, int32_t kx) {
+            auto load_x = [&](int s, int32_t kx, int32_t chunk) {
                 uint8_t *dst = b_tiles + static_cast<size_t>(s) * b_bytes;
+                const int32_t y = chunk * a.n_tile;
                 if (kPair)
-                    tma_load_2d_pair(dst, &tmap_x, peer_addr(&ctl->full[s], 0), kx, rank * (a.n_tile >> 1), pol_x);
+                    tma_load_2d_pair(dst, &tmap_x, peer_addr(&ctl->full[s], 0), kx, y + rank * (a.n_tile >> 1), pol_x);
                 else
-                    tma_load_2d(dst, &tmap_x, &ctl->full[s], kx, 0, pol_x);
+                    tma_load_2d(dst, &tmap_x, &ctl->full[s], kx, y, pol_x);
             };
             // The weights do not depend on the previous kernel: fill the whole ring with weight
             // tiles first, then wait for the previous kernel and add the activation slices.
             const int64_t n_pre = min(static_cast<int64_t>(stages), kb_end - kb_begin);
+            // units are weight-major: unit u covers weight unit u / nch and row chunk u % nch
             for (int64_t i = 0; i < n_pre; ++i) {
                 const int64_t kb = kb_begin + i;
                 const int32_t unit = static_cast<int32_t>(div_nonneg(kb, nkb));
                 const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(unit) * nkb) * BK;
                 expect(static_cast<int>(i));
-                load_w(static_cast<int>(i), kx, unit);
+                load_w(static_cast<int>(i), kx, unit / nch);
                 issued |= 1u << i;
             }
             pdl_wait();
@@ -335,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t kb = kb_begin + i;
                 const int32_t unit = static_cast<int32_t>(div_nonneg(kb, nkb));
                 const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(unit) * nkb) * BK;
-                load_x(static_cast<int>(i), kx);
+                load_x(static_cast<int>(i), kx, unit - (unit / nch) * nch);
             }
             uint32_t stage = static_cast<uint32_t>(n_pre % stages);
             uint32_t phase = (n_pre == stages) ? 1u : 0u;
@@ -347,9 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     latch(a.status, kDevTimeout);
                     break;
                 }
+                const int32_t wu = unit / nch;
                 expect(static_cast<int>(stage));
-                load_w(static_cast<int>(stage), kx, unit);
-                load_x(static_cast<int>(stage), kx);
+                load_w(static_cast<int>(stage), kx, wu);
+                load_x(static_cast<int>(stage), kx, unit - wu * nch);
                 issued |= 1u << stage;
                 issued_parity = phase ? (issued_parity | (1u << stage))
                                       : (issued_parity & ~(1u << stage));
@@ -428,7 +440,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int32_t gi = 0;  // 16-row groups sent by bulk stores
         for (int64_t kb = kb_begin; kb < kb_end;) {
             const int32_t unit = static_cast<int32_t>(div_nonneg(kb, nkb));
-            const int32_t tile = kPair ? 2 * unit + rank : unit;  // this CTA's 128-row tile
+            const int32_t wu = unit / nch, chunk = unit - wu * nch;
+            const int32_t tile = kPair ? 2 * wu + rank : wu;       // this CTA's 128 weight rows
+            const int32_t ticket = kPair ? 2 * unit + rank : unit;  // its (weight tile, row chunk)
+            const int32_t row0 = chunk * a.n_tile, rows_c = min(a.n_tile, a.rows - row0);
             const int64_t t0 = static_cast<int64_t>(unit) * nkb;
             const int64_t k1 = min(kb_end, t0 + nkb);
             const bool full = (kb == t0) && (k1 == t0 + nkb);
@@ -455,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool fits = static_cast<uint32_t>(gl - gf) * 16u * BM * 4u <= ring_bytes;
                     if (threadIdx.x == 64)  // acquire: the other CTAs' partials, for the copies
                         ctl->is_last = (got && !*abort_flag && fits && k1 == kb_end &&
-                                        ld_acquire_gpu(&a.counters[tile]) == gl - gf) ? 1 : 0;
+                                        ld_acquire_gpu(&a.counters[ticket]) == gl - gf) ? 1 : 0;
                     named_barrier_sync(1, 128);
                     owner = ctl->is_last != 0;
                 }
@@ -469,13 +484,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        acc * static_cast<uint32_t>(a.n_tile);
                 staged_fixup(a, &tmap_y, ctl, base, ring_bytes, out_stage, gi, tile, gf, gl, g, gf_second, rank,
-                             t_row, threadIdx.x - 64, m_local, o, o_ok, bias_o, abort_flag);
+                             t_row, threadIdx.x - 64, m_local, o, o_ok, bias_o, row0, rows_c, abort_flag);
             } else if (got) {
                 tc_fence_after();
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        acc * static_cast<uint32_t>(a.n_tile);
                 float *part = part_slot(a, g, first ? 0 : 1, rank);
-                for (int32_t n0 = 0; n0 < a.rows; n0 += 16) {
+                for (int32_t n0 = 0; n0 < rows_c; n0 += 16) {
                     uint32_t r[16];
                     __syncwarp();
                     tmem_ld_16(t_row + static_cast<uint32_t>(n0), r);
@@ -484,16 +499,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float v[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) + (full ? bias_o : 0.0f);
-                        group_store(a, &tmap_y, out_stage, gi, threadIdx.x - 64, m_local, v, full, part, tile, n0);
+                        group_store(a, &tmap_y, out_stage, gi, threadIdx.x - 64, m_local, v, full, part, tile, n0,
+                                    row0, rows_c);
                         continue;
                     }
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int32_t n = n0 + j;
-                        if (n < a.rows) {
+                        if (n < rows_c) {
                             const float v = __uint_as_float(r[j]);
                             if (full) {
-                                if (o_ok) store_y(a, n, o, v + bias_o);
+                                if (o_ok) store_y(a, row0 + n, o, v + bias_o);
                             } else {
                                 part[static_cast<size_t>(n) * BM + m_local] = v;
                             }
@@ -510,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&ctl->acc_empty[acc]);
             }
             if (split && owner) {
-                if (threadIdx.x == 64) a.counters[tile] = 0;  // ready for the next launch
+                if (threadIdx.x == 64) a.counters[ticket] = 0;  // ready for the next launch
                 named_barrier_sync(1, 128);                  // ctl->is_last is reused
             } else if (split) {
                 named_barrier_sync(1, 128);  // this CTA's partials of the tile are written
@@ -523,9 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!*abort_flag) {
                         // release: the partials written before the barrier; acquire: the other
                         // CTAs' partials, for the reads after the next barrier
-                        const int32_t prev = atomic_add_acq_rel_gpu(&a.counters[tile], 1);
+                        const int32_t prev = atomic_add_acq_rel_gpu(&a.counters[ticket], 1);
                         last = (prev == gl - gf);
-                        if (last) a.counters[tile] = 0;  // ready for the next launch
+                        if (last) a.counters[ticket] = 0;  // ready for the next launch
                     }
                     ctl->is_last = last;
                 }
@@ -546,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // 4 rows x 6 CTAs a thread and batch: up to 16 rows all in one batch, so a
                     // tile shared by up to 6 CTAs costs one round trip of loads
                     constexpr int kRowsPerBatch = 4, kCtasPerBatch = 6;  // per thread
-                    for (int32_t n0 = rsub; n0 < a.rows; n0 += 4 * kRowsPerBatch) {
+                    for (int32_t n0 = rsub; n0 < rows_c; n0 += 4 * kRowsPerBatch) {
                         float4 sum[kRowsPerBatch];
                         for (int32_t g0 = gf; g0 <= gl; g0 += kCtasPerBatch) {
                             float4 x[kCtasPerBatch][kRowsPerBatch];
@@ -558,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                 for (int j = 0; j < kRowsPerBatch; ++j) {
                                     const int32_t n = n0 + 4 * j;
-                                    x[c][j] = (gg <= gl && n < a.rows)
+                                    x[c][j] = (gg <= gl && n < rows_c)
                                                   ? __ldcg(reinterpret_cast<const float4 *>(
                                                         src + static_cast<size_t>(n) * BM))
                                                   : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -582,11 +598,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < kRowsPerBatch; ++j) {
                             const int32_t n = n0 + 4 * j;
-                            if (n >= a.rows) continue;
+                            if (n >= rows_c) continue;
                             const float v[4] = {sum[j].x, sum[j].y, sum[j].z, sum[j].w};
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
-                                if (tile * BM + m4 + q < a.M) store_y(a, n, tile * BM + m4 + q, v[q] + b4[q]);
+                                if (tile * BM + m4 + q < a.M) store_y(a, row0 + n, tile * BM + m4 + q, v[q] + b4[q]);
                         }
                     }
                 }
@@ -651,8 +667,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-// Deferred split-K sum for many rows: block (tile, y) adds, for rows y*kReduceRows .. +15 of a
-// tile that more than one CTA worked on, the partials of its CTAs in ascending CTA order (the
+// Deferred split-K sum for many rows: block (t, y) adds, for rows y*kReduceRows .. +15 of the
+// t-th (weight tile, row chunk) when more than one CTA worked on it, the partials of its CTAs in ascending CTA order (the
 // same order and the same sums as the in-kernel fix-up) and writes Y (+ bias).  Thread e sums
 // outputs 4(e % 32) .. +3 of rows e / 32 and e / 32 + 8; all its loads are issued together.
 // ---------------------------------------------------------------------------------------------
@@ -661,10 +677,13 @@ constexpr int kReduceRows = 16;
 __global__ void __launch_bounds__(256) linear_reduce_kernel(const LinearArgs a, int32_t G) {
     pdl_launch_dependents();  // dependents still wait for this grid to finish
     pdl_wait();
-    const int32_t tile = blockIdx.x;
-    const int32_t unit = tile >> a.pair, rank = tile & a.pair;  // G counts workers (CTAs or pairs)
+    const int32_t unit = static_cast<int32_t>(blockIdx.x) >> a.pair;  // G counts workers (CTAs or pairs)
+    const int32_t rank = static_cast<int32_t>(blockIdx.x) & a.pair;
+    const int32_t wu = unit / a.num_chunks, chunk = unit - wu * a.num_chunks;
+    const int32_t tile = a.pair ? 2 * wu + rank : wu;
+    const int32_t row0 = chunk * a.n_tile, rows_c = min(a.n_tile, a.rows - row0);
     const int64_t nkb = a.num_kb;
-    const int64_t total = static_cast<int64_t>(a.num_wtiles) * nkb;
+    const int64_t total = static_cast<int64_t>(a.num_wtiles) * a.num_chunks * nkb;
     const int64_t t0 = static_cast<int64_t>(unit) * nkb;
     const int32_t gf = cta_of(t0, total, G), gl = cta_of(t0 + nkb - 1, total, G);
     if (gf == gl) return;  // one CTA computed the whole tile and wrote it
@@ -682,7 +701,7 @@ __global__ void __launch_bounds__(256) linear_reduce_kernel(const LinearArgs a, 
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int32_t n = blockIdx.y * kReduceRows + rsub + 8 * j;
-                x[c][j] = (gg <= gl && n < a.rows)
+                x[c][j] = (gg <= gl && n < rows_c)
                               ? __ldcg(reinterpret_cast<const float4 *>(src + static_cast<size_t>(n) * BM))
                               : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
@@ -705,14 +724,14 @@ __global__ void __launch_bounds__(256) linear_reduce_kernel(const LinearArgs a, 
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         const int32_t n = blockIdx.y * kReduceRows + rsub + 8 * j;
-        if (n >= a.rows) continue;
+        if (n >= rows_c) continue;
         const float v[4] = {sum[j].x, sum[j].y, sum[j].z, sum[j].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int32_t o = tile * BM + m4 + q;
             if (o >= a.M) continue;
             const float b = a.bias != nullptr ? __bfloat162float(a.bias[o]) : 0.0f;
-            store_y(a, n, o, v[q] + b);
+            store_y(a, row0 + n, o, v[q] + b);
         }
     }
 }
@@ -823,23 +842,27 @@ size_t linear_partials_bytes(int32_t grid, int32_t n_tile) {
     return static_cast<size_t>(grid) * 2 * n_tile * BM * sizeof(float);
 }
 
-size_t linear_counters_bytes(int32_t M) {
-    return static_cast<size_t>((M + BM - 1) / BM) * sizeof(int32_t);
+size_t linear_counters_bytes(int32_t M, int32_t rows) {
+    const int64_t chunks = (static_cast<int64_t>(rows < 1 ? 1 : rows) + kLinearMaxRows - 1) / kLinearMaxRows;
+    return static_cast<size_t>((M + BM - 1) / BM) * static_cast<size_t>(chunks) * sizeof(int32_t);
 }
 
 bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int32_t K, const void *x,
                       int64_t ldx, int32_t rows, const void *bias, void *out, int64_t ldo,
                       int32_t out_bf16, float *partials, int32_t *counters, int32_t *status,
                       int32_t num_sms) {
-    if (M < 1 || K < 1 || rows < 1 || rows > kLinearMaxRows || num_sms < 1) return false;
+    if (M < 1 || K < 1 || rows < 1 || rows > kLinearMaxLaunchRows || num_sms < 1) return false;
     if (ldw < K || ldx < K || ldo < M) return false;
     p->M = M;
     p->K = K;
     p->rows = rows;
-    p->n_tile = linear_n_tile(rows);
+    // more rows than one MMA's N: chunks of kLinearMaxRows rows, each a unit of the split with
+    // every weight tile
+    p->num_chunks = (rows + kLinearMaxRows - 1) / kLinearMaxRows;
+    p->n_tile = linear_n_tile(rows < kLinearMaxRows ? rows : kLinearMaxRows);
     p->num_kb = (K + BK - 1) / BK;
     p->num_tiles = (M + BM - 1) / BM;
-    const int64_t total = static_cast<int64_t>(p->num_kb) * p->num_tiles;
+    const int64_t total = static_cast<int64_t>(p->num_kb) * p->num_tiles * p->num_chunks;
     p->grid = static_cast<int32_t>(total < num_sms ? total : num_sms);
     // CTA pairs (.cta_group::2) for stream-K above 16 rows when the tiles pair up: the split runs
     // over pairs of adjacent tiles and the grid is twice the pairs
@@ -850,7 +873,7 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
         if (pairs > 0) {
             p->pair = 1;
             p->num_wtiles = p->num_tiles / 2;
-            const int64_t total_w = static_cast<int64_t>(p->num_kb) * p->num_wtiles;
+            const int64_t total_w = static_cast<int64_t>(p->num_kb) * p->num_wtiles * p->num_chunks;
             p->grid = 2 * static_cast<int32_t>(total_w < pairs ? total_w : pairs);
         }
     }
@@ -876,7 +899,8 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
     // whole tile's k-blocks (then a tile is shared by at most two CTAs, and the one that reaches
     // it at the end of its range finds the other's partial in and owns the sum), else by a
     // second launch.
-    const int64_t per_cta = static_cast<int64_t>(p->num_kb) * p->num_wtiles / (p->grid >> p->pair);  // fewest of any worker
+    const int64_t per_cta =  // fewest of any worker
+        static_cast<int64_t>(p->num_kb) * p->num_wtiles * p->num_chunks / (p->grid >> p->pair);
     p->owner_fix = (rows > kLinearMaxFixupRows && per_cta >= p->num_kb) ? 1 : 0;
     p->defer = (rows > kLinearMaxFixupRows && !p->owner_fix) ? 1 : 0;
     p->partials = partials;
@@ -961,6 +985,7 @@ cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
     a.owner_fix = p.owner_fix;
     a.pair = p.pair;
     a.num_wtiles = p.num_wtiles;
+    a.num_chunks = p.num_chunks;
     a.slots = 2 * p.grid;
     a.y_tma = p.y_tma;
     a.out_stage_bytes = p.out_stage_bytes;
@@ -975,7 +1000,7 @@ cudaError_t launch_linear_bf16(const LinearPlan &p, cudaStream_t st) {
         e = launch_pdl(linear_bf16_tc_kernel<0>, dim3(p.grid), dim3(kThreads), p.smem_bytes, st, p.tmap_w,
                        p.tmap_x, p.tmap_y, a);
     if (e != cudaSuccess || !p.defer) return e;
-    return launch_pdl(linear_reduce_kernel, dim3(p.num_tiles, (p.rows + kReduceRows - 1) / kReduceRows),
+    return launch_pdl(linear_reduce_kernel, dim3(p.num_tiles * p.num_chunks, (p.n_tile + kReduceRows - 1) / kReduceRows),
                       dim3(256), 0, st, a, p.grid >> p.pair);
 }
 

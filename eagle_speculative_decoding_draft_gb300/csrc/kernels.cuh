@@ -71,8 +71,9 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
 // ---------------------------------------------------------------------------------------------
 constexpr int kLinearTileM = 128;
 constexpr int kLinearTileK = 64;
-constexpr int kLinearMaxRows = 256;  // MMA N limit of one launch
-constexpr int kLinearMaxFixupRows = 16;  // above this, split tiles are summed by a second launch
+constexpr int kLinearMaxRows = 256;  // MMA N limit: rows of one row chunk
+constexpr int kLinearMaxLaunchRows = 32768;  // rows of one launch (row chunks of kLinearMaxRows)
+constexpr int kLinearMaxFixupRows = 16;  // above this, split tiles are summed by their owner or a second launch
 
 struct LinearPlan {
     CUtensorMap tmap_w;  // W [M][K] bf16, box {64, 128}, 128-byte swizzle
@@ -87,17 +88,18 @@ struct LinearPlan {
     int32_t defer;     // rows > kLinearMaxFixupRows: a second launch sums the split tiles
     int32_t owner_fix; // > 16 rows, at most two CTAs per tile: summed in the launch by its owner
     int32_t pair;      // CTA pairs on .cta_group::2 (clusters of 2; grid = 2 x pairs)
-    int32_t num_wtiles;  // units of the stream-K split: tiles, or pairs of tiles
+    int32_t num_wtiles;  // weight units of the stream-K split: tiles, or pairs of tiles
+    int32_t num_chunks;  // row chunks of n_tile (at most kLinearMaxRows) rows
     int32_t y_tma;     // outputs and partials leave by bulk stores (16-row groups)
     int32_t out_stage_bytes;  // their shared-memory staging
     float *partials;   // [grid][2][n_tile][128]
-    int32_t *counters; // [num_tiles], zero before and after
+    int32_t *counters; // [num_tiles][num_chunks], zero before and after
     int32_t *status;
 };
 
 // Bytes of split-K scratch (partials) and tile counters a launch with these sizes needs.
 size_t linear_partials_bytes(int32_t grid, int32_t n_tile);
-size_t linear_counters_bytes(int32_t M);
+size_t linear_counters_bytes(int32_t M, int32_t rows = 1);
 int32_t linear_n_tile(int32_t rows);
 // CTA pairs of the .cta_group::2 mode that fit on the device at once (0: the mode is off).
 int32_t linear_pair_workers(int32_t num_sms);

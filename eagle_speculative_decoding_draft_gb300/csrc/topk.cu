@@ -398,41 +398,31 @@ struct StreamSmem {
     float t0;                      // the k-th largest of them all: the warps' first threshold
 };
 
-// Sorts one value a lane across the warp, largest first (bitonic network over the lanes).
-__device__ __forceinline__ float warp_sort_desc(float x, int32_t lane) {
-#pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const float o = __shfl_xor_sync(kFullMask, x, stride);
-            const bool desc = (lane & size) == 0, lower = (lane & stride) == 0;
-            x = (lower == desc) ? fmaxf(x, o) : fminf(x, o);
-        }
-    }
-    return x;
-}
-
 // The consumers' common first threshold, from the first chunk: every lane's maximum over its
-// elements there is one element of the row, so the k-th largest of the 512 lane maxima (taken
-// as the k-th largest of the warps' k largest) is at most the row's k-th largest value and no
-// element of the row's top k falls below it.  Every consumer warp calls this once (two barriers
-// over the 512 consumer threads); a warp whose chunk did not arrive (got false) adds nothing.
+// elements there is one element of the row, so the k-th largest of the 512 lane maxima is at
+// most the row's k-th largest value and no element of the row's top k falls below it.  Each
+// warp sorts its 32 maxima and keeps its k largest; one warp then takes the k-th largest of
+// those 16 sorted lists by k rounds that each remove the largest head.  Every consumer warp
+// calls this once (two barriers over the 512 consumer threads).
 __device__ __forceinline__ float stream_seed_threshold(StreamSmem *sm, float lane_max, int32_t warp, int32_t lane,
                                                        int32_t k) {
-    const float sorted = warp_sort_desc(lane_max, lane);
+    const float sorted = warp_sort_values(lane_max, lane);
     if (lane < k) sm->seed[warp][lane] = sorted;
     named_barrier_sync(1, kStreamConsumers);
-    const int32_t tid = warp * 32 + lane;
-    if (tid < kStreamWarps * k) {
-        const float v = sm->seed[tid / k][tid % k];
-        int32_t gt = 0, ge = 0;
-        for (int32_t w = 0; w < kStreamWarps; ++w)
-            for (int32_t e = 0; e < k; ++e) {
-                const float u = sm->seed[w][e];
-                gt += u > v ? 1 : 0;
-                ge += u >= v ? 1 : 0;
-            }
-        if (gt < k && ge >= k) sm->t0 = v;  // every writer holds the same value
+    if (warp == 0) {
+        int32_t h = 0;  // this lane's list head (lanes below 16: warp `lane`'s list)
+        float t = -INFINITY;
+        for (int32_t r = 0; r < k; ++r) {
+            const bool live = lane < kStreamWarps && h < k;
+            const float v = live ? sm->seed[lane][h] : -INFINITY;
+            float best = v;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) best = fmaxf(best, __shfl_xor_sync(kFullMask, best, off));
+            const uint32_t hold = __ballot_sync(kFullMask, live && v == best);
+            if (hold != 0u && lane == __ffs(hold) - 1) ++h;  // the lowest lane holding it moves on
+            t = best;
+        }
+        if (lane == 0) sm->t0 = t;
     }
     named_barrier_sync(1, kStreamConsumers);
     return sm->t0;
@@ -518,7 +508,6 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         __syncwarp();
     } else {
         // ---------------- 16 consumer warps ----------------
-        const int32_t tid = static_cast<int32_t>(threadIdx.x) - 32;
         float *wbv = sm->b_v[warp];
         int32_t *wbi = sm->b_i[warp];
         int32_t wn = 0;            // entries in this warp's buffer (the same in every lane)
@@ -556,65 +545,82 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                 thr = stream_seed_threshold(sm, lm, warp, lane, k);
             }
             if (sm->abort) break;
-            for (int32_t v0 = warp * 32; v0 < nv; v0 += kStreamConsumers) {  // warp-uniform trips
-                const int32_t v = v0 + lane;
-                const bool have = v < nv;
-                float x[EPV];
+            // two vectors a lane and round (v and v + 512 of the chunk: a thread still visits its
+            // columns in ascending order); trips are warp-uniform
+            for (int32_t va = warp * 32; va < nv; va += 2 * kStreamConsumers) {
+                float x[2 * EPV];
+                bool have[2];
                 float cmax = -INFINITY;
-                if (have) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(stage + v * 16);
-                    const T *e = reinterpret_cast<const T *>(&raw);
 #pragma unroll
-                    for (int j = 0; j < EPV; ++j) {
-                        x[j] = to_f32(e[j]);
-                        cmax = fmaxf(cmax, x[j]);
+                for (int u = 0; u < 2; ++u) {
+                    const int32_t v = va + u * kStreamConsumers + lane;
+                    have[u] = v < nv;
+                    if (have[u]) {
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(stage + v * 16);
+                        const T *e = reinterpret_cast<const T *>(&raw);
+#pragma unroll
+                        for (int j = 0; j < EPV; ++j) {
+                            x[u * EPV + j] = to_f32(e[j]);
+                            cmax = fmaxf(cmax, x[u * EPV + j]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < EPV; ++j) x[u * EPV + j] = -INFINITY;
                     }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < EPV; ++j) x[j] = -INFINITY;
                 }
                 if (kBestOnly) {
-                    // a thread visits ascending columns: an equal value later ranks after its best
+                    // an equal value later ranks after the thread's best
                     if (cmax > bv) {
 #pragma unroll
-                        for (int j = 0; j < EPV; ++j)
-                            if (x[j] > bv) {
-                                bv = x[j];
-                                bi = col0 + v * EPV + j;
-                            }
+                        for (int u = 0; u < 2; ++u)
+#pragma unroll
+                            for (int j = 0; j < EPV; ++j)
+                                if (x[u * EPV + j] > bv) {
+                                    bv = x[u * EPV + j];
+                                    bi = col0 + (va + u * kStreamConsumers + lane) * EPV + j;
+                                }
                     }
                     continue;
                 }
-                if (want_lse && have) {
+                if (want_lse) {
                     if (cmax > cof + 16.0f) {  // keep the terms below 2^23: rescale to the new max
                         ssum = (cof == -INFINITY) ? 0.0f : ssum * ex2_approx((cof - cmax) * kLog2e);
                         cof = cmax;
                     }
-                    const float cl = cof * kLog2e;
+                    if (cof != -INFINITY) {  // padding (-inf) adds exp(-inf) = 0
+                        const float cl = cof * kLog2e;
+                        float s0 = 0.0f, s1 = 0.0f;  // two chains of adds
 #pragma unroll
-                    for (int j = 0; j < EPV; ++j) ssum += ex2_approx(fmaf(x[j], kLog2e, -cl));
-                }
-                if (__any_sync(kFullMask, have && cmax >= thr)) {
-#pragma unroll
-                    for (int j = 0; j < EPV; ++j) {
-                        bool in = have && x[j] >= thr;
-                        uint32_t ball = __ballot_sync(kFullMask, in);
-                        if (ball == 0u) continue;
-                        if (wn + __popc(ball) > kWarpCap) {
-                            // full: keep the warp's k best, raise the threshold, vote again
-                            wn = warp_keep_best(wbv, wbi, wn, k, lane, thr);
-                            in = have && x[j] >= thr;
-                            ball = __ballot_sync(kFullMask, in);
-                            if (ball == 0u) continue;
+                        for (int j = 0; j < 2 * EPV; j += 2) {
+                            s0 += ex2_approx(fmaf(x[j], kLog2e, -cl));
+                            s1 += ex2_approx(fmaf(x[j + 1], kLog2e, -cl));
                         }
-                        if (in) {
-                            const int32_t pos = wn + __popc(ball & ((1u << lane) - 1u));
-                            wbv[pos] = x[j];
-                            wbi[pos] = col0 + v * EPV + j;
-                        }
-                        wn += __popc(ball);
-                        __syncwarp();
+                        ssum += s0 + s1;
                     }
+                }
+                if (__any_sync(kFullMask, cmax >= thr)) {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int j = 0; j < EPV; ++j) {
+                            bool in = have[u] && x[u * EPV + j] >= thr;
+                            uint32_t ball = __ballot_sync(kFullMask, in);
+                            if (ball == 0u) continue;
+                            if (wn + __popc(ball) > kWarpCap) {
+                                // full: keep the warp's k best, raise the threshold, vote again
+                                wn = warp_keep_best(wbv, wbi, wn, k, lane, thr);
+                                in = have[u] && x[u * EPV + j] >= thr;
+                                ball = __ballot_sync(kFullMask, in);
+                                if (ball == 0u) continue;
+                            }
+                            if (in) {
+                                const int32_t pos = wn + __popc(ball & ((1u << lane) - 1u));
+                                wbv[pos] = x[u * EPV + j];
+                                wbi[pos] = col0 + (va + u * kStreamConsumers + lane) * EPV + j;
+                            }
+                            wn += __popc(ball);
+                            __syncwarp();
+                        }
                 }
             }
             __syncwarp();
@@ -665,26 +671,34 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         }
         return;
     }
+    if (threadIdx.x >= 32) return;
+    // one warp: the row's logsumexp (the warps' (max, sum) pairs merged in warp order), then the
+    // k best of the warps' sorted lists by k rounds that each take the best head (value
+    // descending, column ascending; a column is in one list only)
     float M = -INFINITY, S = 0.0f;
-    for (int w = 0; w < kStreamWarps; ++w) lse_merge(M, S, sm->w_m[w], sm->w_s[w]);
+    if (want_lse) {
+        if (lane == 0)
+            for (int w = 0; w < kStreamWarps; ++w) lse_merge(M, S, sm->w_m[w], sm->w_s[w]);
+        M = __shfl_sync(kFullMask, M, 0);
+        S = __shfl_sync(kFullMask, S, 0);
+    }
     const float lse = want_lse ? M + logf(S) : 0.0f;  // without it the values are the logits
-    // the warps' k best (at most 16 x 16 entries): each ranked by counting the others
-    if (tid < kStreamWarps * k) {
-        const int32_t w = tid / k, e = tid - w * k;
-        if (e < sm->w_i[w]) {
-            const float v = sm->b_v[w][e];
-            const int32_t c = sm->b_i[w][e];
-            int32_t rank = 0;
-            for (int32_t w2 = 0; w2 < kStreamWarps; ++w2)
-                for (int32_t e2 = 0; e2 < sm->w_i[w2]; ++e2)
-                    rank += ranks_before(sm->b_v[w2][e2], sm->b_i[w2][e2], v, c) ? 1 : 0;
-            if (rank < k) {
-                ids[static_cast<int64_t>(row) * k + rank] = c;
-                if (vals) vals[static_cast<int64_t>(row) * k + rank] = v - lse;
-            }
+    const int32_t n_l = lane < kStreamWarps ? sm->w_i[lane] : 0;
+    int32_t h = 0;
+    for (int32_t r = 0; r < k; ++r) {
+        const bool live = h < n_l;
+        float v = live ? sm->b_v[lane][h] : -INFINITY;
+        int32_t c = live ? sm->b_i[lane][h] : INT_MAX;
+        const int32_t mine = c;
+        warp_best(v, c);
+        if (c == INT_MAX) break;  // every list is empty
+        if (live && mine == c) ++h;
+        if (lane == 0) {
+            ids[static_cast<int64_t>(row) * k + r] = c;
+            if (vals) vals[static_cast<int64_t>(row) * k + r] = v - lse;
         }
     }
-    if (tid == 0 && want_lse) lse_out[row] = lse;
+    if (lane == 0 && want_lse) lse_out[row] = lse;
 }
 
 constexpr size_t kStreamSmem = 128 + kStreamStages * kChunkBytes + sizeof(StreamSmem);

@@ -398,7 +398,8 @@ def verify_sample(tokens, parents, target_logits, draft_logits, depth, temperatu
 
 
 def linear_bf16(w, x, bias=None, out_bf16=False, stream=None):
-    """Y = X W^T (+ bias) for bf16 W [M][K], X [rows][K] (rows <= 256) on the tensor cores."""
+    """Y = X W^T (+ bias) for bf16 W [M][K], X [rows][K] (rows <= 32768, in chunks of 256) on the
+    tensor cores."""
     lib = _lib.load()
     M, K = w.shape
     rows = x.shape[0]

@@ -431,7 +431,9 @@ EAGLE_API eagle_status eagle_verify_sample(int32_t batch, int32_t num_nodes, int
  * strides in elements ldw, ldx; multiples of 8), fp32 accumulation on the tensor cores.  Output
  * Y [rows][ldy]: fp32 when out_bf16 == 0, else bf16 rounded to nearest even.  Needs
  * eagle_linear_workspace_bytes(...) bytes of zero-initialised scratch (d_ws, 256-byte aligned),
- * which it leaves zeroed.  rows in [1, 256] per call.
+ * which it leaves zeroed.  rows in [1, 32768] per call: above 256 the rows are taken in chunks of
+ * 256, each a unit of the same launch with every weight tile, so the weights are streamed from
+ * memory once for all chunks.
  */
 EAGLE_API size_t eagle_linear_workspace_bytes(int32_t out_features, int32_t rows);
 EAGLE_API eagle_status eagle_linear_bf16(const void *d_w, int64_t ldw, const void *d_x,

@@ -94,8 +94,8 @@ def test_stateless_entries_reject_bad_sizes_on_the_host(lib):
     assert lib.eagle_expand(0, 0, 2, 3, *([None] * 10), None) == 0    # empty batch
     assert lib.eagle_build_tree(1, 2, 3, 11, *([P(256)] * 11), None) == 1  # m > n_cand
     assert lib.eagle_verify_walk(1, 0, 3, *([P(256)] * 6), None) == 1
-    assert lib.eagle_linear_bf16(P(256), 64, P(256), 64, None, 128, 64, 300, P(256), 128, 0,
-                                 P(256), 1 << 20, None) == 1  # rows > 256
+    assert lib.eagle_linear_bf16(P(256), 64, P(256), 64, None, 128, 64, 32769, P(256), 128, 0,
+                                 P(256), 1 << 20, None) == 1  # rows > 32768
     assert lib.eagle_linear_bf16(P(256), 60, P(256), 64, None, 128, 60, 16, P(256), 128, 0,
                                  P(256), 1 << 20, None) == 1  # ldw not a multiple of 8
 

@@ -178,42 +178,66 @@ def test_empty_batch_is_a_no_op(dev):
     assert out.shape == (0, 3, 64)
 
 
-def test_7b_draft_layer_on_sampled_nodes(dev):
-    """Vicuna-7B draft layer sizes (h 4096, 32 heads of 128, MLP 11008), a 1024-token cache and a
-    61-node tree of depth 6 per request; the oracle checks sampled nodes through their chains."""
-    B, n, P, h, H, Hk, D, I = 2, 61, 1024, 4096, 32, 32, 128, 11008
-    rng = np.random.default_rng(61)
-    w, d = layer(B=B, n=n, P=P, h=h, H=H, Hk=Hk, D=D, I=I, seed=7, fan_in=True)
-    trees = [random_tree(n, 6, rng) for _ in range(B)]
+def sampled_chains(dev, B, n, P, h, H, Hk, D, I, depth, seed, picks, exact_share):
+    """The layer over B requests of an n-node tree each; for `picks` (request, node) pairs the
+    oracle runs the chain root..node as a tree of its own and its last output is compared with
+    the GPU's output for that node."""
+    rng = np.random.default_rng(seed)
+    w, d = layer(B=B, n=n, P=P, h=h, H=H, Hk=Hk, D=D, I=I, seed=seed % 97, fan_in=True)
+    trees = [random_tree(n, depth, rng) for _ in range(B)]
     masks = np.stack([tree_mask(t[0]) for t in trees])
     pos = np.array([[P + dep for dep in t[1]] for t in trees], np.int32)
     out, kn, vn = gpu_layer(dev, w, d, masks, pos)
-    for b in range(B):
-        parents, depths = trees[b]
-        deepest = max(range(n), key=lambda i: depths[i])
-        for node in (deepest, int(rng.integers(1, n))):
-            chain = [node]
-            while parents[chain[-1]] >= 0:
-                chain.append(parents[chain[-1]])
-            chain = chain[::-1]
-            m = len(chain)
-            wc = dict(w)
-            wc["x"] = w["x"][b:b + 1, chain].contiguous()
-            wc["k_cache"], wc["v_cache"] = w["k_cache"][b:b + 1], w["v_cache"][b:b + 1]
-            cpar = [-1] + list(range(m - 1))
-            cpos = pos[b:b + 1, chain]
-            orc = oracle.decoder_layer(wc["x"], w["w_qkv"], w["w_o"], w["w_norm"], w["w_gu"], w["w_d"],
-                                       wc["k_cache"], wc["v_cache"], cpos, tree_mask(cpar)[None], H, Hk,
-                                       new_kv=True)
-            ref, h1, absterms = reference_layer(wc, dict(d, B=1, n=m), cpar, cpos)
-            # At these sizes (sums over 4096 and 11008 terms) the summation order moves the bf16
-            # rounding of a few percent of the MLP's gate and up values; the down projection
-            # gathers ~10^3 such one-ulp moves per output, about a third of an output ulp, so
-            # about a quarter of the outputs round the other way (72% equal measured).
-            check_out(out[b:b + 1, node:node + 1], orc["out"][:, -1:], ref[:, -1:], h1[:, -1:],
-                      absterms[:, -1:], exact_share=0.5)
-            sk, sv = kv_slack(w["x"][b, node], w, d)
-            check_kv(kn[b, node], vn[b, node], orc["k_new"][0, -1], orc["v_new"][0, -1], sk, sv)
+    for b, node in picks(trees, rng):
+        parents = trees[b][0]
+        chain = [node]
+        while parents[chain[-1]] >= 0:
+            chain.append(parents[chain[-1]])
+        chain = chain[::-1]
+        m = len(chain)
+        wc = dict(w)
+        wc["x"] = w["x"][b:b + 1, chain].contiguous()
+        wc["k_cache"], wc["v_cache"] = w["k_cache"][b:b + 1], w["v_cache"][b:b + 1]
+        cpar = [-1] + list(range(m - 1))
+        cpos = pos[b:b + 1, chain]
+        orc = oracle.decoder_layer(wc["x"], w["w_qkv"], w["w_o"], w["w_norm"], w["w_gu"], w["w_d"],
+                                   wc["k_cache"], wc["v_cache"], cpos, tree_mask(cpar)[None], H, Hk,
+                                   new_kv=True)
+        ref, h1, absterms = reference_layer(wc, dict(d, B=1, n=m), cpar, cpos)
+        check_out(out[b:b + 1, node:node + 1], orc["out"][:, -1:], ref[:, -1:], h1[:, -1:],
+                  absterms[:, -1:], exact_share=exact_share)
+        sk, sv = kv_slack(w["x"][b, node], w, d)
+        check_kv(kn[b, node], vn[b, node], orc["k_new"][0, -1], orc["v_new"][0, -1], sk, sv)
+
+
+def test_7b_draft_layer_on_sampled_nodes(dev):
+    """Vicuna-7B draft layer sizes (h 4096, 32 heads of 128, MLP 11008), a 1024-token cache and a
+    61-node tree of depth 6 per request; the oracle checks sampled nodes through their chains.
+    At these sizes (sums over 4096 and 11008 terms) the summation order moves the bf16 rounding of
+    a few percent of the MLP's gate and up values; the down projection gathers ~10^3 such one-ulp
+    moves per output, about a third of an output ulp, so about a quarter of the outputs round the
+    other way (72% equal measured)."""
+    def picks(trees, rng):
+        for b in range(len(trees)):
+            depths = trees[b][1]
+            yield b, max(range(len(depths)), key=lambda i: depths[i])
+            yield b, int(rng.integers(1, len(depths)))
+    sampled_chains(dev, B=2, n=61, P=1024, h=4096, H=32, Hk=32, D=128, I=11008, depth=6, seed=61,
+                   picks=picks, exact_share=0.5)
+
+
+def test_projections_over_several_row_chunks(dev):
+    """366 node rows (6 requests x 61 nodes): every projection runs as one launch over two row
+    chunks of 256 (the second ragged, 110 rows), grouped-query heads; nodes are sampled in both
+    chunks, including the last row."""
+    def picks(trees, rng):
+        yield 0, 1
+        yield 3, 60   # row 243, first chunk
+        yield 4, 20   # row 264, second chunk
+        yield 5, 60   # row 365, the last
+        yield 5, int(rng.integers(1, 61))
+    sampled_chains(dev, B=6, n=61, P=256, h=1024, H=16, Hk=4, D=64, I=2816, depth=6, seed=366,
+                   picks=picks, exact_share=0.5)
 
 
 def test_small_activations_where_the_norm_epsilon_counts(dev):

@@ -46,12 +46,16 @@ def bf16_tensor(rng, shape, std):
 # M = 256): (32000, 4096) at 17, 64 and 256 rows (the LM head: the owner's fix-up), (4096, 8192)
 # at 256 rows and (2000, 2048, 128) (the FC's shape class: the second launch), (12000, 2048, 24),
 # (130, 72, 255) (one pair of tiles split over two pairs with 255 rows, the largest ragged N) and
-# (20480, 520, 40) (160 tiles, ragged last k-block).
+# (20480, 520, 40) (160 tiles, ragged last k-block).  More than 256 rows run as row chunks of 256
+# in one launch: (1000, 520, 300) (CTA pairs, a 44-row last chunk), (777, 1000, 520) (odd tile
+# count: single CTAs, an 8-row last chunk), (4096, 2048, 600) and (2048, 1024, 1100) (3 and 5
+# chunks on CTA pairs).
 LINEAR_CASES = [(128, 64, 1), (200, 200, 17), (1000, 512, 256), (300, 64, 33), (128, 128, 16),
                 (4096, 8192, 10), (32000, 4096, 10), (777, 1000, 100), (130, 72, 255),
                 (4096, 8192, 256), (300, 64, 64), (513, 1000, 49), (70, 4104, 80), (2000, 2048, 128),
                 (20000, 512, 40), (20000, 520, 200), (12000, 2048, 24), (32000, 4096, 256),
-                (32000, 4096, 17), (32000, 4096, 64), (20480, 520, 40)]
+                (32000, 4096, 17), (32000, 4096, 64), (20480, 520, 40),
+                (1000, 520, 300), (777, 1000, 520), (4096, 2048, 600), (2048, 1024, 1100)]
 
 
 @pytest.mark.parametrize("M,K,rows", LINEAR_CASES)
