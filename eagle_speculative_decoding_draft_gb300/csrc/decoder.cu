@@ -642,6 +642,412 @@ __global__ void __launch_bounds__(kFewWarps * 32, 3) tree_attention_few_kernel(c
     }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Tree attention on the 5th-generation tensor cores (tcgen05, accumulators in tensor memory),
+// for head_dim 64 or 128 and more than 64 query rows per (request, kv head).  CTA (request b,
+// kv head hk, 128 query rows, key split), 6 warps:
+//   warp 0     copies the key and value rows of each 64-key tile (cached keys, then the tree's
+//              rotated keys and values from the qkv rows; zeros past the last key) in 16-byte
+//              pieces (cp.async) into a ring of 3 stages, laid out 128-byte-swizzled with the
+//              head dimension contiguous;
+//   warp 1     one thread issues the MMAs:  S_t = Q K_t^T (M = 128 query rows, N = 64 keys,
+//              K = D) into one of two TMEM score buffers, so the next tile's scores are formed
+//              while this tile's softmax runs, and O += P_hi V_t + P_lo V_t (M = 128, N = D,
+//              K = 64 keys; V is read as stored, the MN-major B operand) into a TMEM accumulator;
+//   warps 2-5  one query row per thread (its TMEM lane): read the row of S_t, scale and mask it
+//              (cached keys visible, tree keys by the node's mask row), keep a running max m and
+//              sum l (base-2 exponentials), and write P = 2^(s - m) as bf16 hi + lo (the split of
+//              the mma.sync kernels: ~2^-16 relative) into shared memory as the K-major A
+//              operand.  O is rescaled in TMEM (read, multiplied, written back) only when a
+//              tile's max exceeds m by more than 2^8: below that the terms stay in range, and O
+//              and l keep the same m, so the output is unchanged.
+// Output O / l in bf16, or with key splits the unnormalised O with m (natural log) and l for
+// attention_combine_kernel.  Every wait is bounded (an expired wait ends the CTA's work; the
+// copies and MMAs it started land before it exits).
+// ---------------------------------------------------------------------------------------------
+constexpr int kTcRows = 128;    // query rows per CTA: the MMA's M and the TMEM lanes
+constexpr int kTcKeys = 64;     // keys per tile (the same tiles as kAttnKeys)
+constexpr int kTcStages = 3;    // key/value tiles in flight
+constexpr int kTcThreads = 320;  // warp 0 copies, warp 1 issues MMAs, warps 2-9 softmax
+constexpr float kTcRescale = 8.0f;  // log2 of the growth allowed before O is rescaled
+static_assert(kTcKeys == kAttnKeys, "key splits are planned in kAttnKeys tiles");
+
+template <int D>
+struct TcShape {
+    static constexpr uint32_t kQBytes = kTcRows * D * 2;        // D / 64 blocks of [128 rows][64]
+    static constexpr uint32_t kKVBytes = kTcKeys * D * 2;       // D / 64 blocks of [64 keys][64]
+    static constexpr uint32_t kPBytes = kTcRows * kTcKeys * 2;  // [128 rows][64 keys], hi or lo
+    static constexpr uint32_t kQ = 0;
+    static constexpr uint32_t kK = kQ + kQBytes;
+    static constexpr uint32_t kV = kK + kTcStages * kKVBytes;
+    static constexpr uint32_t kP = kV + kTcStages * kKVBytes;
+    static constexpr uint32_t kBar = kP + 2 * kPBytes;
+    static constexpr size_t smem_bytes = kBar + 128 + 6 * kTcRows * 4 + 1024;  // barriers, row maxima and sums, alignment
+};
+
+struct TcBars {
+    uint64_t kv_full[kTcStages];   // warp 0 -> MMA: tile copied
+    uint64_t kv_empty[kTcStages];  // MMA (commit) -> warp 0: the tile's P V is done
+    uint64_t s_full[2];            // MMA (commit) -> softmax: scores in the buffer
+    uint64_t s_free[2];            // softmax (256) -> MMA: scores read
+    uint64_t p_full;               // softmax (256) -> MMA: P written (and O rescaled)
+    uint64_t o_done;               // MMA (commit) -> softmax: the tile's P V is done
+    uint64_t q_ready;              // softmax (256) -> MMA: query rows copied
+    uint64_t drain;                // unwinding after an expired wait
+    uint32_t tmem_base;
+    int32_t abort;
+};
+
+// Byte offset of 16-byte piece `chunk` (0..7) of row `row` in a 128-byte-swizzled block of
+// 128-byte rows (the layout the tcgen05 descriptors with 128-byte swizzle read).
+__device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t chunk) {
+    return (row >> 3) * 1024u + (row & 7u) * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+static_assert(sizeof(TcBars) <= 128, "the row maxima follow the barriers");
+
+// bar.sync over `n` threads of barrier `id` that also returns the OR of every thread's `pred`.
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                             const AttnArgs a) {
+    using S = TcShape<D>;
+    constexpr uint32_t kTmemCols = 256;  // S buffers at 0 and 64, O at 128
+    extern __shared__ uint8_t tc_smem_raw[];
+    const uint32_t raw_addr = smem_u32(tc_smem_raw);
+    uint8_t *base = tc_smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    TcBars *bar = reinterpret_cast<TcBars *>(base + S::kBar);
+    volatile int32_t *abort_flag = &bar->abort;
+    const int32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t qt = blockIdx.x % a.q_tiles, pair = blockIdx.x / a.q_tiles;
+    const int32_t b = pair / a.Hk, hk = pair - b * a.Hk;
+    const int32_t total = a.P + a.n, num_tiles = (total + kTcKeys - 1) / kTcKeys;
+    const int32_t t_begin = blockIdx.y * a.tiles_per_split;
+    const int32_t T = max(0, min(num_tiles, t_begin + a.tiles_per_split) - t_begin);
+
+    pdl_launch_dependents();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(&bar->kv_full[s], 1);
+            mbar_init(&bar->kv_empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar->s_full[i], 1);
+            mbar_init(&bar->s_free[i], 256);
+        }
+        mbar_init(&bar->p_full, 256);
+        mbar_init(&bar->o_done, 1);
+        mbar_init(&bar->q_ready, 256);
+        mbar_init(&bar->drain, 1);
+        bar->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bar->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar->tmem_base;
+    pdl_wait();  // qkv (rotated) and the caches come from earlier kernels
+
+    if (warp == 0) {
+        // ---------------- key/value copies ----------------
+        // A tile of cached keys only: four (D = 128) or two tensor copies from the cache, counted
+        // in bytes on the stage's barrier.  A tile with tree keys (the last one or two): 16-byte
+        // copies of the qkv rows by the whole warp, then one arrival.
+        if (lane == 0) {
+            prefetch_tensormap(&tmap_k);
+            prefetch_tensormap(&tmap_v);
+        }
+        for (int32_t i = 0; i < T; ++i) {
+            const int32_t st = i % kTcStages;
+            if (i >= kTcStages) {
+                int32_t ok = 1;
+                if (lane == 0 && !mbar_wait(&bar->kv_empty[st], static_cast<uint32_t>(i / kTcStages - 1) & 1u, abort_flag)) {
+                    ok = 0;
+                    *abort_flag = 1;
+                }
+                if (!__shfl_sync(kFullMask, ok, 0)) break;
+            }
+            if (*abort_flag) break;
+            const int32_t key0 = (t_begin + i) * kTcKeys;
+            uint8_t *kd = base + S::kK + st * S::kKVBytes, *vd = base + S::kV + st * S::kKVBytes;
+            if (key0 + kTcKeys <= a.P) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bar->kv_full[st], 2u * S::kKVBytes);
+#pragma unroll
+                    for (int blk = 0; blk < D / 64; ++blk) {
+                        tma_load_4d(kd + blk * (kTcKeys * 128), &tmap_k, &bar->kv_full[st], blk * 64, hk, key0, b);
+                        tma_load_4d(vd + blk * (kTcKeys * 128), &tmap_v, &bar->kv_full[st], blk * 64, hk, key0, b);
+                    }
+                }
+                __syncwarp();
+                continue;
+            }
+            fence_proxy_async_smem();  // the tensor cores' reads of this stage, before these writes
+            for (int32_t c = lane; c < kTcKeys * (D / 8); c += 32) {
+                const int32_t j = c / (D / 8), ch = c - j * (D / 8), key = key0 + j;
+                const __nv_bfloat16 *kp = a.qkv, *vp = a.qkv;
+                bool ok = true;
+                if (key < a.P) {
+                    const int64_t off = ((static_cast<int64_t>(b) * a.P + key) * a.Hk + hk) * D + ch * 8;
+                    kp = a.k_cache + off;
+                    vp = a.v_cache + off;
+                } else if (key < total) {
+                    const int64_t row = static_cast<int64_t>(b) * a.n + (key - a.P);
+                    kp = a.qkv + row * a.nqkv + (a.H + hk) * D + ch * 8;
+                    vp = a.qkv + row * a.nqkv + (a.H + a.Hk + hk) * D + ch * 8;
+                } else {
+                    ok = false;  // past the last key: zeros (P is 0 there; V must stay finite)
+                }
+                const uint32_t off = static_cast<uint32_t>(ch >> 3) * (kTcKeys * 128u) + sw128_off(j, ch & 7);
+                cp_async16(kd + off, kp, ok);
+                cp_async16(vd + off, vp, ok);
+            }
+            cp_async_commit();
+            cp_async_wait_all();
+            fence_proxy_async_smem();  // visible to the tensor cores
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar->kv_full[st]);
+        }
+        cp_async_wait_all();
+    } else if (warp == 1) {
+        // ---------------- MMA issue (one thread) ----------------
+        if (lane == 0 && T > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kTcRows, kTcKeys);
+            constexpr uint32_t idesc_o = idesc_bf16_f32_bmn(kTcRows, D);
+            const uint32_t q0 = smem_u32(base + S::kQ);
+            auto issue_s = [&](int32_t i) -> bool {
+                const int32_t st = i % kTcStages, sb = i & 1;
+                if (!mbar_wait(&bar->kv_full[st], static_cast<uint32_t>(i / kTcStages) & 1u, abort_flag)) return false;
+                if (i >= 2 && !mbar_wait(&bar->s_free[sb], static_cast<uint32_t>((i - 2) >> 1) & 1u, abort_flag))
+                    return false;
+                tc_fence_after();
+                const uint32_t k0 = smem_u32(base + S::kK + st * S::kKVBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t blk = kk >> 2, col = (kk & 3) * 32u;
+                    mma_bf16_ss(tmem + sb * kTcKeys, sw128_kmajor_desc(q0 + blk * (kTcRows * 128u) + col),
+                                sw128_kmajor_desc(k0 + blk * (kTcKeys * 128u) + col), idesc_s, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar->s_full[sb]);
+                return true;
+            };
+            bool ok = mbar_wait(&bar->q_ready, 0, abort_flag);
+            if (ok) ok = issue_s(0);
+            for (int32_t i = 0; i < T && ok; ++i) {
+                if (i + 1 < T && !issue_s(i + 1)) {
+                    ok = false;
+                    break;
+                }
+                if (!mbar_wait(&bar->p_full, static_cast<uint32_t>(i) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int32_t st = i % kTcStages;
+                const uint32_t v0 = smem_u32(base + S::kV + st * S::kKVBytes);
+                const uint32_t ph = smem_u32(base + S::kP);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < kTcKeys / 16; ++kk)  // 16 keys: two groups of 8 rows of V
+                        mma_bf16_ss(tmem + 128u, sw128_kmajor_desc(ph + part * S::kPBytes + kk * 32u),
+                                    sw128_desc(v0 + kk * 2048u, kTcKeys * 128u, 1024u), idesc_o,
+                                    (i > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bar->o_done);
+                mma_commit(&bar->kv_empty[st]);
+            }
+            if (!ok) *abort_flag = 1;
+        }
+        __syncwarp();
+    } else {
+        // ---------------- softmax and output: two threads a query row ----------------
+        // warps 2-9: lane quarter w % 4 of TMEM (the rows), half h of each tile's keys and of O's
+        // columns; the two halves of a row agree on its running max through shared memory
+        const int32_t q = warp & 3, h = (warp - 2) >> 2, r = q * 32 + lane;
+        const int32_t gr = qt * kTcRows + r;
+        const bool live = gr < a.Mq;
+        const int32_t node = live ? gr / a.group : 0, g = live ? gr - node * a.group : 0;
+        {
+            const __nv_bfloat16 *src = a.qkv + static_cast<int64_t>(b * a.n + node) * a.nqkv + (hk * a.group + g) * D;
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c) {
+                const int ch = h * (D / 16) + c;
+                cp_async16(base + S::kQ + (ch >> 3) * (kTcRows * 128u) + sw128_off(r, ch & 7), src + ch * 8, live);
+            }
+            cp_async_commit();
+            cp_async_wait_all();
+            fence_proxy_async_smem();
+            mbar_arrive(&bar->q_ready);
+        }
+        const uint32_t *mrow = a.mask + static_cast<int64_t>(b * a.n + node) * a.W;
+        const float sl2 = rsqrtf(static_cast<float>(D)) * 1.4426950408889634f;  // 1/sqrt(D), base 2
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t o_cols = 128u + static_cast<uint32_t>(h * (D / 2));     // this half's columns of O
+        uint8_t *ph = base + S::kP, *pl = ph + S::kPBytes;
+        // [2 tiles][2 halves][128 rows] of row maxima, then [2 halves][128 rows] of row sums
+        float *xmax = reinterpret_cast<float *>(base + S::kBar + 128);
+        float m2 = -INFINITY, l = 0.0f;
+        for (int32_t i = 0; i < T; ++i) {
+            const int32_t sb = i & 1, key0 = (t_begin + i) * kTcKeys + h * 32;
+            // an expired wait marks the CTA; the softmax warps leave the loop together, at the
+            // barrier below, whose OR of the mark they all receive
+            if (!mbar_wait(&bar->s_full[sb], static_cast<uint32_t>(i >> 1) & 1u, abort_flag)) *abort_flag = 1;
+            __syncwarp();
+            tc_fence_after();
+            float s[32];
+            {
+                uint32_t v[32];
+                tmem_ld_32(t_lane + sb * kTcKeys + h * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(v[j]);
+            }
+            tc_fence_before();
+            mbar_arrive(&bar->s_free[sb]);
+            // hidden keys to -inf (cached keys are visible, tree keys by the mask row)
+            if (!live || key0 + 32 > a.P) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int32_t key = key0 + j;
+                    bool vis = live && key < total;
+                    if (vis && key >= a.P) {
+                        const int32_t tn = key - a.P;
+                        vis = (mrow[tn >> 5] >> (tn & 31)) & 1u;
+                    }
+                    if (!vis) s[j] = -INFINITY;
+                }
+            }
+            float mq[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+            for (int j = 4; j < 32; ++j) mq[j & 3] = fmaxf(mq[j & 3], s[j]);
+            xmax[((i & 1) * 2 + h) * kTcRows + r] = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+            if (named_barrier_or(1, 256, *abort_flag != 0)) break;
+            const float mx = fmaxf(xmax[((i & 1) * 2) * kTcRows + r], xmax[((i & 1) * 2 + 1) * kTcRows + r]) * sl2;
+            const bool raise = mx > m2 + kTcRescale || (m2 == -INFINITY && mx > -INFINITY);
+            float corr = 1.0f;
+            if (raise) {
+                corr = (m2 == -INFINITY) ? 0.0f : ex2_approx(m2 - mx);
+                l *= corr;
+                m2 = mx;
+            }
+            // P = 2^(s sl2 - m) as bf16 hi + lo, in registers before the previous P V is waited for
+            const float mneg = (m2 == -INFINITY) ? 0.0f : -m2;  // hidden keys: 2^-inf = 0
+            uint32_t hi[16], lo[16];
+            float lsum[2] = {0.0f, 0.0f};
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const float p0 = ex2_approx(fmaf(s[2 * u], sl2, mneg));
+                const float p1 = ex2_approx(fmaf(s[2 * u + 1], sl2, mneg));
+                lsum[u & 1] += p0 + p1;
+                const __nv_bfloat162 hv = __floats2bfloat162_rn(p0, p1);
+                const float2 hf = __bfloat1622float2(hv);
+                const __nv_bfloat162 lv = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+                hi[u] = *reinterpret_cast<const uint32_t *>(&hv);
+                lo[u] = *reinterpret_cast<const uint32_t *>(&lv);
+            }
+            l += lsum[0] + lsum[1];
+            // the previous tile's P V is done: P's buffer is free and O holds every earlier tile
+            if (i > 0 && !mbar_wait(&bar->o_done, static_cast<uint32_t>(i - 1) & 1u, abort_flag)) *abort_flag = 1;
+            __syncwarp();
+            tc_fence_after();
+            if (i > 0 && __any_sync(kFullMask, raise && corr != 0.0f)) {
+                // rescale this warp's rows of this half of O (a warp-wide TMEM round trip)
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32(t_lane + o_cols + c * 32u, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * corr);
+                    tmem_st_32(t_lane + o_cols + c * 32u, v);
+                }
+                tmem_wait_st();
+            }
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+                const uint32_t off = sw128_off(r, h * 4 + c8);
+                *reinterpret_cast<uint4 *>(ph + off) = make_uint4(hi[4 * c8], hi[4 * c8 + 1], hi[4 * c8 + 2], hi[4 * c8 + 3]);
+                *reinterpret_cast<uint4 *>(pl + off) = make_uint4(lo[4 * c8], lo[4 * c8 + 1], lo[4 * c8 + 2], lo[4 * c8 + 3]);
+            }
+            fence_proxy_async_smem();  // the writes above, before the MMA reads them
+            tc_fence_before();         // and the rescale's TMEM stores
+            mbar_arrive(&bar->p_full);
+        }
+        if (!*abort_flag && T > 0 && !mbar_wait(&bar->o_done, static_cast<uint32_t>(T - 1) & 1u, abort_flag))
+            *abort_flag = 1;
+        // the row's sum: both halves' shares (every softmax thread reaches this barrier)
+        xmax[(4 + h) * kTcRows + r] = l;
+        const bool stop = named_barrier_or(1, 256, *abort_flag != 0);
+        const float lt = xmax[4 * kTcRows + r] + xmax[5 * kTcRows + r];
+        __syncwarp();
+        if (!stop) {
+            tc_fence_after();
+            const int64_t prow = static_cast<int64_t>(blockIdx.y) * a.B * a.Hk * a.Mq + static_cast<int64_t>(pair) * a.Mq + gr;
+            __nv_bfloat16 *orow = a.o + static_cast<int64_t>(b * a.n + node) * a.H * D + (hk * a.group + g) * D + h * (D / 2);
+            const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t v[32];
+                tmem_ld_32(t_lane + o_cols + c * 32u, v);
+                tmem_wait_ld();
+                if (!live) continue;
+                if (a.splits == 1) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 pk;
+                        uint32_t *pw = reinterpret_cast<uint32_t *>(&pk);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(v[e + 2 * u]) * inv,
+                                                                            __uint_as_float(v[e + 2 * u + 1]) * inv);
+                            pw[u] = *reinterpret_cast<const uint32_t *>(&hv);
+                        }
+                        *reinterpret_cast<uint4 *>(orow + c * 32 + e) = pk;
+                    }
+                } else {
+                    float *po = a.part_o + prow * D + h * (D / 2) + c * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(po + e) =
+                            make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                                        __uint_as_float(v[e + 3]));
+                }
+            }
+            if (live && a.splits > 1 && h == 0) a.part_ml[prow] = make_float2(m2 * 0.6931471805599453f, lt);
+        }
+    }
+
+    // ---------------- teardown ----------------
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (*abort_flag && warp == 1 && lane == 0) {
+        // let every MMA this CTA issued land before its memory is handed on
+        mma_commit(&bar->drain);
+        mbar_wait(&bar->drain, 0, nullptr);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
 // Merges the key splits of each query row: o = sum_s w_s O_s / sum_s w_s l_s with
 // w_s = exp(m_s - max_s m_s) (0 for a split that saw no visible key).  A warp per query row: lane
 // s reads split s's (max, sum) (at most 32 splits), then each lane sums 4 output columns.
@@ -797,6 +1203,7 @@ constexpr int32_t kAttnMaxSplits = 32;
 struct AttnPlan {
     int32_t group, Mq, qw, kw, warps, rows_cta, q_tiles, splits_max;
     bool few;  // at most 8 query rows per (request, kv head): tree_attention_few_kernel
+    bool tc;   // head_dim 64 or 128 and more than 64 query rows: tree_attention_tc_kernel
 };
 
 AttnPlan attn_plan(const eagle_decoder_layer_weights *w, int32_t batch, int32_t nodes, int32_t sms) {
@@ -809,6 +1216,11 @@ AttnPlan attn_plan(const eagle_decoder_layer_weights *w, int32_t batch, int32_t 
     p.rows_cta = p.qw * 16;
     p.q_tiles = (p.Mq + p.rows_cta - 1) / p.rows_cta;
     p.few = p.Mq <= 8;  // one warp's 16-row tile would be half padding: the transposed kernel
+    p.tc = (w->head_dim == 64 || w->head_dim == 128) && p.Mq > 64;
+    if (p.tc) {
+        p.rows_cta = kTcRows;
+        p.q_tiles = (p.Mq + kTcRows - 1) / kTcRows;
+    }
     const int64_t ctas = static_cast<int64_t>(batch) * w->kv_heads * p.q_tiles;
     p.splits_max = ctas >= 2 * sms ? 1 : static_cast<int32_t>(std::min<int64_t>(kAttnMaxSplits, (2 * sms + ctas - 1) / ctas));
     return p;
@@ -890,11 +1302,22 @@ cudaError_t set_attention_smem() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(tree_attention_few_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int32_t>(AttnShape<D>::smem_bytes(16)));
+    if constexpr (D == 64 || D == 128) {
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(tree_attention_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int32_t>(TcShape<D>::smem_bytes));
+    }
     return e;
 }
 
 template <int D>
-cudaError_t launch_attention(const AttnPlan &ap, dim3 grid, const AttnArgs &aa, cudaStream_t st) {
+cudaError_t launch_attention(const AttnPlan &ap, dim3 grid, const AttnArgs &aa, const CUtensorMap &tk,
+                             const CUtensorMap &tv, cudaStream_t st) {
+    if constexpr (D == 64 || D == 128) {
+        if (ap.tc)
+            return launch_pdl(tree_attention_tc_kernel<D>, grid, dim3(kTcThreads), TcShape<D>::smem_bytes, st, tk, tv,
+                              aa);
+    }
     const dim3 block(ap.warps * 32);
     const size_t smem = AttnShape<D>::smem_bytes(ap.rows_cta);
     if (ap.few) return launch_pdl(tree_attention_few_kernel<D>, grid, block, smem, st, aa);
@@ -996,11 +1419,17 @@ eagle_status eagle_decoder_layer(const eagle_decoder_layer_weights *w, int32_t b
                 reinterpret_cast<const __nv_bfloat16 *>(d_v_cache), d_mask, o,
                 reinterpret_cast<float *>(at(L.part_o)), reinterpret_cast<float2 *>(at(L.part_ml))};
     const dim3 agrid(batch * Hk * ap.q_tiles, splits);
+    // the tensor-core kernel reads whole tiles of cached keys by tensor copies
+    CUtensorMap tk{}, tv{};
+    if (ap.tc && prefix > 0 &&
+        (!encode_kv_cache_map(&tk, d_k_cache, batch, prefix, Hk, D) ||
+         !encode_kv_cache_map(&tv, d_v_cache, batch, prefix, Hk, D)))
+        return EAGLE_ERR_CUDA;
     switch (D) {
-        case 32: DEC_CUDA(launch_attention<32>(ap, agrid, aa, st)); break;
-        case 64: DEC_CUDA(launch_attention<64>(ap, agrid, aa, st)); break;
-        case 96: DEC_CUDA(launch_attention<96>(ap, agrid, aa, st)); break;
-        default: DEC_CUDA(launch_attention<128>(ap, agrid, aa, st)); break;
+        case 32: DEC_CUDA(launch_attention<32>(ap, agrid, aa, tk, tv, st)); break;
+        case 64: DEC_CUDA(launch_attention<64>(ap, agrid, aa, tk, tv, st)); break;
+        case 96: DEC_CUDA(launch_attention<96>(ap, agrid, aa, tk, tv, st)); break;
+        default: DEC_CUDA(launch_attention<128>(ap, agrid, aa, tk, tv, st)); break;
     }
     if (splits > 1)
         DEC_CUDA(launch_pdl(attention_combine_kernel, dim3((batch * Hk * ap.Mq + kCombineRows - 1) / kCombineRows),

@@ -836,6 +836,22 @@ bool encode_plan_out(LinearPlan *p, const void *out) {
 
 }  // namespace
 
+bool encode_kv_cache_map(CUtensorMap *map, const void *cache, int32_t B, int32_t P, int32_t Hk, int32_t D) {
+    EncodeTiledFn fn = encoder();
+    if (!fn || B < 1 || P < 1 || Hk < 1 || (D != 64 && D != 128)) return false;
+    if (reinterpret_cast<uintptr_t>(cache) % 16 != 0) return false;
+    // [B][P][Hk][D] bf16 as dims (D, Hk, P, B); one box is 64 head dims of one kv head for 64 keys
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hk), static_cast<cuuint64_t>(P),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hk) * D * 2,
+                             static_cast<cuuint64_t>(P) * Hk * D * 2};
+    cuuint32_t box[4] = {64, 1, 64, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int32_t linear_n_tile(int32_t rows) { return ((rows + 15) / 16) * 16; }
 
 size_t linear_partials_bytes(int32_t grid, int32_t n_tile) {

@@ -101,6 +101,9 @@ struct LinearPlan {
 size_t linear_partials_bytes(int32_t grid, int32_t n_tile);
 size_t linear_counters_bytes(int32_t M, int32_t rows = 1);
 int32_t linear_n_tile(int32_t rows);
+// Tensor map of a bf16 KV cache [B][P][Hk][D] (D 64 or 128) read in boxes of 64 keys x 64 head
+// dims of one kv head, 128-byte swizzled (the tree attention's key and value tiles).
+bool encode_kv_cache_map(CUtensorMap *map, const void *cache, int32_t B, int32_t P, int32_t Hk, int32_t D);
 // CTA pairs of the .cta_group::2 mode that fit on the device at once (0: the mode is off).
 int32_t linear_pair_workers(int32_t num_sms);
 

@@ -108,6 +108,11 @@ CASES = [
     (3, 3, 150, 128, 4, 2, 64, 256, 2),     # 6 query rows of 2-head groups, D = 64, key splits
     (2, 4, 90, 64, 2, 1, 32, 128, 3),       # exactly 8 query rows (MQA pairs), D = 32
     (2, 1, 130, 128, 8, 1, 64, 256, 0),     # a lone root under 8-head groups: 8 query rows of one node
+    # more than 64 query rows per (request, kv head) with D = 64 or 128: the tcgen05 kernel
+    (2, 40, 200, 256, 8, 2, 128, 512, 5),   # 160 rows (two 128-row tiles), ragged keys, key splits
+    (3, 33, 1000, 256, 4, 1, 128, 512, 6),  # MQA, 132 rows, a tile of cached and tree keys, 8 splits
+    (16, 30, 64, 128, 8, 2, 128, 256, 4),   # 120 rows, two key tiles, no key split
+    (2, 50, 129, 128, 4, 2, 64, 256, 5),    # D = 64, 100 rows, three key tiles split
 ]
 
 
