@@ -721,7 +721,7 @@ __device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t n, bool p
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                             const AttnArgs a) {
+                             const __grid_constant__ CUtensorMap tmap_qkv, const AttnArgs a) {
     using S = TcShape<D>;
     constexpr uint32_t kTmemCols = 256;  // S buffers at 0 and 64, O at 128
     extern __shared__ uint8_t tc_smem_raw[];
@@ -766,12 +766,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0) {
         // ---------------- key/value copies ----------------
         // A tile of cached keys only: four (D = 128) or two tensor copies from the cache, counted
-        // in bytes on the stage's barrier.  A tile with tree keys (the last one or two): 16-byte
-        // copies of the qkv rows by the whole warp, then one arrival.
+        // in bytes on the stage's barrier; a tile of tree keys only: the same from the qkv rows
+        // (64 consecutive node rows; rows past the request's nodes are hidden keys, finite, or
+        // zeros past the last row).  The one tile that holds both: 16-byte copies by the whole
+        // warp, then one arrival.
         if (lane == 0) {
             prefetch_tensormap(&tmap_k);
             prefetch_tensormap(&tmap_v);
+            prefetch_tensormap(&tmap_qkv);
         }
+        const uint64_t pol_qkv = policy_evict_last();  // the tree's keys are read by every query tile
         for (int32_t i = 0; i < T; ++i) {
             const int32_t st = i % kTcStages;
             if (i >= kTcStages) {
@@ -792,6 +796,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int blk = 0; blk < D / 64; ++blk) {
                         tma_load_4d(kd + blk * (kTcKeys * 128), &tmap_k, &bar->kv_full[st], blk * 64, hk, key0, b);
                         tma_load_4d(vd + blk * (kTcKeys * 128), &tmap_v, &bar->kv_full[st], blk * 64, hk, key0, b);
+                    }
+                }
+                __syncwarp();
+                continue;
+            }
+            if (key0 >= a.P) {
+                if (lane == 0) {
+                    const int32_t y = b * a.n + (key0 - a.P);
+                    mbar_arrive_expect_tx(&bar->kv_full[st], 2u * S::kKVBytes);
+#pragma unroll
+                    for (int blk = 0; blk < D / 64; ++blk) {
+                        tma_load_2d(kd + blk * (kTcKeys * 128), &tmap_qkv, &bar->kv_full[st], (a.H + hk) * D + blk * 64,
+                                    y, pol_qkv);
+                        tma_load_2d(vd + blk * (kTcKeys * 128), &tmap_qkv, &bar->kv_full[st],
+                                    (a.H + a.Hk + hk) * D + blk * 64, y, pol_qkv);
                     }
                 }
                 __syncwarp();
@@ -919,16 +938,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(&bar->s_free[sb]);
-            // hidden keys to -inf (cached keys are visible, tree keys by the mask row)
+            // hidden keys to -inf (cached keys are visible, tree keys by the mask row: the 32
+            // keys of this half tile span at most two of its words, read once)
             if (!live || key0 + 32 > a.P) {
+                const int32_t t0 = key0 - a.P, first = max(t0, 0) >> 5;
+                const uint32_t w0 = (live && first < a.W) ? mrow[first] : 0u;
+                const uint32_t w1 = (live && first + 1 < a.W) ? mrow[first + 1] : 0u;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const int32_t key = key0 + j;
+                    const int32_t key = key0 + j, tn = t0 + j;
                     bool vis = live && key < total;
-                    if (vis && key >= a.P) {
-                        const int32_t tn = key - a.P;
-                        vis = (mrow[tn >> 5] >> (tn & 31)) & 1u;
-                    }
+                    if (vis && tn >= 0) vis = (((tn >> 5) == first ? w0 : w1) >> (tn & 31)) & 1u;
                     if (!vis) s[j] = -INFINITY;
                 }
             }
@@ -1312,11 +1332,11 @@ cudaError_t set_attention_smem() {
 
 template <int D>
 cudaError_t launch_attention(const AttnPlan &ap, dim3 grid, const AttnArgs &aa, const CUtensorMap &tk,
-                             const CUtensorMap &tv, cudaStream_t st) {
+                             const CUtensorMap &tv, const CUtensorMap &tq, cudaStream_t st) {
     if constexpr (D == 64 || D == 128) {
         if (ap.tc)
             return launch_pdl(tree_attention_tc_kernel<D>, grid, dim3(kTcThreads), TcShape<D>::smem_bytes, st, tk, tv,
-                              aa);
+                              tq, aa);
     }
     const dim3 block(ap.warps * 32);
     const size_t smem = AttnShape<D>::smem_bytes(ap.rows_cta);
@@ -1420,16 +1440,19 @@ eagle_status eagle_decoder_layer(const eagle_decoder_layer_weights *w, int32_t b
                 reinterpret_cast<float *>(at(L.part_o)), reinterpret_cast<float2 *>(at(L.part_ml))};
     const dim3 agrid(batch * Hk * ap.q_tiles, splits);
     // the tensor-core kernel reads whole tiles of cached keys by tensor copies
-    CUtensorMap tk{}, tv{};
+    CUtensorMap tk{}, tv{}, tq{};
     if (ap.tc && prefix > 0 &&
         (!encode_kv_cache_map(&tk, d_k_cache, batch, prefix, Hk, D) ||
          !encode_kv_cache_map(&tv, d_v_cache, batch, prefix, Hk, D)))
         return EAGLE_ERR_CUDA;
+    if (ap.tc && !encode_bf16_rows_map(&tq, qkv, static_cast<uint64_t>(nqkv), static_cast<uint64_t>(rows),
+                                       static_cast<uint64_t>(nqkv), 64, kTcKeys))
+        return EAGLE_ERR_CUDA;
     switch (D) {
-        case 32: DEC_CUDA(launch_attention<32>(ap, agrid, aa, tk, tv, st)); break;
-        case 64: DEC_CUDA(launch_attention<64>(ap, agrid, aa, tk, tv, st)); break;
-        case 96: DEC_CUDA(launch_attention<96>(ap, agrid, aa, tk, tv, st)); break;
-        default: DEC_CUDA(launch_attention<128>(ap, agrid, aa, tk, tv, st)); break;
+        case 32: DEC_CUDA(launch_attention<32>(ap, agrid, aa, tk, tv, tq, st)); break;
+        case 64: DEC_CUDA(launch_attention<64>(ap, agrid, aa, tk, tv, tq, st)); break;
+        case 96: DEC_CUDA(launch_attention<96>(ap, agrid, aa, tk, tv, tq, st)); break;
+        default: DEC_CUDA(launch_attention<128>(ap, agrid, aa, tk, tv, tq, st)); break;
     }
     if (splits > 1)
         DEC_CUDA(launch_pdl(attention_combine_kernel, dim3((batch * Hk * ap.Mq + kCombineRows - 1) / kCombineRows),

@@ -836,6 +836,11 @@ bool encode_plan_out(LinearPlan *p, const void *out) {
 
 }  // namespace
 
+bool encode_bf16_rows_map(CUtensorMap *map, const void *ptr, uint64_t cols, uint64_t rows, uint64_t ld,
+                          uint32_t box_cols, uint32_t box_rows) {
+    return encode_bf16_2d(map, ptr, cols, rows, ld, box_cols, box_rows);
+}
+
 bool encode_kv_cache_map(CUtensorMap *map, const void *cache, int32_t B, int32_t P, int32_t Hk, int32_t D) {
     EncodeTiledFn fn = encoder();
     if (!fn || B < 1 || P < 1 || Hk < 1 || (D != 64 && D != 128)) return false;

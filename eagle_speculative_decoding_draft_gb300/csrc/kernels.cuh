@@ -104,6 +104,10 @@ int32_t linear_n_tile(int32_t rows);
 // Tensor map of a bf16 KV cache [B][P][Hk][D] (D 64 or 128) read in boxes of 64 keys x 64 head
 // dims of one kv head, 128-byte swizzled (the tree attention's key and value tiles).
 bool encode_kv_cache_map(CUtensorMap *map, const void *cache, int32_t B, int32_t P, int32_t Hk, int32_t D);
+// Tensor map of a bf16 matrix [rows][ld] (cols used) in boxes of box_cols x box_rows, 128-byte
+// swizzled.
+bool encode_bf16_rows_map(CUtensorMap *map, const void *ptr, uint64_t cols, uint64_t rows, uint64_t ld,
+                          uint32_t box_cols, uint32_t box_rows);
 // CTA pairs of the .cta_group::2 mode that fit on the device at once (0: the mode is off).
 int32_t linear_pair_workers(int32_t num_sms);
 
