@@ -385,6 +385,8 @@ constexpr int kStreamThreads = kStreamConsumers + 32;  // + the producer warp
 constexpr uint32_t kChunkBytes = 16384;
 constexpr int kStreamStages = 6;
 constexpr int kWarpCap = 64;  // a warp's candidate buffer
+constexpr int kSeedChunks = 4;  // chunks whose lane maxima give the first threshold
+static_assert(kSeedChunks <= kStreamStages, "the seed's chunks are all in the ring at once");
 
 struct StreamSmem {
     uint64_t full[kStreamStages];
@@ -532,15 +534,33 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
             const int32_t col0 = c * static_cast<int32_t>(kChunkBytes / sizeof(T));
             const uint8_t *stage = ring + st * kChunkBytes;
             if (!kBestOnly && c == 0) {
-                // before any element is kept: a threshold from the lane maxima of this chunk, so
-                // that few elements enter the buffers and few compactions follow
+                // before any element is kept: a threshold from the lane maxima of the first
+                // kSeedChunks chunks (already in the ring), so that few elements enter the
+                // buffers and few rounds take the candidate path
+                const int32_t nseed = min(nchunk, kSeedChunks);
+                int32_t all = got;
+                for (int32_t c2 = 1; c2 < nseed; ++c2) {
+                    int32_t g2 = 1;
+                    if (lane == 0) g2 = mbar_wait(&sm->full[c2], 0u, &sm->abort);
+                    if (!__shfl_sync(kFullMask, g2, 0)) all = 0;
+                }
+                __syncwarp();
+                if (!all) {
+                    sm->abort = 1;
+                    latch(status, kDevTimeout);
+                }
                 float lm = -INFINITY;  // fmaxf drops NaN: never NaN
-                if (got)
-                    for (int32_t v = warp * 32 + lane; v < nv; v += kStreamConsumers) {
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(stage + v * 16);
-                        const T *e = reinterpret_cast<const T *>(&raw);
+                if (all)
+                    for (int32_t c2 = 0; c2 < nseed; ++c2) {
+                        const uint8_t *stg = ring + c2 * kChunkBytes;
+                        const int32_t nv2 =
+                            static_cast<int32_t>(min(kChunkBytes, row_bytes - static_cast<uint32_t>(c2) * kChunkBytes) / 16u);
+                        for (int32_t v = warp * 32 + lane; v < nv2; v += kStreamConsumers) {
+                            const uint4 raw = *reinterpret_cast<const uint4 *>(stg + v * 16);
+                            const T *e = reinterpret_cast<const T *>(&raw);
 #pragma unroll
-                        for (int j = 0; j < EPV; ++j) lm = fmaxf(lm, to_f32(e[j]));
+                            for (int j = 0; j < EPV; ++j) lm = fmaxf(lm, to_f32(e[j]));
+                        }
                     }
                 thr = stream_seed_threshold(sm, lm, warp, lane, k);
             }
