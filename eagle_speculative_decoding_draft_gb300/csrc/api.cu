@@ -30,6 +30,7 @@ struct Layout {
     size_t status, counters, partials, x, fhat, logits, row_ids, row_logp, row_lse;
     size_t pool_tok, pool_S, pool_par, pool_row, front_cand, front_S;
     size_t root_tok, node_tok, node_src, g, node_x, node_fhat, ext_x, ext_fhat;
+    size_t xtickets;      // per request: rows of the level whose top-k is done (fused expand)
     // static tree (EAGLE-1) constants per node, and the drafted nodes' scores
     size_t sp_node, sp_mask, node_S;
     size_t st_feat, st_tok, st_pos, st_tokens, st_parents, st_positions, st_mask, st_acc_len,
@@ -168,6 +169,7 @@ Layout make_layout(const eagle_tree_config *c, int32_t num_sms, const StaticShap
     L.st_pos = take(static_cast<size_t>(B) * 4);
     L.st_in_end = o;
     L.counters = take(L.counters_bytes);
+    L.xtickets = take(static_cast<size_t>(B) * 4);  // zero at init, like the tile tickets
     L.partials = take(L.partials_bytes);
     L.x = take(static_cast<size_t>(L.r_pad) * 2 * h * L.eb);
     L.fhat = take(static_cast<size_t>(d) * L.r_pad * h * L.eb);
@@ -461,9 +463,12 @@ static eagle_status init_handle(const eagle_tree_config *cfg, const StaticShape 
                 return EAGLE_ERR_UNSUPPORTED;
             }
             if (!plan_seq(&t->fc[l], cfg->fc_weight, 2 * h, h, 2 * h, t->ws + L.x, 2 * h, R, cfg->fc_bias,
-                          t->fhat_level(l), h, 1, 2, t->partials, t->counters, t->status, sms) ||
-                !plan_seq(&t->lm[l], cfg->lm_head, h, V, h, t->fhat_level(l), h, R, nullptr,
-                          t->ws + L.logits, V, 0, 4, t->partials, t->counters, t->status, sms)) {
+                          t->fhat_level(l), h, 1, 2, t->partials, t->counters, t->status, sms)) {
+                delete t;
+                return EAGLE_ERR_UNSUPPORTED;
+            }
+            if (!plan_seq(&t->lm[l], cfg->lm_head, h, V, h, t->fhat_level(l), h, R, nullptr, t->ws + L.logits, V, 0,
+                          4, t->partials, t->counters, t->status, sms)) {
                 delete t;
                 return EAGLE_ERR_UNSUPPORTED;
             }
@@ -545,10 +550,10 @@ static eagle_status level_tail(eagle_tree *t, int32_t level, float *d_logits_out
         ++t->launches;
     }
     // log-softmax + top-k children of every row
-    EAGLE_CUDA(launch_row_topk(lg, 0, R, V, V, L.kk, t->at<int32_t>(L.row_ids), t->at<float>(L.row_logp),
-                               t->at<float>(L.row_lse), st, t->status));
-    ++t->launches;
     if (t->is_static) {
+        EAGLE_CUDA(launch_row_topk(lg, 0, R, V, V, L.kk, t->at<int32_t>(L.row_ids), t->at<float>(L.row_logp),
+                                   t->at<float>(L.row_lse), st, t->status));
+        ++t->launches;
         // the nodes of depth level+1 take their ranked tokens; those with children get their rows
         const StaticShape &sh = t->shape;
         const bool more_s = level < d - 1;
@@ -604,8 +609,18 @@ static eagle_status level_tail(eagle_tree *t, int32_t level, float *d_logits_out
     e.emb = c.embedding;
     e.x_next = more ? x : nullptr;
     e.status = t->status;
-    EAGLE_CUDA(launch_expand(e, st));
+    // the top-k launch runs the expand too when it copies no rows (its last finishing row of each
+    // request does the request's expand)
+    FusedExpand fx{nullptr, 0, nullptr};
+    if (e.x_next == nullptr) fx = FusedExpand{&e, level == 0 ? 1 : k, t->at<int32_t>(L.xtickets)};
+    bool fused = false;
+    EAGLE_CUDA(launch_row_topk(lg, 0, R, V, V, L.kk, t->at<int32_t>(L.row_ids), t->at<float>(L.row_logp),
+                               t->at<float>(L.row_lse), st, t->status, &fx, &fused));
     ++t->launches;
+    if (!fused) {
+        EAGLE_CUDA(launch_expand(e, st));
+        ++t->launches;
+    }
     t->next_level = level + 1;
     if (more) t->front_current = out_buf;
     return EAGLE_OK;

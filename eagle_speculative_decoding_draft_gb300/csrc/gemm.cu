@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t unit = static_cast<int32_t>(div_nonneg(kb, nkb));
                 const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(unit) * nkb) * BK;
                 expect(static_cast<int>(i));
-                load_w(static_cast<int>(i), kx, unit / nch);
+                load_w(static_cast<int>(i), kx, nch == 1 ? unit : unit / nch);
                 issued |= 1u << i;
             }
             pdl_wait();
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t kb = kb_begin + i;
                 const int32_t unit = static_cast<int32_t>(div_nonneg(kb, nkb));
                 const int32_t kx = static_cast<int32_t>(kb - static_cast<int64_t>(unit) * nkb) * BK;
-                load_x(static_cast<int>(i), kx, unit - (unit / nch) * nch);
+                load_x(static_cast<int>(i), kx, nch == 1 ? 0 : unit - (unit / nch) * nch);
             }
             uint32_t stage = static_cast<uint32_t>(n_pre % stages);
             uint32_t phase = (n_pre == stages) ? 1u : 0u;
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     latch(a.status, kDevTimeout);
                     break;
                 }
-                const int32_t wu = unit / nch;
+                const int32_t wu = nch == 1 ? unit : unit / nch;
                 expect(static_cast<int>(stage));
                 load_w(static_cast<int>(stage), kx, wu);
                 load_x(static_cast<int>(stage), kx, unit - wu * nch);
@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int32_t gi = 0;  // 16-row groups sent by bulk stores
         for (int64_t kb = kb_begin; kb < kb_end;) {
             const int32_t unit = static_cast<int32_t>(div_nonneg(kb, nkb));
-            const int32_t wu = unit / nch, chunk = unit - wu * nch;
+            const int32_t wu = nch == 1 ? unit : unit / nch, chunk = unit - wu * nch;
             const int32_t tile = kPair ? 2 * wu + rank : wu;       // this CTA's 128 weight rows
             const int32_t ticket = kPair ? 2 * unit + rank : unit;  // its (weight tile, row chunk)
             const int32_t row0 = chunk * a.n_tile, rows_c = min(a.n_tile, a.rows - row0);

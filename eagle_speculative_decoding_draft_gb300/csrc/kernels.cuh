@@ -135,9 +135,19 @@ cudaError_t launch_linear_f32(const float *w, int64_t ldw, const float *x, int64
 // least 32 KB, one CTA per row streaming it once through shared memory.  `status` (may be null)
 // receives kDevTimeout if a streamed copy does not land in time.
 // ---------------------------------------------------------------------------------------------
+struct ExpandArgs;
+// The expand of a draft level run inside the top-k launch: the last row of each request to finish
+// (a ticket per request, zero before and after) runs that request's expand.  Only for an expand
+// without row copies (x_next null).
+struct FusedExpand {
+    const ExpandArgs *args;  // null: no fused expand
+    int32_t rows_per_req;
+    int32_t *tickets;        // [B]
+};
 cudaError_t launch_row_topk(const void *logits, int32_t is_bf16, int32_t rows, int32_t V,
                             int64_t ld, int32_t k, int32_t *ids, float *vals, float *lse,
-                            cudaStream_t st, int32_t *status = nullptr);
+                            cudaStream_t st, int32_t *status = nullptr, const FusedExpand *fx = nullptr,
+                            bool *fused = nullptr);
 
 // ---------------------------------------------------------------------------------------------
 // Tree kernels

@@ -28,6 +28,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "expand.cuh"
 #include "kernels.cuh"
 #include "select.cuh"
 
@@ -90,7 +91,8 @@ __device__ __forceinline__ void visit(const T *z, const uint4 (&cache)[kCacheVec
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2)
     row_topk_kernel(const T *__restrict__ logits, int32_t V, int64_t ld, int32_t k,
-                    int32_t *__restrict__ ids, float *__restrict__ vals, float *__restrict__ lse_out) {
+                    int32_t *__restrict__ ids, float *__restrict__ vals, float *__restrict__ lse_out,
+                    const ExpandArgs ea, int32_t fx_rows, int32_t *fx_tickets) {
     constexpr int EPV = 16 / sizeof(T);
     __shared__ float s_max[kWarps], s_kth[kWarps], s_sum[kWarps];
     __shared__ float c_v[kCand];
@@ -329,6 +331,24 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
         if (want_lse && tid == 0) lse_out[row] = lse;
+        if (fx_rows > 0) {
+            // fused expand: the last of a request's rows to finish runs the request's expand
+            __shared__ int32_t s_last;
+            __shared__ ExpandSmem esm;
+            __syncthreads();  // this row's ids and values are written
+            const int32_t req = row / fx_rows;
+            if (tid == 0) {
+                __threadfence();  // release them before the ticket
+                const int32_t prev = atomicAdd(&fx_tickets[req], 1);
+                s_last = (prev == fx_rows - 1) ? 1 : 0;
+                if (s_last) {
+                    fx_tickets[req] = 0;  // ready for the next launch
+                    __threadfence();      // and the other rows' results are read after this
+                }
+            }
+            __syncthreads();
+            if (s_last) expand_request(ea, req, tid, esm, true, true);
+        }
     }
 }
 
@@ -347,7 +367,7 @@ int sms_of_current_device() {
 
 template <typename T>
 cudaError_t launch_typed(const T *logits, int32_t rows, int32_t V, int64_t ld, int32_t k, int32_t *ids,
-                         float *vals, float *lse, cudaStream_t st) {
+                         float *vals, float *lse, cudaStream_t st, const FusedExpand *fx = nullptr) {
     constexpr int EPV = 16 / sizeof(T);
     // about two vectors per thread per CTA, at most kMaxCluster CTAs, and no more CTAs than two
     // per SM in all (a power of two)
@@ -358,8 +378,16 @@ cudaError_t launch_typed(const T *logits, int32_t rows, int32_t V, int64_t ld, i
     if (c > kMaxCluster) c = kMaxCluster;
     unsigned C = 1;
     while (static_cast<int64_t>(C) * 2 <= c) C *= 2;
+    ExpandArgs ea{};
+    int32_t fx_rows = 0;
+    int32_t *fx_tickets = nullptr;
+    if (fx && fx->args) {
+        ea = *fx->args;
+        fx_rows = fx->rows_per_req;
+        fx_tickets = fx->tickets;
+    }
     return launch_pdl_cluster(row_topk_kernel<T>, dim3(static_cast<unsigned>(rows) * C), dim3(kThreads), C, 0,
-                              st, logits, V, ld, k, ids, vals, lse);
+                              st, logits, V, ld, k, ids, vals, lse, ea, fx_rows, fx_tickets);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -756,7 +784,9 @@ bool stream_suits(const void *logits, int32_t esize, int32_t rows, int32_t V, in
 }  // namespace
 
 cudaError_t launch_row_topk(const void *logits, int32_t is_bf16, int32_t rows, int32_t V, int64_t ld,
-                            int32_t k, int32_t *ids, float *vals, float *lse, cudaStream_t st, int32_t *status) {
+                            int32_t k, int32_t *ids, float *vals, float *lse, cudaStream_t st, int32_t *status,
+                            const FusedExpand *fx, bool *fused) {
+    if (fused) *fused = false;
     if (rows < 1) return cudaSuccess;
     if (k >= 1 && k <= 16 && stream_suits(logits, is_bf16 ? 2 : 4, rows, V, ld, k == 1 && lse == nullptr)) {
         if (is_bf16)
@@ -764,9 +794,14 @@ cudaError_t launch_row_topk(const void *logits, int32_t is_bf16, int32_t rows, i
                                  status, st);
         return launch_stream(reinterpret_cast<const float *>(logits), rows, V, ld, k, ids, vals, lse, status, st);
     }
+    // the cluster kernel: it can run the level's expand (rows with logsumexp only)
+    const bool fuse = fx && fx->args && lse != nullptr && fx->rows_per_req > 0 && fx->tickets != nullptr;
+    if (fused) *fused = fuse;
     if (is_bf16)
-        return launch_typed(reinterpret_cast<const __nv_bfloat16 *>(logits), rows, V, ld, k, ids, vals, lse, st);
-    return launch_typed(reinterpret_cast<const float *>(logits), rows, V, ld, k, ids, vals, lse, st);
+        return launch_typed(reinterpret_cast<const __nv_bfloat16 *>(logits), rows, V, ld, k, ids, vals, lse, st,
+                            fuse ? fx : nullptr);
+    return launch_typed(reinterpret_cast<const float *>(logits), rows, V, ld, k, ids, vals, lse, st,
+                        fuse ? fx : nullptr);
 }
 
 }  // namespace eagle

@@ -14,6 +14,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "expand.cuh"
 #include "kernels.cuh"
 
 namespace eagle {
@@ -31,65 +32,12 @@ __device__ __forceinline__ int32_t cand_depth(int32_t c, int32_t k) {
 constexpr int kExpandThreads = 256;
 
 __global__ void __launch_bounds__(kExpandThreads) expand_kernel(const ExpandArgs a) {
-    __shared__ float sS[256];
-    __shared__ int32_t sTok[256], sRow[256], sC[256];
-    __shared__ int32_t slot[16];
+    __shared__ ExpandSmem sm;
     pdl_launch_dependents();  // dependents still wait for this grid to finish
     pdl_wait();
-    const int32_t b = blockIdx.x, t = threadIdx.x, k = a.k, kk = a.k * a.k;
-    const int32_t nl = (a.level == 0) ? k : kk;
-    if (t < nl) {
-        int32_t tok, row, par, c;
-        float S;
-        if (a.level == 0) {
-            row = b;
-            tok = a.row_ids[static_cast<int64_t>(b) * k + t];
-            S = a.row_logp[static_cast<int64_t>(b) * k + t];
-            par = -1;
-            c = t;
-        } else {
-            const int32_t s = t / k, j = t - (t / k) * k;
-            row = b * k + s;
-            tok = a.row_ids[static_cast<int64_t>(row) * k + j];
-            S = a.front_S_in[b * k + s] + a.row_logp[static_cast<int64_t>(row) * k + j];
-            par = a.front_cand_in[b * k + s];
-            c = k + (a.level - 1) * kk + t;
-            // the frontier holds candidates of the previous level
-            if (!dcheck(par >= (a.level == 1 ? 0 : k + (a.level - 2) * kk) && par < k + (a.level - 1) * kk, a.status))
-                par = 0;
-        }
-        if (!dcheck(c < a.n_cand, a.status)) c = 0;
-        if (tok < 0 || tok >= a.V) {
-            latch(a.status, kDevBounds);
-            tok = 0;
-        }
-        sS[t] = S;
-        sTok[t] = tok;
-        sRow[t] = row;
-        sC[t] = c;
-        if (blockIdx.y == 0) {
-            const int64_t o = static_cast<int64_t>(b) * a.n_cand + c;
-            a.pool_tok[o] = tok;
-            a.pool_S[o] = S;
-            a.pool_parent[o] = par;
-            a.pool_row[o] = row;
-        }
-    }
-    if (a.front_cand_out == nullptr) return;  // last level: no next frontier
-    if (t < 16) slot[t] = 0;  // every slot is overwritten when the scores are finite
-    __syncthreads();
-    if (t < nl) {
-        int32_t rank = 0;
-        for (int32_t u = 0; u < nl; ++u) rank += ranks_before(sS[u], sC[u], sS[t], sC[t]) ? 1 : 0;
-        if (rank < k) slot[rank] = t;
-    }
-    __syncthreads();
-    if (t < k && !dcheck(slot[t] >= 0 && slot[t] < nl, a.status)) slot[t] = 0;  // every rank < k is taken
-    __syncthreads();
-    if (blockIdx.y == 0 && t < k) {
-        a.front_cand_out[b * k + t] = sC[slot[t]];
-        a.front_S_out[b * k + t] = sS[slot[t]];
-    }
+    const int32_t b = blockIdx.x, t = threadIdx.x, k = a.k;
+    if (!expand_request(a, b, t, sm, blockIdx.y == 0, false)) return;
+    const int32_t *slot = sm.slot, *sRow = sm.sRow, *sTok = sm.sTok;
     if (a.x_next == nullptr || a.fhat == nullptr) return;
     const int32_t eb = a.elem_bytes;
     const int32_t vpr = (2 * a.h * eb) / 16, vh = (a.h * eb) / 16;
