@@ -59,9 +59,13 @@ def parse_args():
                    help="wall-clock budget of the oracle's timed sample (all cores), per workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=100)
-    p.add_argument("--side-figures", choices=["all", "headline", "none"], default="all",
+    p.add_argument("--side-figures", choices=["all", "headline", "none", "decoder"], default="all",
                    help="workloads that also time extend rounds, static trees, sampling and "
-                        "greedy verification alone and the draft decoder layer")
+                        "greedy verification alone and the draft decoder layer (decoder: every "
+                        "measured workload times the draft decoder layer alone)")
+    p.add_argument("--decoder-requests", type=int, default=0,
+                   help="run the draft decoder layer figure on the first N requests of the step's "
+                        "tree (0: all of them); a smaller case for profiling its kernels")
     return p.parse_args()
 
 
@@ -355,7 +359,7 @@ def layer_dims(w):
 DECODER_PREFIX = 1024  # cached tokens per request in front of the tree
 
 
-def decoder_layer_figure(w, dev, tree_out, rank, calls=200):
+def decoder_layer_figure(w, dev, tree_out, rank, calls=200, requests=0):
     """The draft decoder layer over the step's tree: every node of every request, its mask and
     depth positions from the tree build, a DECODER_PREFIX-token KV cache per request.  Synthetic
     bf16 weights N(0, 1/sqrt(fan-in)), inputs and caches N(0, 1).  CUDA events over `calls` calls
@@ -367,6 +371,8 @@ def decoder_layer_figure(w, dev, tree_out, rank, calls=200):
         return None
     H, Hk, D, I = dims
     h, B, n, P = w.hidden, w.batch, w.num_nodes, DECODER_PREFIX
+    if 0 < requests < B:
+        B = requests
     gen = torch.Generator(device=dev)
     gen.manual_seed(4242 + rank)
     bf = lambda *shape, s=1.0: (torch.randn(*shape, generator=gen, device=dev) * s).to(torch.bfloat16)
@@ -375,8 +381,8 @@ def decoder_layer_figure(w, dev, tree_out, rank, calls=200):
                        bf(2 * I, h, s=h ** -0.5), bf(h, I, s=I ** -0.5), H, Hk)
     x = bf(B, n, h)
     kc, vc = bf(B, P, Hk, D), bf(B, P, Hk, D)
-    pos = (tree_out["positions"] + P).contiguous()
-    mask = tree_out["mask"].contiguous()
+    pos = (tree_out["positions"][:B] + P).contiguous()
+    mask = tree_out["mask"][:B].contiguous()
     out = torch.empty_like(x)
     for _ in range(5):
         lay(x, kc, vc, pos, mask, out=out, new_kv=True)
@@ -530,7 +536,20 @@ def e2e_figure(eng, w, sets_host, steps, ranks):
                    "tree and verify results copied out, stream synchronised"}
 
 
-def side_figures(eng, w, inp, sets, tree_out, ver_out, dev, rank, K):
+def decoder_only_figure(eng, w, sets, tree_out, ver_out, dev, rank, requests=0):
+    """The draft decoder layer figure alone (over the tree of input set 0)."""
+    feat0, tok0, T0 = sets[0][0], sets[0][1], sets[0][2]
+    eng.step(feat0, tok0, T0, tree_out=tree_out, verify_out=ver_out)
+    dec = decoder_layer_figure(w, dev, tree_out, rank, requests=requests)
+    if dec is not None:
+        peak, _ = hbm_peak()
+        tp, _ = tensor_peak()
+        dec["frac_of_hbm"] = dec["achieved_gbs"] / peak
+        dec["frac_of_bf16_sustained"] = dec["tflops"] / tp
+    return dec
+
+
+def side_figures(eng, w, inp, sets, tree_out, ver_out, dev, rank, K, decoder_requests=0):
     """Figures beside the step: extend rounds, an EAGLE-1 static tree, sampling and greedy
     verification alone, and the draft decoder layer over the step's tree."""
     import torch
@@ -640,7 +659,7 @@ def side_figures(eng, w, inp, sets, tree_out, ver_out, dev, rank, K):
 
     # the draft decoder layer over the step's tree
     eng.step(feat0, tok0, T0, tree_out=tree_out, verify_out=ver_out)
-    dec = decoder_layer_figure(w, dev, tree_out, rank)
+    dec = decoder_layer_figure(w, dev, tree_out, rank, requests=decoder_requests)
     if dec is not None:
         dec["frac_of_hbm"] = dec["achieved_gbs"] / peak
         tp, _ = tensor_peak()
@@ -823,7 +842,11 @@ def measure(args, w, dev, ranks, rank, local, headline):
         "gpu_launches": int(ranks.sum(round(launches_per_step * K))),
     }
     if args.side_figures == "all" or (args.side_figures == "headline" and headline):
-        entry.update(side_figures(eng, w, inp, sets, tree_out, ver_out, dev, rank, K))
+        entry.update(side_figures(eng, w, inp, sets, tree_out, ver_out, dev, rank, K,
+                                  args.decoder_requests))
+    elif args.side_figures == "decoder":
+        entry["draft_decoder_layer"] = decoder_only_figure(eng, w, sets, tree_out, ver_out, dev, rank,
+                                                           args.decoder_requests)
     eng.close()
     if rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
         entry["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds, one_thread=headline)

@@ -19,7 +19,7 @@
 //               every CTA covers a whole tile, by the CTA that reaches the tile at the end of its
 //               range and finds its partner's ticket in (the partner's partial bulk-copied into
 //               its idle ring, its own values straight from TMEM), else by a second launch;
-//   bulk stores above 16 rows every 16-row group of outputs or partials is assembled in shared
+//   bulk stores above 16 rows every 32-row group of outputs or partials is assembled in shared
 //               memory and leaves by one bulk store (TMA tensor store into Y, 1-D bulk store of
 //               partials) instead of per-thread stores to rows far apart;
 //   CTA pairs   above 16 rows, with an even number of weight tiles, the CTAs run as
@@ -51,7 +51,8 @@ constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB weight tile
 constexpr int kMaxStages = 16;
 constexpr int kThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
 constexpr size_t kMaxDynSmem = 232448;  // 227 KB per CTA on sm_100-class parts
-constexpr uint32_t kGroupBytes = 16u * BM * 4u;  // one 16-row group of a 128-wide tile in fp32
+constexpr int kGroupRows = 32;  // rows of one bulk-stored group of outputs or partials
+constexpr uint32_t kGroupBytes = kGroupRows * BM * 4u;  // one group of a 128-wide tile in fp32
 constexpr uint32_t kOutStageBytes = 2u * kGroupBytes;  // two staging buffers for bulk stores
 
 struct SmemCtl {
@@ -79,7 +80,7 @@ struct LinearArgs {
     int32_t slots;      // partial-sum slots of the launch: two per CTA of the main kernel
     int32_t num_wtiles; // weight units: tiles, or pairs of tiles
     int32_t num_chunks; // row chunks of n_tile rows; the split's units are (weight unit, chunk)
-    int32_t y_tma;      // 16-row groups of Y and of partials go out by bulk stores (tmap_y valid)
+    int32_t y_tma;      // 32-row groups of Y and of partials go out by bulk stores (tmap_y valid)
     int32_t out_stage_bytes;  // shared-memory staging of those groups (after the ring)
     float *partials;
     int32_t *counters;
@@ -115,12 +116,12 @@ __device__ __forceinline__ void store_y(const LinearArgs &a, int32_t r, int32_t 
         reinterpret_cast<float *>(a.out)[static_cast<int64_t>(r) * a.ldo + o] = v;
 }
 
-// Writes rows n0 .. n0 + 15 of this thread's column (m_local) of a 128-wide tile through one of two
+// Writes rows n0 .. n0 + 31 of this thread's column (m_local) of a 128-wide tile through one of two
 // shared-memory staging buffers; thread et 0 sends the group with one bulk store: a TMA tensor
 // store into Y (to_y: rows and columns outside Y are dropped; bf16 when Y is bf16) or a 1-D bulk
 // store of the rows into the partial slot `part` (fp32, [row][128]).  All 128 epilogue threads.
 __device__ __forceinline__ void group_store(const LinearArgs &a, const CUtensorMap *tmap_y, uint8_t *out_stage,
-                                            int32_t &gi, int32_t et, int32_t m_local, const float (&v)[16],
+                                            int32_t &gi, int32_t et, int32_t m_local, const float (&v)[kGroupRows],
                                             bool to_y, float *part, int32_t tile, int32_t n0, int32_t row0,
                                             int32_t rows_c) {
     uint8_t *buf = out_stage + static_cast<size_t>(gi & 1) * kGroupBytes;
@@ -129,11 +130,11 @@ __device__ __forceinline__ void group_store(const LinearArgs &a, const CUtensorM
     if (to_y && a.out_bf16) {
         __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(buf);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) ob[j * BM + m_local] = __float2bfloat16_rn(v[j]);
+        for (int j = 0; j < kGroupRows; ++j) ob[j * BM + m_local] = __float2bfloat16_rn(v[j]);
     } else {
         float *ob = reinterpret_cast<float *>(buf);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) ob[j * BM + m_local] = v[j];
+        for (int j = 0; j < kGroupRows; ++j) ob[j * BM + m_local] = v[j];
     }
     fence_proxy_async_smem();  // the writes above, before the bulk store reads them
     named_barrier_sync(1, 128);
@@ -142,7 +143,7 @@ __device__ __forceinline__ void group_store(const LinearArgs &a, const CUtensorM
             tma_store_2d(tmap_y, buf, tile * BM, row0 + n0);
         else
             bulk_store(part + static_cast<size_t>(n0) * BM, buf,
-                       static_cast<uint32_t>(min(16, rows_c - n0)) * BM * 4u);
+                       static_cast<uint32_t>(min(kGroupRows, rows_c - n0)) * BM * 4u);
         bulk_commit();
     }
     ++gi;
@@ -162,10 +163,10 @@ __device__ __forceinline__ bool staged_fixup(const LinearArgs &a, const CUtensor
                                              volatile int32_t *abort_flag) {
     const int32_t np = gl - gf;  // partials read from global memory
     const uint32_t row_bytes = BM * 4u;
-    int32_t cr = static_cast<int32_t>(ring_bytes / (static_cast<uint32_t>(np) * row_bytes)) & ~15;
+    int32_t cr = static_cast<int32_t>(ring_bytes / (static_cast<uint32_t>(np) * row_bytes)) & ~(kGroupRows - 1);
     cr = min(cr, a.n_tile);
     const int32_t nch = (rows_c + cr - 1) / cr;
-    cr = (((rows_c + nch - 1) / nch) + 15) & ~15;
+    cr = (((rows_c + nch - 1) / nch) + kGroupRows - 1) & ~(kGroupRows - 1);
     const float *staged = reinterpret_cast<const float *>(ring);
     for (int32_t c = 0; c < nch; ++c) {
         const int32_t r0 = c * cr, rc = min(cr, rows_c - r0);
@@ -192,41 +193,41 @@ __device__ __forceinline__ bool staged_fixup(const LinearArgs &a, const CUtensor
         }
         named_barrier_sync(1, 128);
         if (*abort_flag) return false;
-        for (int32_t n0 = r0; n0 < r0 + rc; n0 += 16) {
-            uint32_t r[16];
+        for (int32_t n0 = r0; n0 < r0 + rc; n0 += kGroupRows) {
+            uint32_t r[kGroupRows];
             __syncwarp();
-            tmem_ld_16(t_row + static_cast<uint32_t>(n0), r);
+            tmem_ld_32(t_row + static_cast<uint32_t>(n0), r);
             tmem_wait_ld();
-            // 16 rows at a time: every load of the group, then every add, then every store
+            // a group at a time: every load of the group, then every add, then every store
             const float *src0 = staged + static_cast<size_t>(n0 - r0) * BM + m_local;
-            float sum[16];
+            float sum[kGroupRows];
             int32_t pi = 0;
             for (int32_t gg = gf; gg <= gl; ++gg) {
-                float v[16];
+                float v[kGroupRows];
                 if (gg == self) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+                    for (int j = 0; j < kGroupRows; ++j) v[j] = __uint_as_float(r[j]);
                 } else {
                     const float *src = src0 + static_cast<size_t>(pi) * cr * BM;  // rows of the chunk
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = src[static_cast<size_t>(j) * BM];
+                    for (int j = 0; j < kGroupRows; ++j) v[j] = src[static_cast<size_t>(j) * BM];
                     ++pi;
                 }
                 if (gg == gf) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) sum[j] = v[j];
+                    for (int j = 0; j < kGroupRows; ++j) sum[j] = v[j];
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) sum[j] += v[j];
+                    for (int j = 0; j < kGroupRows; ++j) sum[j] += v[j];
                 }
             }
             if (a.y_tma) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) sum[j] += bias_o;
+                for (int j = 0; j < kGroupRows; ++j) sum[j] += bias_o;
                 group_store(a, tmap_y, out_stage, gi, et, m_local, sum, true, nullptr, tile, n0, row0, rows_c);
             } else if (o_ok) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
+                for (int j = 0; j < kGroupRows; ++j)
                     if (n0 + j < r0 + rc) store_y(a, row0 + n0 + j, o, sum[j] + bias_o);
             }
         }
@@ -437,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t m_local = q * 32 + lane;
         uint32_t acc = 0, acc_phase = 0;
         bool first = true;
-        int32_t gi = 0;  // 16-row groups sent by bulk stores
+        int32_t gi = 0;  // 32-row groups sent by bulk stores
         for (int64_t kb = kb_begin; kb < kb_end;) {
             const int32_t unit = static_cast<int32_t>(div_nonneg(kb, nkb));
             const int32_t wu = nch == 1 ? unit : unit / nch, chunk = unit - wu * nch;
@@ -467,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 gf = cta_of(t0, total, G);
                 gl = cta_of(t0 + nkb - 1, total, G);
                 if (a.owner_fix) {
-                    const bool fits = static_cast<uint32_t>(gl - gf) * 16u * BM * 4u <= ring_bytes;
+                    const bool fits = static_cast<uint32_t>(gl - gf) * kGroupRows * BM * 4u <= ring_bytes;
                     if (threadIdx.x == 64)  // acquire: the other CTAs' partials, for the copies
                         ctl->is_last = (got && !*abort_flag && fits && k1 == kb_end &&
                                         ld_acquire_gpu(&a.counters[ticket]) == gl - gf) ? 1 : 0;
@@ -490,28 +491,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        acc * static_cast<uint32_t>(a.n_tile);
                 float *part = part_slot(a, g, first ? 0 : 1, rank);
-                for (int32_t n0 = 0; n0 < rows_c; n0 += 16) {
-                    uint32_t r[16];
-                    __syncwarp();
-                    tmem_ld_16(t_row + static_cast<uint32_t>(n0), r);
-                    tmem_wait_ld();
-                    if (a.y_tma) {  // a whole tile into Y, or this CTA's partial
-                        float v[16];
+                if (a.y_tma) {  // a whole tile into Y, or this CTA's partial, in 32-row groups
+                    for (int32_t n0 = 0; n0 < rows_c; n0 += kGroupRows) {
+                        uint32_t r[kGroupRows];
+                        __syncwarp();
+                        tmem_ld_32(t_row + static_cast<uint32_t>(n0), r);
+                        tmem_wait_ld();
+                        float v[kGroupRows];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) + (full ? bias_o : 0.0f);
+                        for (int j = 0; j < kGroupRows; ++j) v[j] = __uint_as_float(r[j]) + (full ? bias_o : 0.0f);
                         group_store(a, &tmap_y, out_stage, gi, threadIdx.x - 64, m_local, v, full, part, tile, n0,
                                     row0, rows_c);
-                        continue;
                     }
+                } else {
+                    for (int32_t n0 = 0; n0 < rows_c; n0 += 16) {
+                        uint32_t r[16];
+                        __syncwarp();
+                        tmem_ld_16(t_row + static_cast<uint32_t>(n0), r);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int32_t n = n0 + j;
-                        if (n < rows_c) {
-                            const float v = __uint_as_float(r[j]);
-                            if (full) {
-                                if (o_ok) store_y(a, row0 + n, o, v + bias_o);
-                            } else {
-                                part[static_cast<size_t>(n) * BM + m_local] = v;
+                        for (int j = 0; j < 16; ++j) {
+                            const int32_t n = n0 + j;
+                            if (n < rows_c) {
+                                const float v = __uint_as_float(r[j]);
+                                if (full) {
+                                    if (o_ok) store_y(a, row0 + n, o, v + bias_o);
+                                } else {
+                                    part[static_cast<size_t>(n) * BM + m_local] = v;
+                                }
                             }
                         }
                     }
@@ -828,10 +835,10 @@ bool encode_out_2d(CUtensorMap *map, const void *ptr, int32_t out_bf16, uint64_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The output map of a plan: {128, 16} boxes for the epilogue's 16-row groups.
+// The output map of a plan: {128, 32} boxes for the epilogue's 32-row groups.
 bool encode_plan_out(LinearPlan *p, const void *out) {
     return encode_out_2d(&p->tmap_y, out, p->out_bf16, static_cast<uint64_t>(p->M), static_cast<uint64_t>(p->rows),
-                         static_cast<uint64_t>(p->ldo), BM, 16u);
+                         static_cast<uint64_t>(p->ldo), BM, static_cast<uint32_t>(kGroupRows));
 }
 
 }  // namespace
@@ -899,7 +906,7 @@ bool plan_linear_bf16(LinearPlan *p, const void *w, int64_t ldw, int32_t M, int3
         }
     }
     const size_t stage_bytes = kABytes + static_cast<size_t>(p->n_tile >> p->pair) * 128;
-    // above 16 rows (stream-K), outputs and partials leave in 16-row groups by bulk stores
+    // above 16 rows (stream-K), outputs and partials leave in 32-row groups by bulk stores
     const bool want_y_tma = rows > kLinearMaxFixupRows;
     p->out_stage_bytes = want_y_tma ? static_cast<int32_t>(kOutStageBytes) : 0;
     size_t stages = (kMaxDynSmem - 1024 - sizeof(SmemCtl) - p->out_stage_bytes) / stage_bytes;

@@ -78,7 +78,7 @@ constexpr int kLinearMaxFixupRows = 16;  // above this, split tiles are summed b
 struct LinearPlan {
     CUtensorMap tmap_w;  // W [M][K] bf16, box {64, 128}, 128-byte swizzle
     CUtensorMap tmap_x;  // X [rows][K] bf16, box {64, n_tile}, 128-byte swizzle
-    CUtensorMap tmap_y;  // Y [rows][ldo], box {128, 16}, no swizzle (valid when y_tma)
+    CUtensorMap tmap_y;  // Y [rows][ldo], box {128, 32}, no swizzle (valid when y_tma)
     int32_t M, K, rows, n_tile, num_kb, num_tiles, stages, tmem_cols, grid;
     size_t smem_bytes;
     const void *bias;  // [M] bf16 or null
