@@ -174,7 +174,7 @@ def teacher_forced_check(inp, w, gpu, b, logits_rows, T_b, ver_b, pos_base, rec)
 
     Every draft row's input [f^ of the row that produced its node || E[token]] is taken from the
     GPU's intermediate state, so each comparison sees one level's arithmetic only (no drift
-    carried from earlier levels), and the benchmark spec's rule applies as written: a decision may differ
+    carried from earlier levels), and the parity rule applies as written: a decision may differ
     only where its margin is at most 1e-3.  Checked per row: f^ against the oracle's FC (equal
     up to one bf16 rounding step, i.e. one ulp, in at most 1% of the elements), the logits against
     the oracle's LM head on the GPU's f^ (2e-2 absolute for bf16, 1e-4 relative for fp32), the top-k

@@ -17,7 +17,7 @@ Two comparisons per checked request:
   within tolerance.  Whole trees rarely agree at bf16 (see the floors below), so this comparison is
   recorded rather than floored, except for the fp32 workload and the SGLang shape.
 * teacher-forced: each level is checked against the oracle fed the GPU's own inputs to that level,
-  so there is no drift and the benchmark spec's rule holds as written: every decision identical wherever
+  so there is no drift and the parity rule holds as written: every decision identical wherever
   its margin exceeds 1e-3, frontier, rerank, tree and verify bit-exact (parity.teacher_forced_check).
   Nearly every checked request must come out whole (no decision differing at all).
 
